@@ -1,0 +1,244 @@
+"""fp64 CPU oracle for Cut Cross-Entropy (linear cross-entropy).
+
+TEST INFRASTRUCTURE ONLY.  This package is imported by the tests, by
+``__graft_entry__.smoke()`` and by ``bench.py``'s CPU-baseline / reference
+legs, and by nothing else.  The product path (``linear_cross_entropy_gb300``)
+never imports it, and this package imports nothing from the product: the two
+share only the seeded input generator ``cce_workloads``.
+
+What it computes is the plain definition of the loss and its gradient, in
+float64, from the bf16-rounded inputs widened exactly to float64:
+
+* logits            a_iv = sum_d E_id C_vd            (one library matmul)
+* log-sum-exp       LSE_i = m_i + log sum_v exp(a_iv - m_i),  m_i = max_v a_iv
+* loss              loss_i = LSE_i - a_{i, x_i}
+* logit gradient    G_iv = exp(a_iv - LSE_i) - [v = x_i]
+* input gradients   dE_i = w_i sum_v G_iv C_v ,   dC_v = sum_i w_i G_iv E_i
+
+Passages followed (page title, section):
+
+* "Cut Cross-Entropy: Training Loss Without the Logit Matrix, and Why 0.1%
+  Element Sparsity Becomes 50% Block Sparsity" -- section "The decomposition"
+  (loss = LSE - target logit; backward G = S - onehot, dE = G C, dC = G^T E);
+  section "Gradient filtering: the part that makes it fast" (a tile is
+  skipped when every |G| < eps, eps = 2^-12, tested on |S - onehot|).
+* "Cut Your Losses in Large-Vocabulary Language Models" -- "The Mathematical
+  Decomposition" (the loss splits into an indexed logit and a log-sum-exp),
+  "Memory-Efficient Linear-Log-Sum-Exp, Backward Pass (Algorithm 3)",
+  "The Combined Backward Pass (Algorithm 4)".  That page writes the
+  log-likelihood (target - LSE) and G = onehot - S; the loss here is its
+  negative, LSE - target, whose gradient is S - onehot (the first page's
+  sign).
+* "cut-cross-entropy" kernel card -- "Correctness": ignore_index rows add no
+  loss and get exactly zero gradient; a fully masked batch has zero loss and
+  zero gradients; reductions none / sum / mean.
+* Reading where the pages are silent: mean divides by the number of
+  non-ignored rows, clamped to at least 1 (the chunked-CE code on the
+  "fused-linear-cross-entropy" page clamps the count the same way); the LSE of
+  an ignored row is still the true LSE of its logits.
+
+The gradient weights w_i follow from the reduction: w_i = g (sum),
+g / max(count, 1) (mean), g_i (none), and 0 on ignored rows, where g is the
+incoming gradient of the reduced loss.
+
+Pins (tests/test_oracle_pins.py): closed forms (C = 0 gives loss = log V;
+N = 1, V = 2 gives a softplus), central finite differences of the loss for dE
+and dC, torch.nn.functional.cross_entropy on materialised fp64 logits,
+row sums of G equal to zero, vocabulary-permutation invariance, the
+pigeonhole bound on entries >= 2^-12 and the eps tie case.  Every function
+below is pinned by at least one of them.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+IGNORE_INDEX = -100
+FILTER_EPS = 2.0 ** -12  # finfo(bf16).eps / 32
+
+_ROW_BLOCK_BYTES = 1 << 28  # memory bound for one block of dense logit rows
+
+
+def widen_bf16(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> float64, exactly."""
+    u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return u.view(np.float32).astype(np.float64)
+
+
+def _row_blocks(n_rows: int, V: int):
+    step = max(1, _ROW_BLOCK_BYTES // (8 * max(V, 1)))
+    for r0 in range(0, n_rows, step):
+        yield r0, min(n_rows, r0 + step)
+
+
+def logits(E: np.ndarray, C: np.ndarray) -> np.ndarray:
+    """a = E C^T for the given rows of E (float64 matmul)."""
+    return E @ C.T
+
+
+def log_sum_exp(A: np.ndarray) -> np.ndarray:
+    """Row-wise LSE_i = m_i + log sum_v exp(a_iv - m_i)."""
+    m = A.max(axis=1)
+    return m + np.log(np.exp(A - m[:, None]).sum(axis=1))
+
+
+def forward(E, C, x, ignore_index=IGNORE_INDEX, reduction="mean", rows=None):
+    """Forward pass for the listed rows (all rows when rows is None).
+
+    Returns a dict with per-row ``lse``, ``target_logit`` (NaN on ignored
+    rows), ``loss_rows`` (0 on ignored rows) and, when all rows were
+    computed, ``count`` (non-ignored rows) and the reduced ``loss``.
+    """
+    E = np.asarray(E, np.float64)
+    C = np.asarray(C, np.float64)
+    x = np.asarray(x, np.int64)
+    V = C.shape[0]
+    idx = np.arange(E.shape[0]) if rows is None else np.asarray(rows, np.int64)
+    lse = np.empty(len(idx))
+    tgt = np.full(len(idx), np.nan)
+    for r0, r1 in _row_blocks(len(idx), V):
+        rr = idx[r0:r1]
+        A = logits(E[rr], C)
+        lse[r0:r1] = log_sum_exp(A)
+        xr = x[rr]
+        ok = xr != ignore_index
+        if np.any(ok & ((xr < 0) | (xr >= V))):
+            raise ValueError("target out of range")
+        sel = np.nonzero(ok)[0]
+        tgt[r0 + sel] = A[sel, xr[sel]]
+    valid = x[idx] != ignore_index
+    loss_rows = np.where(valid, lse - np.where(valid, tgt, 0.0), 0.0)
+    out = {"lse": lse, "target_logit": tgt, "loss_rows": loss_rows}
+    if rows is None:
+        count = int(valid.sum())
+        out["count"] = count
+        out["loss"] = reduce_loss(loss_rows, count, reduction)
+    return out
+
+
+def reduce_loss(loss_rows, count, reduction):
+    """none -> the rows; sum -> their sum; mean -> sum / max(count, 1)."""
+    if reduction == "none":
+        return np.asarray(loss_rows, np.float64)
+    s = float(np.sum(loss_rows))
+    if reduction == "sum":
+        return s
+    if reduction == "mean":
+        return s / max(count, 1)
+    raise ValueError(reduction)
+
+
+def row_weights(x, ignore_index, reduction, grad_out, count=None):
+    """w_i: the factor multiplying row i's logit gradient."""
+    x = np.asarray(x, np.int64)
+    valid = x != ignore_index
+    if reduction == "none":
+        g = np.broadcast_to(np.asarray(grad_out, np.float64), x.shape)
+        return np.where(valid, g, 0.0)
+    g = float(np.asarray(grad_out, np.float64).reshape(()))
+    if reduction == "sum":
+        return np.where(valid, g, 0.0)
+    if reduction == "mean":
+        n = int(valid.sum()) if count is None else int(count)
+        return np.where(valid, g / max(n, 1), 0.0)
+    raise ValueError(reduction)
+
+
+def grad_logits(A, lse, x_rows, v0=0, ignore_index=IGNORE_INDEX):
+    """G = exp(A - LSE) - onehot(x) for a block of logits.
+
+    A holds rows (tokens) x columns v0 .. v0 + A.shape[1] - 1 of the logit
+    matrix; ignored rows are all zero.
+    """
+    G = np.exp(A - np.asarray(lse)[:, None])
+    x_rows = np.asarray(x_rows, np.int64)
+    r = np.nonzero((x_rows >= v0) & (x_rows < v0 + A.shape[1]))[0]
+    G[r, x_rows[r] - v0] -= 1.0
+    G[x_rows == ignore_index] = 0.0
+    return G
+
+
+def backward_dE(E, C, x, lse_rows, w_rows, rows, ignore_index=IGNORE_INDEX):
+    """dE_i = w_i sum_v G_iv C_v for the listed rows (lse/w given per listed row)."""
+    E = np.asarray(E, np.float64)
+    C = np.asarray(C, np.float64)
+    rows = np.asarray(rows, np.int64)
+    out = np.empty((len(rows), E.shape[1]))
+    for r0, r1 in _row_blocks(len(rows), C.shape[0]):
+        rr = rows[r0:r1]
+        G = grad_logits(logits(E[rr], C), lse_rows[r0:r1], x[rr], 0, ignore_index)
+        out[r0:r1] = np.asarray(w_rows[r0:r1])[:, None] * (G @ C)
+    return out
+
+
+def backward_dC(E, C, x, lse, w, vrows, ignore_index=IGNORE_INDEX):
+    """dC_v = sum_i w_i G_iv E_i for the listed vocabulary rows.
+
+    Needs LSE and w for every token row i.
+    """
+    E = np.asarray(E, np.float64)
+    C = np.asarray(C, np.float64)
+    x = np.asarray(x, np.int64)
+    vrows = np.asarray(vrows, np.int64)
+    A = logits(E, C[vrows])                      # [N, len(vrows)]
+    G = np.exp(A - np.asarray(lse)[:, None])
+    G -= (x[:, None] == vrows[None, :]).astype(np.float64)
+    G[x == ignore_index] = 0.0
+    return (np.asarray(w)[:, None] * G).T @ E
+
+
+def backward(E, C, x, lse, w, ignore_index=IGNORE_INDEX):
+    """Full dE [N, D] and dC [V, D] (small problems: materialises G)."""
+    E = np.asarray(E, np.float64)
+    C = np.asarray(C, np.float64)
+    G = grad_logits(logits(E, C), lse, x, 0, ignore_index)
+    Gw = np.asarray(w)[:, None] * G
+    return Gw @ C, Gw.T @ E
+
+
+def tile_survival(E, C, x, lse, BN, BV, eps=FILTER_EPS, ignore_index=IGNORE_INDEX):
+    """Filter decision per (BN x BV) tile: True when some in-range entry has
+    |G_iv| >= eps (unscaled G; ignored rows contribute nothing)."""
+    E = np.asarray(E, np.float64)
+    C = np.asarray(C, np.float64)
+    return tile_keep(grad_logits(logits(E, C), lse, x, 0, ignore_index), BN, BV, eps)
+
+
+def tile_keep(G, BN, BV, eps=FILTER_EPS):
+    """Survival of each (BN x BV) tile of a logit-gradient matrix G: the tile
+    is skipped iff every |G| < eps, so an entry equal to eps keeps it."""
+    G = np.abs(np.asarray(G))
+    nbn, nbv = -(-G.shape[0] // BN), -(-G.shape[1] // BV)
+    keep = np.zeros((nbn, nbv), dtype=bool)
+    for a in range(nbn):
+        for b in range(nbv):
+            keep[a, b] = bool(np.any(G[a * BN:(a + 1) * BN, b * BV:(b + 1) * BV] >= eps))
+    return keep
+
+
+def backward_filtered(E, C, x, lse, w, BN, BV, eps=FILTER_EPS, ignore_index=IGNORE_INDEX):
+    """dE, dC with the contributions of skipped tiles removed; also returns
+    the survival map.  With eps = 0 no tile is skipped."""
+    E = np.asarray(E, np.float64)
+    C = np.asarray(C, np.float64)
+    G = grad_logits(logits(E, C), lse, x, 0, ignore_index)
+    keep = tile_survival(E, C, x, lse, BN, BV, eps, ignore_index)
+    mask = np.repeat(np.repeat(keep, BN, axis=0), BV, axis=1)[:G.shape[0], :G.shape[1]]
+    Gw = np.asarray(w)[:, None] * np.where(mask, G, 0.0)
+    return Gw @ C, Gw.T @ E, keep
+
+
+def from_bits(E_bits, C_bits):
+    """Widen the bf16 inputs of a workload to float64 (E, C)."""
+    return widen_bf16(E_bits), widen_bf16(C_bits)
+
+
+def fwd_bwd_rows(E, C, x, rows, ignore_index=IGNORE_INDEX, reduction="mean", grad_out=1.0):
+    """Forward + backward of the sub-problem made of the listed token rows
+    (a standalone batch): returns (loss, dE_rows, dC).  Used to time the
+    oracle on a bounded sample of a workload."""
+    rows = np.asarray(rows, np.int64)
+    Es, xs = np.asarray(E)[rows], np.asarray(x)[rows]
+    f = forward(Es, C, xs, ignore_index, reduction)
+    w = row_weights(xs, ignore_index, reduction, grad_out, f["count"])
+    dE, dC = backward(Es, C, xs, f["lse"], w, ignore_index)
+    return f["loss"], dE, dC
