@@ -278,3 +278,22 @@ def small(name: str, N: int, D: int, V: int, **kw) -> Workload:
     base = dict(c_scale=4.0, targets="zipf", boost=3.0, ignore_frac=0.05, reduction="mean")
     base.update(kw)
     return Workload(name, N, D, V, **base)
+
+
+def frequent_token_inputs(N: int, D: int, V: int, n_freq: int = 256, seed: int = 0,
+                          ignore_frac: float = 0.05):
+    """A supplementary workload where the gradient filter bites: the n_freq
+    lowest ids are "frequent tokens" with large classifier rows (as byte-pair
+    merge order puts frequent tokens at low ids), every other row is small,
+    and targets are drawn uniformly among the frequent ids.  Softmax mass then
+    sits in the first n_freq columns, so most 128 x 128 tiles are skippable.
+    Returns (E_bits, C_bits, x)."""
+    g = _gen(seed, 7)
+    big = normal_bf16(seed, 8, n_freq * D, 6.0 / math.sqrt(D))
+    small = normal_bf16(seed, 9, (V - n_freq) * D, 0.5 / math.sqrt(D))
+    C_bits = np.concatenate([big, small]).reshape(V, D)
+    E_bits = normal_bf16(seed, 10, N * D, 1.0).reshape(N, D)
+    x = g.integers(0, n_freq, size=N, dtype=np.int64)
+    u = _uniform_open(_gen(seed, 11), N)
+    x = np.where(u < ignore_frac, np.int64(IGNORE_INDEX), x)
+    return E_bits, C_bits, x

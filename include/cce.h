@@ -1,0 +1,175 @@
+/*
+ * cce.h -- C ABI of the GB300 (sm_103a) Cut Cross-Entropy library.
+ *
+ * The operation is the classifier-head matmul fused with cross-entropy over a
+ * large vocabulary, computed forward and backward without ever writing the
+ * N x V logit matrix to device memory:
+ *
+ *   loss_i = LSE_i - C[x_i] . E_i,   LSE_i = log sum_v exp(C_v . E_i)
+ *
+ * ("Cut Your Losses in Large-Vocabulary Language Models", section "The
+ * Mathematical Decomposition"; "Cut Cross-Entropy: Training Loss Without the
+ * Logit Matrix ...", section "The decomposition").  The backward pass
+ * recomputes the logits tile by tile, forms G = softmax - onehot(x) and
+ * contracts it into dE = G C and dC = G^T E ("Cut Your Losses ...", sections
+ * "Memory-Efficient Linear-Log-Sum-Exp, Backward Pass (Algorithm 3)" and
+ * "The Combined Backward Pass (Algorithm 4)"), skipping tiles whose every
+ * |G| < filter_eps ("Gradient Filtering").
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Layouts: E [N, D] bf16, C [V, D] bf16, dE [N, D] bf16, dC [V, D] bf16,
+ *   all row-major and dense (row pitch D elements); x [N] int64; lse [N] fp32.
+ *   bf16 buffers are passed as void* (raw 16-bit IEEE bfloat16 values).
+ * - Every pointer is a DEVICE pointer of the current CUDA device unless its
+ *   comment says host.  The caller owns every buffer, including the
+ *   workspace; the library allocates no device memory.
+ * - Requirements checked synchronously, before anything is launched:
+ *   non-null pointers; 1 <= N, V < 2^31; 1 <= D < 2^31 with D % 8 == 0 (16-byte
+ *   row pitch for TMA); E, C, dE, dC, lse, loss and workspace 16-byte aligned;
+ *   ws_bytes >= the matching *_workspace_bytes(); a valid reduction; a finite
+ *   filter_eps >= 0; current device of compute capability 10.3.  A failed check
+ *   returns its status and launches nothing.
+ * - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default
+ *   stream).  Outputs are overwritten, never accumulated into.
+ * - Targets: x_i must lie in [0, V) or equal ignore_index.  Rows with
+ *   x_i == ignore_index add no loss and receive exactly zero gradient
+ *   ("cut-cross-entropy" kernel card, section "Correctness").  An out-of-range
+ *   target does not cause an out-of-bounds access: the row is treated as
+ *   ignored and CCE_DEVERR_TARGET_RANGE is OR-ed into *dev_err, which the
+ *   caller reads after synchronising (the Python binding raises on it).
+ * - Device error word (*dev_err, int32, device memory, optional: NULL allowed):
+ *   bits are only ever OR-ed in; the caller zeroes it.
+ *     CCE_DEVERR_TARGET_RANGE  a target was outside [0, V) and not ignored
+ *     CCE_DEVERR_TIMEOUT       a pipeline wait inside a kernel ran out (a
+ *                              bug); the kernel returned early, outputs are
+ *                              undefined.
+ */
+#ifndef CCE_GB300_H
+#define CCE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CCE_OK = 0,
+  CCE_ERR_NULL = 1,         /* a required pointer is NULL */
+  CCE_ERR_SHAPE = 2,        /* N, D or V out of range, or D % 8 != 0 */
+  CCE_ERR_ALIGN = 3,        /* a buffer is not 16-byte aligned */
+  CCE_ERR_ARG = 4,          /* bad reduction or filter_eps */
+  CCE_ERR_WORKSPACE = 5,    /* ws_bytes smaller than the query */
+  CCE_ERR_DEVICE = 6,       /* current device is not compute capability 10.3 */
+  CCE_ERR_CUDA = 7,         /* a CUDA runtime/driver call failed */
+  CCE_ERR_TARGET_RANGE = 8, /* status form of CCE_DEVERR_TARGET_RANGE */
+  CCE_ERR_TIMEOUT = 9       /* status form of CCE_DEVERR_TIMEOUT */
+} cce_status;
+
+typedef enum { CCE_RED_NONE = 0, CCE_RED_SUM = 1, CCE_RED_MEAN = 2 } cce_reduction;
+
+#define CCE_DEVERR_TARGET_RANGE 1
+#define CCE_DEVERR_TIMEOUT 2
+
+/* Default gradient-filter threshold, finfo(bf16).eps / 32 = 2^-12
+ * ("Cut Cross-Entropy: Training Loss Without the Logit Matrix ...", section
+ * "Gradient filtering: the part that makes it fast"). */
+#define CCE_FILTER_EPS_DEFAULT 0.000244140625f
+
+/* Bytes of device workspace cce_forward / cce_backward need for these sizes
+ * (0 for invalid sizes).  Pure host arithmetic; needs no GPU. */
+size_t cce_forward_workspace_bytes(int64_t N, int64_t D, int64_t V);
+size_t cce_backward_workspace_bytes(int64_t N, int64_t D, int64_t V);
+
+/*
+ * Forward: linear-log-sum-exp with target capture ("Cut Your Losses ...",
+ * "Memory-Efficient Linear-Log-Sum-Exp, Forward Pass (Algorithm 2)" and
+ * "Memory-Efficient Indexed Matrix Multiplication (Algorithm 1)"; the
+ * running (max, sumexp) fold of the "cut-cross-entropy" card's "Method").
+ *
+ *   E, C, x       inputs as above.
+ *   ignore_index  target value of rows to ignore (PyTorch's default is -100).
+ *   reduction     CCE_RED_NONE: loss[i] = loss_i for all N rows (0 on ignored
+ *                 rows); CCE_RED_SUM: loss[0] = sum_i loss_i;
+ *                 CCE_RED_MEAN: loss[0] = sum_i loss_i / max(count, 1), count =
+ *                 number of non-ignored rows (a fully ignored batch gives 0).
+ *   loss          [N] fp32 for NONE, else [1] fp32 (written).
+ *   lse           [N] fp32 (written): LSE_i for every row, ignored rows too.
+ *                 Keep it for cce_backward.
+ *   workspace     >= cce_forward_workspace_bytes(N, D, V) bytes, scratch.
+ *   dev_err       optional device error word (see above).
+ * The result is deterministic: repeated calls give bitwise identical outputs.
+ */
+cce_status cce_forward(const void* E, const void* C, const int64_t* x, int64_t N, int64_t D, int64_t V,
+                       int64_t ignore_index, int reduction, float* loss, float* lse, void* workspace,
+                       size_t ws_bytes, int32_t* dev_err, void* stream);
+
+/*
+ * Backward: recompute + G + filter + dE/dC ("Cut Your Losses ...",
+ * "The Combined Backward Pass (Algorithm 4)", "Gradient Filtering").
+ *
+ *   lse           [N] fp32 from cce_forward on the same E, C.
+ *   grad_out      device fp32: [1] (SUM, MEAN: the gradient of the reduced
+ *                 loss) or [N] (NONE: the gradient of each row's loss).
+ *   filter_eps    skip a 128x128 (token x vocab) tile when every unscaled
+ *                 |G| = |softmax - onehot| in it is < filter_eps (an entry
+ *                 equal to filter_eps keeps the tile); 0 disables the filter.
+ *                 Skipped tiles issue no MMA and no store.
+ *   dE            [N, D] bf16 (written); ignored rows are exactly +0.
+ *   dC            [V, D] bf16 (written, each vocab row by exactly one CTA, no
+ *                 atomics); vocab rows whose tiles were all skipped are 0.
+ *   workspace     >= cce_backward_workspace_bytes(N, D, V) bytes, scratch.
+ *   dev_stats     optional device int64[2] (written): {tiles, skipped tiles}
+ *                 over the ceil(N/128) x ceil(V/128) filter tiles.
+ */
+cce_status cce_backward(const void* E, const void* C, const int64_t* x, const float* lse,
+                        const float* grad_out, int64_t N, int64_t D, int64_t V, int64_t ignore_index,
+                        int reduction, float filter_eps, void* dE, void* dC, void* workspace,
+                        size_t ws_bytes, int32_t* dev_err, int64_t* dev_stats, void* stream);
+
+/* Memory accounting (host arithmetic, no GPU).  Reproduces the page's memory
+ * table ("Cut Cross-Entropy: Training Loss Without the Logit Matrix ...",
+ * section "The memory numbers hold up"): the fp32 N x V logit buffer that the
+ * method avoids, the bf16 gradients dC and dE, and this library's workspaces
+ * ("extra" device memory beyond inputs and outputs). */
+typedef struct {
+  uint64_t logits_fp32_bytes;   /* N * V * 4: never allocated by this library */
+  uint64_t dE_bytes;            /* N * D * 2 */
+  uint64_t dC_bytes;            /* V * D * 2 */
+  uint64_t lse_bytes;           /* N * 4 */
+  uint64_t fwd_workspace_bytes; /* cce_forward_workspace_bytes() */
+  uint64_t bwd_workspace_bytes; /* cce_backward_workspace_bytes() */
+  uint64_t bwd_chunk_cols;      /* vocabulary columns per backward chunk */
+  uint64_t fwd_vocab_splits;    /* vocabulary splits of the forward partials */
+} cce_memory_report;
+
+cce_status cce_memory_accounting(int64_t N, int64_t D, int64_t V, cce_memory_report* out /* host */);
+
+/* Human-readable name of a status. */
+const char* cce_status_string(cce_status s);
+
+/* ABI version (major * 100 + minor). */
+int cce_abi_version(void);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t cce_kernel_launch_count(void);
+
+/* Phase timing for measurement.  When enabled, every cce_forward /
+ * cce_backward records CUDA events on its stream around each kernel phase.
+ * cce_profile_read synchronises on those events and returns, per phase, the
+ * summed milliseconds and the number of launches since the last reset.
+ * Phases: 0 fwd_lse_gemm, 1 fwd_combine, 2 bwd_prep, 3 bwd_recompute_g,
+ * 4 bwd_dC_gemm, 5 bwd_dE_gemm, 6 bwd_finalize. */
+#define CCE_NUM_PHASES 7
+cce_status cce_profile_enable(int enable);
+cce_status cce_profile_reset(void);
+cce_status cce_profile_read(double* ms /* host [CCE_NUM_PHASES] */, int64_t* launches /* host [CCE_NUM_PHASES] */);
+const char* cce_profile_phase_name(int phase);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CCE_GB300_H */

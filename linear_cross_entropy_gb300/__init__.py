@@ -1,0 +1,199 @@
+"""Cut Cross-Entropy for GB300 (sm_103a): the classifier-head matmul fused with
+cross-entropy, forward and backward, without writing the N x V logit matrix.
+
+Python binding of libcce.so.  Every step of the computation runs in the
+library's CUDA kernels; this module only marshals arguments (PyTorch provides
+device memory and streams).  There is no CPU fallback: importing fails when
+the library is not built, and calls fail on tensors that are not CUDA tensors.
+
+    loss = linear_cross_entropy(E, C, x)     # E [N,D] bf16, C [V,D] bf16, x [N] int64
+    loss.backward()                          # E.grad, C.grad (bf16)
+
+Semantics ("Cut Your Losses in Large-Vocabulary Language Models", section
+"The Mathematical Decomposition"; "cut-cross-entropy" kernel card,
+"Correctness"): loss_i = LSE_i - C[x_i] . E_i; rows with x_i == ignore_index
+add no loss and get exactly zero gradient; reduction none / sum / mean (mean
+over non-ignored rows, 0 for a fully ignored batch).
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+from ._lib import CCEError, DEVERR_TARGET_RANGE, DEVERR_TIMEOUT, RED
+
+FILTER_EPS = 2.0 ** -12  # finfo(bf16).eps / 32
+
+__all__ = [
+    "linear_cross_entropy", "cce_forward", "cce_backward", "CCEError", "FILTER_EPS",
+    "forward_workspace_bytes", "backward_workspace_bytes", "memory_report", "kernel_launch_count",
+    "Profiler",
+]
+
+_lib.load()
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream_handle(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_inputs(E, C, x):
+    for name, t, dt in (("E", E, torch.bfloat16), ("C", C, torch.bfloat16), ("x", x, torch.int64)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor (no CPU path)")
+        if t.dtype != dt:
+            raise ValueError(f"{name} must be {dt}, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if E.dim() != 2 or C.dim() != 2 or x.dim() != 1:
+        raise ValueError("expected E [N, D], C [V, D], x [N]")
+    if E.shape[1] != C.shape[1] or E.shape[0] != x.shape[0]:
+        raise ValueError(f"shape mismatch: E {tuple(E.shape)}, C {tuple(C.shape)}, x {tuple(x.shape)}")
+
+
+def forward_workspace_bytes(N, D, V) -> int:
+    return int(_lib.load().cce_forward_workspace_bytes(N, D, V))
+
+
+def backward_workspace_bytes(N, D, V) -> int:
+    return int(_lib.load().cce_backward_workspace_bytes(N, D, V))
+
+
+def memory_report(N, D, V) -> dict:
+    rep = _lib.MemoryReport()
+    _lib.check(_lib.load().cce_memory_accounting(N, D, V, ctypes.byref(rep)), "cce_memory_accounting")
+    return {k: int(getattr(rep, k)) for k, _ in _lib.MemoryReport._fields_}
+
+
+def kernel_launch_count() -> int:
+    return int(_lib.load().cce_kernel_launch_count())
+
+
+def _raise_dev_err(dev_err):
+    v = int(dev_err.item())
+    if v & DEVERR_TIMEOUT:
+        raise CCEError(9, "a kernel pipeline wait timed out")
+    if v & DEVERR_TARGET_RANGE:
+        raise CCEError(8, "target index outside [0, V) and not ignore_index")
+
+
+def cce_forward(E, C, x, ignore_index=-100, reduction="mean", *, stream=None, check_errors=True,
+                workspace=None, dev_err=None):
+    """Returns (loss, lse).  loss is [N] for reduction='none', else a 0-d tensor."""
+    _check_inputs(E, C, x)
+    N, D = E.shape
+    V = C.shape[0]
+    lib = _lib.load()
+    red = RED[reduction]
+    dev = E.device
+    loss = torch.empty(N if red == 0 else 1, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    need = int(lib.cce_forward_workspace_bytes(N, D, V))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    if dev_err is None:
+        dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.cce_forward(_ptr(E), _ptr(C), _ptr(x), N, D, V, int(ignore_index), red, _ptr(loss), _ptr(lse),
+                             _ptr(workspace), workspace.numel(), _ptr(dev_err), _stream_handle(stream))
+    _lib.check(st, "cce_forward")
+    if check_errors:
+        _raise_dev_err(dev_err)
+    return (loss if red == 0 else loss.reshape(())), lse
+
+
+def cce_backward(E, C, x, lse, grad_out, ignore_index=-100, reduction="mean", filter_eps=FILTER_EPS, *,
+                 stream=None, check_errors=True, workspace=None, dev_err=None, stats=False, dE=None, dC=None):
+    """Returns (dE, dC) or (dE, dC, {tiles, skipped}) with stats=True."""
+    _check_inputs(E, C, x)
+    N, D = E.shape
+    V = C.shape[0]
+    lib = _lib.load()
+    red = RED[reduction]
+    dev = E.device
+    g = grad_out.to(device=dev, dtype=torch.float32).contiguous().reshape(-1)
+    if g.numel() != (N if red == 0 else 1):
+        raise ValueError("grad_out must have N elements for reduction='none', else 1")
+    lse = lse.contiguous()
+    if dE is None:
+        dE = torch.empty_like(E)
+    if dC is None:
+        dC = torch.empty_like(C)
+    need = int(lib.cce_backward_workspace_bytes(N, D, V))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    if dev_err is None:
+        dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
+    st_t = torch.zeros(2, dtype=torch.int64, device=dev) if stats else None
+    with torch.cuda.device(dev):
+        st = lib.cce_backward(_ptr(E), _ptr(C), _ptr(x), _ptr(lse), _ptr(g), N, D, V, int(ignore_index), red,
+                              float(filter_eps), _ptr(dE), _ptr(dC), _ptr(workspace), workspace.numel(),
+                              _ptr(dev_err), _ptr(st_t), _stream_handle(stream))
+    _lib.check(st, "cce_backward")
+    if check_errors:
+        _raise_dev_err(dev_err)
+    if stats:
+        s = st_t.tolist()
+        return dE, dC, {"tiles": s[0], "skipped": s[1]}
+    return dE, dC
+
+
+class LinearCrossEntropyFunction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, E, C, x, ignore_index, reduction, filter_eps):
+        loss, lse = cce_forward(E, C, x, ignore_index, reduction)
+        ctx.save_for_backward(E, C, x, lse)
+        ctx.cfg = (ignore_index, reduction, filter_eps)
+        return loss
+
+    @staticmethod
+    def backward(ctx, grad_loss):
+        E, C, x, lse = ctx.saved_tensors
+        ignore_index, reduction, filter_eps = ctx.cfg
+        dE, dC = cce_backward(E, C, x, lse, grad_loss, ignore_index, reduction, filter_eps)
+        return dE, dC, None, None, None, None
+
+
+def linear_cross_entropy(E, C, x, ignore_index=-100, reduction="mean", filter_eps=FILTER_EPS):
+    """Cross-entropy of the logits E @ C^T against targets x, never materialised.
+
+    E [N, D] bf16 (hidden states), C [V, D] bf16 (classifier weight), x [N]
+    int64.  filter_eps is the backward's tile-skip threshold (0 disables)."""
+    return LinearCrossEntropyFunction.apply(E, C, x, ignore_index, reduction, filter_eps)
+
+
+@dataclass
+class PhaseTimes:
+    ms: dict
+    launches: dict
+
+
+class Profiler:
+    """Per-phase CUDA-event timing recorded by the library on its stream."""
+
+    def __enter__(self):
+        lib = _lib.load()
+        lib.cce_profile_reset()
+        lib.cce_profile_enable(1)
+        return self
+
+    def __exit__(self, *exc):
+        _lib.load().cce_profile_enable(0)
+        return False
+
+    @staticmethod
+    def read() -> PhaseTimes:
+        lib = _lib.load()
+        ms = (ctypes.c_double * _lib.NUM_PHASES)()
+        cnt = (ctypes.c_int64 * _lib.NUM_PHASES)()
+        _lib.check(lib.cce_profile_read(ms, cnt), "cce_profile_read")
+        names = [lib.cce_profile_phase_name(i).decode() for i in range(_lib.NUM_PHASES)]
+        return PhaseTimes({n: ms[i] for i, n in enumerate(names)}, {n: cnt[i] for i, n in enumerate(names)})

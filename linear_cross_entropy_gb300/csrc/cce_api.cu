@@ -1,0 +1,656 @@
+// Host side of the C ABI (include/cce.h): argument checks, workspace layout,
+// tensor maps, launches, phase timing; plus the small bandwidth-bound kernels
+// of the path (forward combine and loss reduction, backward target count,
+// dE finalisation, filter statistics).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <numeric>
+#include <vector>
+
+#include "../../include/cce.h"
+#include "internal.h"
+
+namespace cce {
+namespace {
+
+constexpr int REF_SMS = 152;          // split count heuristic assumes this many SMs
+constexpr size_t ALIGN = 256;         // sub-buffer alignment inside a workspace
+constexpr size_t G_CHUNK_BUDGET = size_t(512) << 20;  // bytes of the backward G chunk buffer
+constexpr int64_t MIN_CHUNK = 2048, MAX_CHUNK = 32768;
+constexpr int COMBINE_THREADS = 256;
+
+std::atomic<uint64_t> g_launches{0};
+
+// ------------------------------------------------------------ small kernels
+// Per row: LSE from the per-split partials (fixed split order), loss, and a
+// deterministic per-block partial sum for the reduction.
+__global__ void combine_kernel(const float* __restrict__ part_m, const float* __restrict__ part_s,
+                               const float* __restrict__ tgt, const int64_t* __restrict__ x, int N, int S, int V,
+                               long long ignore_index, int reduction, float* __restrict__ lse,
+                               float* __restrict__ loss_rows, double* __restrict__ blk_sum,
+                               int* __restrict__ blk_cnt, int32_t* dev_err) {
+  __shared__ double ssum[COMBINE_THREADS];
+  __shared__ int scnt[COMBINE_THREADS];
+  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  double my = 0.0;
+  int mycnt = 0;
+  if (row < N) {
+    float M = -INFINITY;
+    for (int s = 0; s < S; ++s) M = fmaxf(M, part_m[static_cast<size_t>(s) * N + row]);
+    float sum = 0.0f;
+    for (int s = 0; s < S; ++s) {
+      const size_t i = static_cast<size_t>(s) * N + row;
+      sum += part_s[i] * exp2f(part_m[i] - M);
+    }
+    const float L = (M + log2f(sum)) * 0.6931471805599453f;
+    lse[row] = L;
+    const long long xi = static_cast<long long>(x[row]);
+    bool valid = xi != ignore_index;
+    if (valid && (xi < 0 || xi >= V)) {
+      if (dev_err) atomicOr(reinterpret_cast<int*>(dev_err), CCE_DEVERR_TARGET_RANGE);
+      valid = false;
+    }
+    const float lr = valid ? (L - tgt[row]) : 0.0f;
+    if (reduction == CCE_RED_NONE) loss_rows[row] = lr;
+    my = static_cast<double>(lr);
+    mycnt = valid ? 1 : 0;
+  }
+  ssum[threadIdx.x] = my;
+  scnt[threadIdx.x] = mycnt;
+  __syncthreads();
+  for (int w = COMBINE_THREADS / 2; w > 0; w >>= 1) {
+    if (static_cast<int>(threadIdx.x) < w) {
+      ssum[threadIdx.x] += ssum[threadIdx.x + w];
+      scnt[threadIdx.x] += scnt[threadIdx.x + w];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    blk_sum[blockIdx.x] = ssum[0];
+    blk_cnt[blockIdx.x] = scnt[0];
+  }
+}
+
+// One block: fixed-order sum of the per-block partials -> the reduced loss.
+__global__ void finish_loss_kernel(const double* __restrict__ blk_sum, const int* __restrict__ blk_cnt, int nblk,
+                                   int reduction, float* __restrict__ loss) {
+  __shared__ double ssum[COMBINE_THREADS];
+  __shared__ long long scnt[COMBINE_THREADS];
+  double s = 0.0;
+  long long c = 0;
+  for (int i = threadIdx.x; i < nblk; i += COMBINE_THREADS) {
+    s += blk_sum[i];
+    c += blk_cnt[i];
+  }
+  ssum[threadIdx.x] = s;
+  scnt[threadIdx.x] = c;
+  __syncthreads();
+  for (int w = COMBINE_THREADS / 2; w > 0; w >>= 1) {
+    if (static_cast<int>(threadIdx.x) < w) {
+      ssum[threadIdx.x] += ssum[threadIdx.x + w];
+      scnt[threadIdx.x] += scnt[threadIdx.x + w];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const double total = ssum[0];
+    const long long cnt = scnt[0];
+    loss[0] = static_cast<float>(reduction == CCE_RED_SUM ? total : total / static_cast<double>(cnt > 0 ? cnt : 1));
+  }
+}
+
+// One block: number of non-ignored rows (mean reduction) and target range check.
+__global__ void count_kernel(const int64_t* __restrict__ x, int N, int V, long long ignore_index, int* count,
+                             int32_t* dev_err) {
+  __shared__ int sc[1024];
+  int c = 0;
+  bool bad = false;
+  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    const long long xi = static_cast<long long>(x[i]);
+    if (xi == ignore_index) continue;
+    if (xi < 0 || xi >= V) {
+      bad = true;
+      continue;
+    }
+    ++c;
+  }
+  if (bad && dev_err) atomicOr(reinterpret_cast<int*>(dev_err), CCE_DEVERR_TARGET_RANGE);
+  sc[threadIdx.x] = c;
+  __syncthreads();
+  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+    if (static_cast<int>(threadIdx.x) < w) sc[threadIdx.x] += sc[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *count = sc[0];
+}
+
+// dE (bf16) from the fp32 accumulator; ignored / invalid rows are exactly +0.
+__global__ void finalize_de_kernel(const float4* __restrict__ acc, const int64_t* __restrict__ x, int N, int D,
+                                   int V, long long ignore_index, uint2* __restrict__ dE) {
+  const size_t per_row = static_cast<size_t>(D) / 4;
+  const size_t total = static_cast<size_t>(N) * per_row;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t row = i / per_row;
+    const long long xi = static_cast<long long>(x[row]);
+    const bool valid = xi != ignore_index && xi >= 0 && xi < V;
+    uint2 out = make_uint2(0u, 0u);
+    if (valid) {
+      const float4 v = acc[i];
+      __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+      std::memcpy(&out.x, &lo, 4);
+      std::memcpy(&out.y, &hi, 4);
+    }
+    dE[i] = out;
+  }
+}
+
+__global__ void stats_kernel(const uint8_t* __restrict__ bitmap, long long n, int64_t* stats) {
+  __shared__ long long sz[1024];
+  long long z = 0;
+  for (long long i = threadIdx.x; i < n; i += blockDim.x) z += bitmap[i] == 0 ? 1 : 0;
+  sz[threadIdx.x] = z;
+  __syncthreads();
+  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+    if (static_cast<int>(threadIdx.x) < w) sz[threadIdx.x] += sz[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    stats[0] = n;
+    stats[1] = sz[0];
+  }
+}
+
+// ------------------------------------------------------------ host helpers
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int fwd_splits(int64_t N, int64_t V) {
+  const int64_t n_blocks = cdiv(N, BM), v_tiles = cdiv(V, BN);
+  const int64_t s_max = std::max<int64_t>(1, v_tiles / 4);
+  const int64_t base = REF_SMS / std::gcd<int64_t>(n_blocks, REF_SMS);
+  int64_t S;
+  if (base <= s_max) {
+    S = base;
+    while (n_blocks * S < 2 * REF_SMS && S + base <= s_max) S += base;
+  } else {
+    S = std::min<int64_t>(s_max, std::max<int64_t>(1, cdiv(2 * REF_SMS, n_blocks)));
+  }
+  return static_cast<int>(std::min(S, v_tiles));
+}
+
+int64_t bwd_chunk_cols(int64_t N, int64_t V) {
+  const int64_t vpad = cdiv(V, BN) * BN;
+  int64_t vc = static_cast<int64_t>(G_CHUNK_BUDGET / (2 * static_cast<size_t>(N))) / BN * BN;
+  vc = std::max<int64_t>(MIN_CHUNK, std::min<int64_t>(MAX_CHUNK, vc));
+  // At least two chunks whenever V spans more than one tile, so the staging
+  // buffer is never an N x V matrix.
+  if (V > BN) vc = std::min(vc, cdiv(cdiv(V, 2), BN) * BN);
+  return std::min(vc, vpad);
+}
+
+struct FwdLayout {
+  size_t part_m, part_s, tgt, blk_sum, blk_cnt, total;
+  int S, nblk;
+};
+
+FwdLayout fwd_layout(int64_t N, int64_t V) {
+  FwdLayout L{};
+  L.S = fwd_splits(N, V);
+  L.nblk = static_cast<int>(cdiv(N, COMBINE_THREADS));
+  size_t o = 0;
+  L.part_m = o;
+  o = align_up(o + sizeof(float) * L.S * N, ALIGN);
+  L.part_s = o;
+  o = align_up(o + sizeof(float) * L.S * N, ALIGN);
+  L.tgt = o;
+  o = align_up(o + sizeof(float) * N, ALIGN);
+  L.blk_sum = o;
+  o = align_up(o + sizeof(double) * L.nblk, ALIGN);
+  L.blk_cnt = o;
+  o = align_up(o + sizeof(int) * L.nblk, ALIGN);
+  L.total = o;
+  return L;
+}
+
+struct BwdLayout {
+  size_t count, bitmap, gbuf, deacc, total;
+  int64_t vc, bm_ld, n128;
+};
+
+BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V) {
+  BwdLayout L{};
+  L.vc = bwd_chunk_cols(N, V);
+  L.bm_ld = cdiv(V, 128);
+  L.n128 = cdiv(N, 128);
+  size_t o = 0;
+  L.count = o;
+  o = align_up(o + sizeof(int), ALIGN);
+  L.bitmap = o;
+  o = align_up(o + static_cast<size_t>(L.n128 * L.bm_ld), ALIGN);
+  L.gbuf = o;
+  o = align_up(o + static_cast<size_t>(N) * L.vc * 2, ALIGN);
+  L.deacc = o;
+  o = align_up(o + static_cast<size_t>(N) * D * 4, ALIGN);
+  L.total = o;
+  return L;
+}
+
+bool sizes_ok(int64_t N, int64_t D, int64_t V) {
+  const int64_t lim = int64_t(1) << 31;
+  return N >= 1 && N < lim && V >= 1 && V < lim && D >= 8 && D < lim && D % 8 == 0;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------- device state
+struct DeviceInfo {
+  bool init = false;
+  bool ok = false;
+  int sms = 0;
+};
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+cce_status device_check(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return CCE_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.init) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return CCE_ERR_CUDA;
+    }
+    d.ok = (major == 10 && minor == 3);
+    d.sms = sms;
+    if (d.ok) {
+      if (prepare_gemm_kernels() != cudaSuccess) {
+        cudaGetLastError();
+        return CCE_ERR_CUDA;
+      }
+      if (!g_encode) {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr) {
+          cudaGetLastError();
+          return CCE_ERR_CUDA;
+        }
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+      }
+    }
+    d.init = true;
+  }
+  if (!d.ok) return CCE_ERR_DEVICE;
+  *sms = d.sms;
+  return CCE_OK;
+}
+
+// 2-D row-major tensor map with a 128-byte-swizzled box (inner box = 128 B).
+bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* ptr, uint64_t inner,
+               uint64_t outer, uint64_t pitch_elems, uint32_t box_inner, uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch_elems * esize};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------- phase timing
+struct PhaseRec {
+  int phase;
+  cudaEvent_t a, b;
+};
+bool g_prof = false;
+std::vector<PhaseRec> g_recs;
+std::vector<cudaEvent_t> g_pool;
+double g_ms[CCE_NUM_PHASES];
+int64_t g_cnt[CCE_NUM_PHASES];
+
+cudaEvent_t pool_get() {
+  if (!g_pool.empty()) {
+    cudaEvent_t e = g_pool.back();
+    g_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+struct PhaseScope {
+  bool on;
+  PhaseRec rec;
+  cudaStream_t s;
+  PhaseScope(int phase, cudaStream_t st) : on(false), s(st) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_prof) return;
+    rec.phase = phase;
+    rec.a = pool_get();
+    rec.b = pool_get();
+    on = rec.a && rec.b;
+    if (on) cudaEventRecord(rec.a, s);
+  }
+  ~PhaseScope() {
+    if (!on) return;
+    cudaEventRecord(rec.b, s);
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_recs.push_back(rec);
+  }
+};
+
+cce_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return CCE_OK;
+  return CCE_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace cce
+
+using namespace cce;
+
+extern "C" {
+
+int cce_abi_version(void) { return 100; }
+
+uint64_t cce_kernel_launch_count(void) { return g_launches.load(); }
+
+const char* cce_status_string(cce_status s) {
+  switch (s) {
+    case CCE_OK: return "ok";
+    case CCE_ERR_NULL: return "null pointer";
+    case CCE_ERR_SHAPE: return "bad shape (need 1 <= N, V < 2^31; 8 <= D < 2^31, D % 8 == 0)";
+    case CCE_ERR_ALIGN: return "buffer not 16-byte aligned";
+    case CCE_ERR_ARG: return "bad argument (reduction or filter_eps)";
+    case CCE_ERR_WORKSPACE: return "workspace too small";
+    case CCE_ERR_DEVICE: return "current device is not compute capability 10.3 (sm_103a)";
+    case CCE_ERR_CUDA: return "CUDA error";
+    case CCE_ERR_TARGET_RANGE: return "target index outside [0, V) and not ignore_index";
+    case CCE_ERR_TIMEOUT: return "a kernel pipeline wait timed out";
+  }
+  return "unknown status";
+}
+
+size_t cce_forward_workspace_bytes(int64_t N, int64_t D, int64_t V) {
+  if (!sizes_ok(N, D, V)) return 0;
+  return fwd_layout(N, V).total;
+}
+
+size_t cce_backward_workspace_bytes(int64_t N, int64_t D, int64_t V) {
+  if (!sizes_ok(N, D, V)) return 0;
+  return bwd_layout(N, D, V).total;
+}
+
+cce_status cce_memory_accounting(int64_t N, int64_t D, int64_t V, cce_memory_report* out) {
+  if (!out) return CCE_ERR_NULL;
+  if (!sizes_ok(N, D, V)) return CCE_ERR_SHAPE;
+  out->logits_fp32_bytes = static_cast<uint64_t>(N) * V * 4;
+  out->dE_bytes = static_cast<uint64_t>(N) * D * 2;
+  out->dC_bytes = static_cast<uint64_t>(V) * D * 2;
+  out->lse_bytes = static_cast<uint64_t>(N) * 4;
+  out->fwd_workspace_bytes = fwd_layout(N, V).total;
+  const BwdLayout b = bwd_layout(N, D, V);
+  out->bwd_workspace_bytes = b.total;
+  out->bwd_chunk_cols = static_cast<uint64_t>(b.vc);
+  out->fwd_vocab_splits = static_cast<uint64_t>(fwd_layout(N, V).S);
+  return CCE_OK;
+}
+
+cce_status cce_forward(const void* E, const void* C, const int64_t* x, int64_t N, int64_t D, int64_t V,
+                       int64_t ignore_index, int reduction, float* loss, float* lse, void* workspace,
+                       size_t ws_bytes, int32_t* dev_err, void* stream) {
+  if (!E || !C || !x || !loss || !lse || !workspace) return CCE_ERR_NULL;
+  if (!sizes_ok(N, D, V)) return CCE_ERR_SHAPE;
+  if (!aligned16(E) || !aligned16(C) || !aligned16(loss) || !aligned16(lse) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(x) & 7u))
+    return CCE_ERR_ALIGN;
+  if (reduction != CCE_RED_NONE && reduction != CCE_RED_SUM && reduction != CCE_RED_MEAN) return CCE_ERR_ARG;
+  const FwdLayout W = fwd_layout(N, V);
+  if (ws_bytes < W.total) return CCE_ERR_WORKSPACE;
+  int sms = 0;
+  cce_status st = device_check(&sms);
+  if (st != CCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  // A = E [N, D]: box 64 (D) x 128 rows.  B = C [V, D]: box 64 (D) x 256 rows.
+  if (!make_tmap(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, E, D, N, D, BK, BM) ||
+      !make_tmap(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, D, V, D, BK, BN))
+    return CCE_ERR_CUDA;
+  a.tmOut = a.tmA;  // unused
+  a.N = static_cast<int>(N);
+  a.D = static_cast<int>(D);
+  a.V = static_cast<int>(V);
+  a.n_blocks = static_cast<int>(cdiv(N, BM));
+  a.k_blocks = static_cast<int>(cdiv(D, BK));
+  a.splits = W.S;
+  a.v_tiles = static_cast<int>(cdiv(V, BN));
+  a.x = x;
+  a.ignore_index = ignore_index;
+  a.part_m = reinterpret_cast<float*>(ws + W.part_m);
+  a.part_s = reinterpret_cast<float*>(ws + W.part_s);
+  a.tgt = reinterpret_cast<float*>(ws + W.tgt);
+  a.dev_err = dev_err;
+  const int units = a.n_blocks * a.splits;
+  {
+    PhaseScope ps(0, s);
+    cudaError_t e = launch_gemm(MODE_FWD, a, std::min(units, sms), s);
+    g_launches++;
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  {
+    PhaseScope ps(1, s);
+    float* loss_rows = (reduction == CCE_RED_NONE) ? loss : nullptr;
+    combine_kernel<<<W.nblk, COMBINE_THREADS, 0, s>>>(
+        a.part_m, a.part_s, a.tgt, x, a.N, W.S, a.V, static_cast<long long>(ignore_index), reduction, lse,
+        loss_rows, reinterpret_cast<double*>(ws + W.blk_sum), reinterpret_cast<int*>(ws + W.blk_cnt), dev_err);
+    g_launches++;
+    if (reduction != CCE_RED_NONE) {
+      finish_loss_kernel<<<1, COMBINE_THREADS, 0, s>>>(reinterpret_cast<double*>(ws + W.blk_sum),
+                                                       reinterpret_cast<int*>(ws + W.blk_cnt), W.nblk, reduction,
+                                                       loss);
+      g_launches++;
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return CCE_OK;
+}
+
+cce_status cce_backward(const void* E, const void* C, const int64_t* x, const float* lse, const float* grad_out,
+                        int64_t N, int64_t D, int64_t V, int64_t ignore_index, int reduction, float filter_eps,
+                        void* dE, void* dC, void* workspace, size_t ws_bytes, int32_t* dev_err,
+                        int64_t* dev_stats, void* stream) {
+  if (!E || !C || !x || !lse || !grad_out || !dE || !dC || !workspace) return CCE_ERR_NULL;
+  if (!sizes_ok(N, D, V)) return CCE_ERR_SHAPE;
+  if (!aligned16(E) || !aligned16(C) || !aligned16(lse) || !aligned16(dE) || !aligned16(dC) ||
+      !aligned16(workspace) || (reinterpret_cast<uintptr_t>(x) & 7u) || (reinterpret_cast<uintptr_t>(grad_out) & 3u) ||
+      (reinterpret_cast<uintptr_t>(dev_stats) & 7u))
+    return CCE_ERR_ALIGN;
+  if (reduction != CCE_RED_NONE && reduction != CCE_RED_SUM && reduction != CCE_RED_MEAN) return CCE_ERR_ARG;
+  if (!(filter_eps >= 0.0f) || !std::isfinite(filter_eps)) return CCE_ERR_ARG;
+  const BwdLayout W = bwd_layout(N, D, V);
+  if (ws_bytes < W.total) return CCE_ERR_WORKSPACE;
+  int sms = 0;
+  cce_status st = device_check(&sms);
+  if (st != CCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* count = reinterpret_cast<int*>(ws + W.count);
+  uint8_t* bitmap = ws + W.bitmap;
+  void* gbuf = ws + W.gbuf;
+  float* deacc = reinterpret_cast<float*>(ws + W.deacc);
+
+  {
+    PhaseScope ps(2, s);
+    count_kernel<<<1, 1024, 0, s>>>(x, static_cast<int>(N), static_cast<int>(V), static_cast<long long>(ignore_index),
+                                    count, dev_err);
+    g_launches++;
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+
+  GemmArgs g;  // recompute + G
+  std::memset(&g, 0, sizeof(g));
+  GemmArgs c;  // dC
+  std::memset(&c, 0, sizeof(c));
+  GemmArgs d;  // dE
+  std::memset(&d, 0, sizeof(d));
+  const uint64_t vc = static_cast<uint64_t>(W.vc);
+  bool ok = true;
+  ok &= make_tmap(&g.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, E, D, N, D, BK, BM);
+  ok &= make_tmap(&g.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, D, V, D, BK, BN);
+  ok &= make_tmap(&g.tmOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, gbuf, vc, N, vc, 64, 32);
+  ok &= make_tmap(&c.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, gbuf, vc, N, vc, 64, 64);
+  ok &= make_tmap(&c.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, E, D, N, D, 64, 64);
+  ok &= make_tmap(&c.tmOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dC, D, V, D, 64, 32);
+  ok &= make_tmap(&d.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, gbuf, vc, N, vc, 64, BM);
+  ok &= make_tmap(&d.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, D, V, D, 64, 64);
+  ok &= make_tmap(&d.tmOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, deacc, D, N, D, 32, 32);
+  if (!ok) return CCE_ERR_CUDA;
+
+  for (GemmArgs* p : {&g, &c, &d}) {
+    p->N = static_cast<int>(N);
+    p->D = static_cast<int>(D);
+    p->V = static_cast<int>(V);
+    p->n_blocks = static_cast<int>(cdiv(N, BM));
+    p->x = x;
+    p->ignore_index = ignore_index;
+    p->lse = lse;
+    p->grad_out = grad_out;
+    p->count = count;
+    p->reduction = reduction;
+    p->eps = filter_eps;
+    p->bitmap = bitmap;
+    p->bm_ld = static_cast<int>(W.bm_ld);
+    p->dev_err = dev_err;
+  }
+  g.k_blocks = static_cast<int>(cdiv(D, BK));
+  c.k_blocks = static_cast<int>(cdiv(N, BK));
+  c.n_tiles = static_cast<int>(cdiv(D, BN));
+  d.n_tiles = c.n_tiles;
+  d.m_tiles = static_cast<int>(cdiv(N, BM));
+
+  const int64_t nchunks = cdiv(V, W.vc);
+  for (int64_t ch = 0; ch < nchunks; ++ch) {
+    const int v0 = static_cast<int>(ch * W.vc);
+    const int w = static_cast<int>(std::min<int64_t>(W.vc, V - v0));
+    for (GemmArgs* p : {&g, &c, &d}) {
+      p->chunk_v0 = v0;
+      p->chunk_w = w;
+    }
+    g.v_tiles = static_cast<int>(cdiv(w, BN));
+    c.m_tiles = static_cast<int>(cdiv(w, BM));
+    d.k_blocks = static_cast<int>(cdiv(w, BK));
+    d.first_chunk = (ch == 0) ? 1 : 0;
+    cudaError_t e;
+    {
+      PhaseScope ps(3, s);
+      e = launch_gemm(MODE_BWD_G, g, static_cast<int>(std::min<int64_t>(sms, int64_t(g.n_blocks) * g.v_tiles)), s);
+      g_launches++;
+      if (e != cudaSuccess) return cuda_status(e);
+    }
+    {
+      PhaseScope ps(4, s);
+      e = launch_gemm(MODE_DC, c, static_cast<int>(std::min<int64_t>(sms, int64_t(c.m_tiles) * c.n_tiles)), s);
+      g_launches++;
+      if (e != cudaSuccess) return cuda_status(e);
+    }
+    {
+      PhaseScope ps(5, s);
+      e = launch_gemm(MODE_DE, d, static_cast<int>(std::min<int64_t>(sms, int64_t(d.m_tiles) * d.n_tiles)), s);
+      g_launches++;
+      if (e != cudaSuccess) return cuda_status(e);
+    }
+  }
+  {
+    PhaseScope ps(6, s);
+    const size_t n4 = static_cast<size_t>(N) * D / 4;
+    const int blocks = static_cast<int>(std::min<size_t>(static_cast<size_t>(sms) * 8, (n4 + 255) / 256));
+    finalize_de_kernel<<<std::max(blocks, 1), 256, 0, s>>>(reinterpret_cast<const float4*>(deacc), x,
+                                                           static_cast<int>(N), static_cast<int>(D),
+                                                           static_cast<int>(V), static_cast<long long>(ignore_index),
+                                                           static_cast<uint2*>(dE));
+    g_launches++;
+    if (dev_stats) {
+      stats_kernel<<<1, 1024, 0, s>>>(bitmap, static_cast<long long>(W.n128 * W.bm_ld), dev_stats);
+      g_launches++;
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return CCE_OK;
+}
+
+cce_status cce_profile_enable(int enable) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_prof = enable != 0;
+  return CCE_OK;
+}
+
+cce_status cce_profile_reset(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (auto& r : g_recs) {
+    g_pool.push_back(r.a);
+    g_pool.push_back(r.b);
+  }
+  g_recs.clear();
+  for (int i = 0; i < CCE_NUM_PHASES; ++i) {
+    g_ms[i] = 0.0;
+    g_cnt[i] = 0;
+  }
+  return CCE_OK;
+}
+
+cce_status cce_profile_read(double* ms, int64_t* launches) {
+  if (!ms || !launches) return CCE_ERR_NULL;
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (auto& r : g_recs) {
+    if (cudaEventSynchronize(r.b) != cudaSuccess) return CCE_ERR_CUDA;
+    float t = 0.0f;
+    if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) return CCE_ERR_CUDA;
+    g_ms[r.phase] += t;
+    g_cnt[r.phase] += 1;
+    g_pool.push_back(r.a);
+    g_pool.push_back(r.b);
+  }
+  g_recs.clear();
+  for (int i = 0; i < CCE_NUM_PHASES; ++i) {
+    ms[i] = g_ms[i];
+    launches[i] = g_cnt[i];
+  }
+  return CCE_OK;
+}
+
+const char* cce_profile_phase_name(int phase) {
+  static const char* names[CCE_NUM_PHASES] = {"fwd_lse_gemm",  "fwd_combine", "bwd_prep",   "bwd_recompute_g",
+                                               "bwd_dC_gemm",   "bwd_dE_gemm", "bwd_finalize"};
+  if (phase < 0 || phase >= CCE_NUM_PHASES) return "";
+  return names[phase];
+}
+
+}  // extern "C"

@@ -115,6 +115,17 @@ def forward(E, C, x, ignore_index=IGNORE_INDEX, reduction="mean", rows=None):
     return out
 
 
+def indexed_logits(E, C, x, ignore_index=IGNORE_INDEX):
+    """o_i = C[x_i] . E_i, the indexed matrix product (NaN on ignored rows)."""
+    E = np.asarray(E, np.float64)
+    C = np.asarray(C, np.float64)
+    x = np.asarray(x, np.int64)
+    ok = x != ignore_index
+    out = np.full(E.shape[0], np.nan)
+    out[ok] = np.einsum("nd,nd->n", E[ok], C[x[ok]])
+    return out
+
+
 def reduce_loss(loss_rows, count, reduction):
     """none -> the rows; sum -> their sum; mean -> sum / max(count, 1)."""
     if reduction == "none":

@@ -1,0 +1,186 @@
+"""GPU-vs-oracle parity on seeded inputs, through the C ABI.
+
+Sizes are small enough for the fp64 oracle to finish in seconds, yet span
+several 128 x 256 tiles and ragged tails in N, D and V, several backward
+vocabulary chunks, every reduction, ignored rows and the filter on and off.
+"""
+import numpy as np
+import pytest
+import torch
+
+import cce_workloads as W
+import oracle as O
+from tests.gpu_util import (TOL_GRAD, TOL_GRAD_FILTERED, assert_forward_close, assert_grads_close, make,
+                            oracle_full, rel_fro, run_cuda)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from linear_cross_entropy_gb300 import build
+    build.build()
+
+
+@pytest.mark.parametrize("filter_on", [True, False])
+def test_tiny_config(filter_on):
+    """The tiny workload (N=256, D=128, V=4096, mean), full comparison."""
+    w, (E, C, x) = make("tiny")
+    eps = O.FILTER_EPS if filter_on else 0.0
+    got = run_cuda(E, C, x, reduction=w.reduction, filter_eps=eps)
+    ref = oracle_full(E, C, x, reduction=w.reduction)
+    assert_forward_close(got, ref, w.reduction, x)
+    assert_grads_close(got, ref["dE"], ref["dC"], TOL_GRAD_FILTERED if filter_on else TOL_GRAD, x)
+
+
+@pytest.mark.parametrize("N,D,V", [
+    (300, 96, 1000),    # ragged in every dimension; D not a multiple of 64
+    (129, 64, 257),     # one row / one column past a tile
+    (1, 64, 300),       # a single token
+    (1000, 256, 5000),  # several row blocks and vocabulary tiles
+    (640, 128, 9000),   # several backward chunks
+])
+@pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
+def test_ragged_shapes_unfiltered(N, D, V, reduction):
+    w, (E, C, x) = make(W.small("r", N, D, V, reduction=reduction))
+    g = np.random.default_rng(N + V).standard_normal(N) if reduction == "none" else 1.0
+    got = run_cuda(E, C, x, reduction=reduction, filter_eps=0.0, grad_out=g)
+    ref = oracle_full(E, C, x, reduction=reduction, grad_out=g)
+    assert_forward_close(got, ref, reduction, x)
+    assert_grads_close(got, ref["dE"], ref["dC"], TOL_GRAD, x)
+
+
+def test_target_in_short_final_panel():
+    """'Correctness': a ragged vocabulary with targets inside the short final panel."""
+    N, D, V = 200, 64, 1000 + 37
+    w, (E, C, x) = make(W.small("p", N, D, V, ignore_frac=0.0))
+    x = x.copy()
+    x[::3] = V - 1 - (np.arange(len(x[::3])) % 37)
+    got = run_cuda(E, C, x, reduction="mean", filter_eps=0.0)
+    ref = oracle_full(E, C, x, reduction="mean")
+    assert_forward_close(got, ref, "mean", x)
+    assert_grads_close(got, ref["dE"], ref["dC"], TOL_GRAD, x)
+
+
+def test_multi_chunk_backward():
+    """V wide enough for several backward vocabulary chunks (dE accumulates)."""
+    import linear_cross_entropy_gb300 as cce
+    N, D, V = 256, 64, 40000
+    assert cce.memory_report(N, D, V)["bwd_chunk_cols"] < V
+    w, (E, C, x) = make(W.small("c", N, D, V))
+    got = run_cuda(E, C, x, reduction="mean", filter_eps=0.0)
+    ref = oracle_full(E, C, x, reduction="mean")
+    assert_forward_close(got, ref, "mean", x)
+    assert_grads_close(got, ref["dE"], ref["dC"], TOL_GRAD, x)
+
+
+def test_filter_matches_filtered_oracle():
+    """Frequent-token inputs: softmax mass sits in the lowest 256 ids, so most
+    128 x 128 tiles are skipped.  The filtered result matches the filtered
+    oracle tightly and the unfiltered oracle within 1e-2; the skip count
+    equals the oracle's tile survival map (no tile lies near eps here)."""
+    N, D, V = 512, 128, 6000
+    E, C, x = W.frequent_token_inputs(N, D, V, n_freq=256, seed=3)
+    got = run_cuda(E, C, x, reduction="mean", filter_eps=O.FILTER_EPS)
+    ref = oracle_full(E, C, x, reduction="mean", filter_eps=O.FILTER_EPS)
+    assert_forward_close(got, ref, "mean", x)
+    assert_grads_close(got, ref["dE"], ref["dC"], TOL_GRAD_FILTERED, x)
+    assert rel_fro(got["dE"], ref["dE_f"]) <= TOL_GRAD
+    assert rel_fro(got["dC"], ref["dC_f"]) <= TOL_GRAD
+    keep = ref["keep"]
+    st = got["stats"]
+    assert st["tiles"] == keep.size
+    assert st["skipped"] == int((~keep).sum())
+    assert st["skipped"] > keep.size // 2
+    # rows of dC in fully skipped vocabulary slices are exact zeros
+    dead = np.nonzero(~keep.any(axis=0))[0]
+    assert len(dead) > 0
+    for b in dead[:8]:
+        assert np.all(got["dC"][b * 128:(b + 1) * 128] == 0.0)
+
+
+def test_fully_ignored_batch():
+    """'Correctness': a fully masked batch gives zero loss and finite zero gradients."""
+    w, (E, C, x) = make(W.small("i", 300, 64, 1000))
+    x = np.full_like(x, -100)
+    got = run_cuda(E, C, x, reduction="mean")
+    assert float(got["loss"].reshape(())) == 0.0
+    assert np.all(got["dE"] == 0.0) and np.all(got["dC"] == 0.0)
+    assert np.all(np.isfinite(got["lse"]))
+
+
+def test_custom_ignore_index():
+    w, (E, C, x) = make(W.small("j", 200, 64, 700, ignore_frac=0.0))
+    x = x.copy()
+    x[5:40] = 7  # rows whose target equals the custom ignore_index are ignored
+    got = run_cuda(E, C, x, ignore_index=7, reduction="sum", filter_eps=0.0)
+    ref = oracle_full(E, C, x, ignore_index=7, reduction="sum")
+    assert_forward_close(got, ref, "sum", x, ignore_index=7)
+    assert_grads_close(got, ref["dE"], ref["dC"], TOL_GRAD, x, ignore_index=7)
+
+
+def test_repeated_calls_are_bitwise_identical():
+    import linear_cross_entropy_gb300 as cce
+    from tests.gpu_util import to_device
+    w, (E, C, x) = make(W.small("d", 700, 128, 3000))
+    Et, Ct, xt = to_device(E, C, x)
+    l1, s1 = cce.cce_forward(Et, Ct, xt)
+    l2, s2 = cce.cce_forward(Et, Ct, xt)
+    assert torch.equal(l1, l2) and torch.equal(s1, s2)
+    g = torch.ones(1, device="cuda")
+    a = cce.cce_backward(Et, Ct, xt, s1, g)
+    b = cce.cce_backward(Et, Ct, xt, s1, g)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_out_of_range_target_is_reported():
+    import linear_cross_entropy_gb300 as cce
+    from tests.gpu_util import to_device
+    w, (E, C, x) = make(W.small("o", 64, 64, 500, ignore_frac=0.0))
+    x = x.copy()
+    x[3] = 500
+    x[9] = -5
+    Et, Ct, xt = to_device(E, C, x)
+    with pytest.raises(cce.CCEError) as ei:
+        cce.cce_forward(Et, Ct, xt)
+    assert ei.value.status == 8
+    # the row was treated as ignored: the call completed and the context is usable
+    loss, lse = cce.cce_forward(Et, Ct, xt, check_errors=False)
+    assert torch.isfinite(lse).all()
+    with pytest.raises(cce.CCEError):
+        cce.cce_backward(Et, Ct, xt, lse, torch.ones(1, device="cuda"))
+
+
+def test_autograd_function_matches_oracle():
+    import linear_cross_entropy_gb300 as cce
+    from tests.gpu_util import to_device
+    w, (E, C, x) = make(W.small("a", 300, 128, 2000))
+    Et, Ct, xt = to_device(E, C, x)
+    Et.requires_grad_(True)
+    Ct.requires_grad_(True)
+    loss = cce.linear_cross_entropy(Et, Ct, xt, filter_eps=0.0)
+    (2.5 * loss).backward()
+    ref = oracle_full(E, C, x, reduction="mean", grad_out=2.5)
+    assert abs(loss.item() - ref["loss"]) <= 1e-5 * abs(ref["loss"])
+    assert rel_fro(Et.grad.double().cpu().numpy(), ref["dE"]) <= TOL_GRAD
+    assert rel_fro(Ct.grad.double().cpu().numpy(), ref["dC"]) <= TOL_GRAD
+
+
+def test_no_n_by_v_allocation():
+    """The caching allocator never sees an N x V-sized block during fwd + bwd."""
+    import linear_cross_entropy_gb300 as cce
+    from tests.gpu_util import to_device
+    N, D, V = 2048, 256, 60000
+    w, (E, C, x) = make(W.small("m", N, D, V))
+    Et, Ct, xt = to_device(E, C, x)
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats()
+    base = torch.cuda.memory_allocated()
+    loss, lse = cce.cce_forward(Et, Ct, xt)
+    dE, dC = cce.cce_backward(Et, Ct, xt, lse, torch.ones(1, device="cuda"))
+    torch.cuda.synchronize()
+    extra = torch.cuda.max_memory_allocated() - base
+    outputs = dE.numel() * 2 + dC.numel() * 2 + lse.numel() * 4 + 4
+    assert extra - outputs < N * V * 2, (extra, outputs)
