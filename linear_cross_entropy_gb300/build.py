@@ -1,6 +1,8 @@
 """Build libcce.so (the C-ABI library) in-tree with nvcc for sm_103a.
 
-    python -m linear_cross_entropy_gb300.build [--verbose-ptxas]
+    python linear_cross_entropy_gb300/build.py [--verbose-ptxas]
+
+(run by path: importing the package loads the library this script builds)
 
 Each translation unit is compiled in parallel, then linked into
 linear_cross_entropy_gb300/libcce.so against the shared CUDA runtime (the

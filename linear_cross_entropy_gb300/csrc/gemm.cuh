@@ -256,7 +256,22 @@ struct EpiCtx {
   int q;           // lane quadrant = tile rows 32q .. 32q + 31
   uint8_t* buf;    // this warp's 8 KiB staging area
   int iter;        // tiles processed so far by this warp
+  int last_buf;    // staging half read by the most recent bulk group (-1: none)
 };
+
+// Before overwriting staging half b: if the most recent bulk group reads b,
+// wait for every group; otherwise all but that most recent one (older groups
+// may have used b).  Correct however many stores were skipped.
+__device__ __forceinline__ void staging_acquire(EpiCtx& e, int b) {
+  if (lane_id() == 0) {
+    if (e.last_buf == b) {
+      bulk_wait_read<0>();
+    } else {
+      bulk_wait_read<1>();
+    }
+  }
+  __syncwarp();
+}
 
 __device__ __forceinline__ void release_tmem(const SmemLayout& L, int acc) {
   tc_fence_before();
@@ -359,6 +374,7 @@ __device__ __forceinline__ bool epi_bwd_g(const GemmArgs& a, const SmemLayout& L
   for (int h = 0; h < 2; ++h) {
     if (lane == 0) bulk_wait_read<0>();  // staging buffer free again
     __syncwarp();
+    e.last_buf = -1;
     bool surv = false;
 #pragma unroll 1
     for (int cc = 0; cc < 4; ++cc) {
@@ -427,11 +443,14 @@ __device__ __forceinline__ void epi_dc(const GemmArgs& a, const SmemLayout& L, c
   const uint32_t lane = lane_id();
   const bool empty = tile_empty<MODE_DC>(a, t);
   const uint32_t tbase = e.taddr + static_cast<uint32_t>(acc * BN);
+  const int gy = a.chunk_v0 + t.m * BM + e.q * 32;
+  // boxes that start inside dC (no store may start outside the tensor)
+  const int nbox = (gy < a.V) ? min(BN / 64, (a.D - t.n * BN + 63) / 64) : 0;
 #pragma unroll 1
-  for (int j = 0; j < BN / 64; ++j) {
-    uint8_t* buf = e.buf + (j & 1) * 4096;
-    if (lane == 0) bulk_wait_read<1>();
-    __syncwarp();
+  for (int j = 0; j < nbox; ++j) {
+    const int b = j & 1;
+    uint8_t* buf = e.buf + b * 4096;
+    staging_acquire(e, b);
     const uint32_t sb = smem_u32(buf);
     if (!empty) {
       uint32_t r0[32], r1[32];
@@ -454,15 +473,15 @@ __device__ __forceinline__ void epi_dc(const GemmArgs& a, const SmemLayout& L, c
 #pragma unroll
       for (int u = 0; u < 8; ++u) st_shared_v4(sb + swz(lane, u), 0u, 0u, 0u, 0u);
     }
-    if (j == BN / 64 - 1) release_tmem(L, acc);
     fence_proxy_async_smem();
     __syncwarp();
-    const int gx = t.n * BN + 64 * j, gy = a.chunk_v0 + t.m * BM + e.q * 32;
-    if (lane == 0 && gx < a.D && gy < a.V) {  // no store starts outside dC
-      tma_store_2d(&a.tmOut, buf, gx, gy);
+    if (lane == 0) {
+      tma_store_2d(&a.tmOut, buf, t.n * BN + 64 * j, gy);
       bulk_commit();
     }
+    e.last_buf = b;
   }
+  release_tmem(L, acc);
 }
 
 // DE: fp32 output tile, rows = tokens, cols = D; store (first chunk) or reduce-add.
@@ -474,11 +493,14 @@ __device__ __forceinline__ void epi_de(const GemmArgs& a, const SmemLayout& L, c
     return;
   }
   const uint32_t tbase = e.taddr + static_cast<uint32_t>(acc * BN);
+  const int gy = t.m * BM + e.q * 32;
+  // boxes that start inside dE (no store or reduce may start outside the tensor)
+  const int nbox = (gy < a.N) ? min(BN / 32, (a.D - t.n * BN + 31) / 32) : 0;
 #pragma unroll 1
-  for (int j = 0; j < BN / 32; ++j) {
-    uint8_t* buf = e.buf + (j & 1) * 4096;
-    if (lane == 0) bulk_wait_read<1>();
-    __syncwarp();
+  for (int j = 0; j < nbox; ++j) {
+    const int b = j & 1;
+    uint8_t* buf = e.buf + b * 4096;
+    staging_acquire(e, b);
     const uint32_t sb = smem_u32(buf);
     if (!empty) {
       uint32_t r[32];
@@ -490,19 +512,19 @@ __device__ __forceinline__ void epi_de(const GemmArgs& a, const SmemLayout& L, c
 #pragma unroll
       for (int u = 0; u < 8; ++u) st_shared_v4(sb + swz(lane, u), 0u, 0u, 0u, 0u);
     }
-    if (j == BN / 32 - 1) release_tmem(L, acc);
     fence_proxy_async_smem();
     __syncwarp();
-    const int gx = t.n * BN + 32 * j, gy = t.m * BM + e.q * 32;
-    if (lane == 0 && gx < a.D && gy < a.N) {  // no store starts outside dE
+    if (lane == 0) {
       if (a.first_chunk) {
-        tma_store_2d(&a.tmOut, buf, gx, gy);
+        tma_store_2d(&a.tmOut, buf, t.n * BN + 32 * j, gy);
       } else {
-        tma_reduce_add_2d(&a.tmOut, buf, gx, gy);
+        tma_reduce_add_2d(&a.tmOut, buf, t.n * BN + 32 * j, gy);
       }
       bulk_commit();
     }
+    e.last_buf = b;
   }
+  release_tmem(L, acc);
 }
 
 template <int MODE>
@@ -513,6 +535,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& a, const SmemLayou
   e.taddr = tmem_base + (static_cast<uint32_t>(e.q * 32) << 16);
   e.buf = L.epi + (warp - 2) * EPI_WARP_BYTES;
   e.iter = 0;
+  e.last_buf = -1;
   FwdState st{NEG_BIG, 0.0f};
   int acc = 0;
   uint32_t acc_phase = 0;

@@ -17,3 +17,9 @@ def pytest_configure(config):
 def rng():
     import numpy as np
     return np.random.default_rng(1234)
+
+
+def build_library():
+    """Build libcce.so if it is stale (loads build.py by path, see __graft_entry__)."""
+    import __graft_entry__
+    __graft_entry__._build_module().build()

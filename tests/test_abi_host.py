@@ -13,8 +13,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def lib():
-    from linear_cross_entropy_gb300 import build as B
-    B.build()
+    from tests.conftest import build_library
+    build_library()
     from linear_cross_entropy_gb300 import _lib
     return _lib.load()
 

@@ -20,8 +20,8 @@ pytestmark = pytest.mark.gpu
 def _built():
     if not torch.cuda.is_available():
         pytest.skip("needs a GPU")
-    from linear_cross_entropy_gb300 import build
-    build.build()
+    from tests.conftest import build_library
+    build_library()
 
 
 @pytest.mark.parametrize("filter_on", [True, False])
