@@ -1,0 +1,412 @@
+"""Benchmark of the Cut Cross-Entropy hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+                    [--config qwen] [--filter on|off]
+
+One step = cce_forward + cce_backward (every stage of the path: LSE GEMM with
+target capture, combine + reduction, target count, recompute + G + filter,
+dC GEMM, dE GEMM, dE finalise) over one batch of the seeded synthetic
+workload, inputs resident in HBM.  Prints one JSON line (rank 0).
+
+Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
+and torch.cuda.synchronize() on both sides, CUDA events on the launching
+stream, max over ranks.  Multi-GPU runs (torchrun) are independent replicas
+(the path does not shard): value = tokens of all ranks / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import cce_workloads as W  # noqa: E402
+
+METRIC = "CCE fwd+bwd tokens/s and % of bf16 tensor peak; peak extra HBM bytes"
+UNIT = "tokens/s"
+DEFAULT_CONFIG = "qwen"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+GEMM_PHASES = ("fwd_lse_gemm", "bwd_recompute_g", "bwd_dC_gemm", "bwd_dE_gemm")
+SOURCE_FILES = ("linear_cross_entropy_gb300/csrc/gemm.cuh", "linear_cross_entropy_gb300/csrc/ptx.cuh",
+                "linear_cross_entropy_gb300/csrc/gemm_args.h")
+WORKLOAD_NAMES = {
+    "tiny": "tiny CCE head", "qwen": "Qwen2.5-0.5B-shaped head", "gemma": "Gemma-2-2B-shaped head",
+    "llama": "Llama-3-8B-shaped head", "long": "long-context filter stress",
+}
+
+
+# --------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    for rel in SOURCE_FILES:
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_phase: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    cur = source_digest()
+    with open(path) as fh:
+        for line in fh:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            f = dict(kv.split("=", 1) for kv in line.split())
+            if f.get("phase") == kernel_phase and f.get("workload") == workload and f.get("source") == cur:
+                return float(f["dram_bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def reduce_max(value: float, dist, device) -> float:
+    """Max of a per-rank float over all ranks (identity without a process group)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(elapsed_ms_by_rank, tokens_per_step, steps):
+    """Whole-job throughput: tokens of all ranks / max time over ranks."""
+    t = max(elapsed_ms_by_rank)
+    world = len(elapsed_ms_by_rank)
+    return {"value": tokens_per_step * steps * world / (t / 1e3), "ms_per_step": t / steps}
+
+
+# ---------------------------------------------------------- CPU oracle
+def oracle_sample_rate(w: W.Workload, E_bits, C_bits, x, target_s: float = 12.0):
+    """Times the fp64 oracle (as it stands) on a bounded sample: forward +
+    backward of the first k token rows as a standalone batch, k grown until a
+    run takes a few seconds.  Returns (tokens/s, sample description, cores)."""
+    import oracle
+    C = oracle.widen_bf16(C_bits)
+    E = oracle.widen_bf16(E_bits[: min(w.N, 4096)])
+    k, spent, rate = 8, 0.0, None
+    while True:
+        rows = np.arange(k)
+        t0 = time.perf_counter()
+        oracle.fwd_bwd_rows(E, C, x, rows, reduction=w.reduction)
+        dt = time.perf_counter() - t0
+        spent += dt
+        rate = k / dt
+        if dt > target_s / 3 or spent > target_s or 2 * k > E.shape[0]:
+            break
+        k = min(E.shape[0], max(2 * k, int(k * (target_s / 3) / max(dt, 1e-3))))
+    sample = (f"fp64 oracle forward+backward of the first {k} tokens of the workload as a standalone batch "
+              f"(V={w.V}, D={w.D}); {dt:.1f} s")
+    return rate, sample, os.cpu_count() or 1
+
+
+# ----------------------------------------------------------- GPU arm
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import linear_cross_entropy_gb300 as cce
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = W.CONFIGS[args.config]
+    eps = W_FILTER_EPS if args.filter == "on" else 0.0
+    E_bits, C_bits, x = W.make_inputs(w)
+    N, D, V = w.N, w.D, w.V
+    E = torch.from_numpy(E_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    C = torch.from_numpy(C_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    xt = torch.from_numpy(x).to(dev)
+    red = w.reduction
+    g = torch.ones(N if red == "none" else 1, dtype=torch.float32, device=dev)
+    ws_f = torch.empty(cce.forward_workspace_bytes(N, D, V), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(cce.backward_workspace_bytes(N, D, V), dtype=torch.uint8, device=dev)
+    dE = torch.empty_like(E)
+    dC = torch.empty_like(C)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stats = torch.zeros(2, dtype=torch.int64, device=dev)
+
+    def step():
+        loss, lse = cce.cce_forward(E, C, xt, -100, red, workspace=ws_f, dev_err=err, check_errors=False)
+        cce.cce_backward(E, C, xt, lse, g, -100, red, eps, workspace=ws_b, dev_err=err, check_errors=False,
+                         dE=dE, dC=dC)
+        return loss
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    # filter statistics and peak extra memory of one step (untimed)
+    torch.cuda.reset_peak_memory_stats(dev)
+    base = torch.cuda.memory_allocated(dev)
+    loss, lse = cce.cce_forward(E, C, xt, -100, red, dev_err=err, check_errors=False)
+    _, _, st = cce.cce_backward(E, C, xt, lse, g, -100, red, eps, dev_err=err, check_errors=False, stats=True)
+    torch.cuda.synchronize()
+    outputs = dE.numel() * 2 + dC.numel() * 2 + N * 4 + (N * 4 if red == "none" else 4) + 16
+    peak_extra = torch.cuda.max_memory_allocated(dev) - base - outputs
+    kept = 1.0 - st["skipped"] / max(st["tiles"], 1)
+    del loss, lse
+
+    stream = torch.cuda.current_stream(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = cce.kernel_launch_count()
+    uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    with ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local_rank)) as clocks, cce.Profiler():
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    phases = cce.Profiler.read()
+    launches = cce.kernel_launch_count() - launches0
+    elapsed = ev0.elapsed_time(ev1)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} set during the timed steps")
+    elapsed_max = reduce_max(elapsed, dist, dev)
+    if dist:
+        dist.barrier()
+    agg = aggregate([elapsed_max] * world, N, args.steps)
+
+    # end to end through the public API: pinned host inputs copied in, loss read back, every step
+    Eh = torch.from_numpy(E_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    Ch = torch.from_numpy(C_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    xh = torch.from_numpy(x).pin_memory()
+    Ed, Cd, xd = torch.empty_like(E), torch.empty_like(C), torch.empty_like(xt)
+    loss_h = torch.empty(1, dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        Ed.copy_(Eh, non_blocking=True)
+        Cd.copy_(Ch, non_blocking=True)
+        xd.copy_(xh, non_blocking=True)
+        Ed.requires_grad_(True)
+        Cd.requires_grad_(True)
+        loss = cce.linear_cross_entropy(Ed, Cd, xd, -100, red, eps)
+        loss.backward()
+        loss_h.copy_(loss.detach().reshape(1), non_blocking=True)
+        Ed.requires_grad_(False)
+        Cd.requires_grad_(False)
+        Ed.grad = None
+        Cd.grad = None
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    e2e = {"value": N * e2e_steps / e2e_s, "unit": UNIT,
+           "h2d_bytes_per_step": Eh.numel() * 2 + Ch.numel() * 2 + xh.numel() * 8, "d2h_bytes_per_step": 4,
+           "steps": e2e_steps, "api": "linear_cross_entropy + backward (autograd Function over the C ABI)"}
+
+    # roofline of the dominant GEMM phase, timed live with the library's events
+    peaks, peak_src = load_peaks()
+    flops = {"fwd_lse_gemm": 2.0 * N * D * V, "bwd_recompute_g": 2.0 * N * D * V,
+             "bwd_dC_gemm": 2.0 * N * D * V * kept, "bwd_dE_gemm": 2.0 * N * D * V * kept}
+    phase_rep = {}
+    for name, ms in phases.ms.items():
+        n_l = phases.launches[name]
+        if n_l == 0:
+            continue
+        rep = {"ms_per_step": ms / args.steps, "launches_per_step": n_l / args.steps}
+        if name in flops:
+            rep["tflops"] = flops[name] * args.steps / (ms / 1e3) / 1e12
+        phase_rep[name] = rep
+    dom = max(GEMM_PHASES, key=lambda p: phases.ms.get(p, 0.0))
+    achieved = phase_rep[dom]["tflops"]
+    peak = peaks["bf16_tflops_sustained"]
+    launches_dom = phases.launches[dom] / args.steps
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "peak_kind": f"sustained bf16 ({peak_src})",
+                "frac_of_burst_peak": round(achieved / peaks["bf16_tflops"], 4),
+                "traffic": recorded_traffic(dom, args.config),
+                "algorithmic_flops_per_launch": flops[dom] / launches_dom}
+    total_flops = 8.0 * N * D * V
+    out = {
+        "metric": METRIC, "value": round(agg["value"], 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(agg["ms_per_step"], 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD_NAMES[args.config]} N={N} D={D} V={V}", "N": N, "D": D, "V": V,
+                   "reduction": red, "filter_eps": eps, "ignore_frac": w.ignore_frac,
+                   "l2": f"inputs larger than L2 (C is {C.numel() * 2 / 1e6:.0f} MB)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "tflops_8NDV": round(total_flops / (agg["ms_per_step"] / 1e3) / 1e12, 1),
+        "frac_of_bf16_peak_8NDV": round(total_flops / (agg["ms_per_step"] / 1e3) / 1e12 / peak, 4),
+        "tiles_skipped_frac": round(st["skipped"] / max(st["tiles"], 1), 4),
+        "peak_extra_hbm_bytes": int(peak_extra),
+        "roofline": roofline, "phases": phase_rep, "e2e": e2e, "gpu_launches": int(launches),
+        "clocks": clocks.summary(),
+    }
+    del Eh, Ch, Ed, Cd
+    return out, (w, E_bits, C_bits, x)
+
+
+W_FILTER_EPS = 2.0 ** -12
+
+
+def run_reference(args):
+    """The fp64 oracle on the host cores: each step one bounded sample."""
+    import oracle
+    w = W.CONFIGS[args.config]
+    E_bits, C_bits, x = W.make_inputs(w)
+    rate, sample, cores = oracle_sample_rate(w, E_bits, C_bits, x, target_s=6.0)
+    k = max(1, int(round(rate * 3.0)))  # ~3 s per step
+    C = oracle.widen_bf16(C_bits)
+    E = oracle.widen_bf16(E_bits[:k])
+    rows = np.arange(k)
+    for _ in range(args.warmup):
+        oracle.fwd_bwd_rows(E, C, x, rows, reduction=w.reduction)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.fwd_bwd_rows(E, C, x, rows, reduction=w.reduction)
+    dt = time.perf_counter() - t0
+    value = k * args.steps / dt
+    desc = (f"each step: fp64 oracle forward+backward of the first {k} tokens of the workload as a standalone "
+            f"batch (V={w.V}, D={w.D})")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD_NAMES[args.config]} N={w.N} D={w.D} V={w.V}", "N": w.N, "D": w.D,
+                   "V": w.V, "reduction": w.reduction},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    ap.add_argument("--config", choices=tuple(W.CONFIGS), default=DEFAULT_CONFIG)
+    ap.add_argument("--filter", choices=("on", "off"), default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.filter is None:
+        args.filter = W.CONFIGS[args.config].filter_modes[0]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    out, inputs = run_gpu(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            w, E_bits, C_bits, x = inputs
+            rate, sample, cores = oracle_sample_rate(w, E_bits, C_bits, x)
+            out["cpu_baseline"] = {"value": round(rate, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+                                   "sample": sample}
+        else:
+            out["cpu_baseline"] = None
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
