@@ -358,3 +358,38 @@ def _transposed_logits(E, C):
 ])
 def test_planted_mistake_is_caught(rng, name, overrides):
     assert _pin_suite(_mutant(**overrides), rng) != [], name
+
+
+def test_indexed_logits_match_gathered_torch_logits(rng):
+    """Algorithm 1 (indexed matmul): o_i = C[x_i] . E_i equals the gathered
+    entry of torch's materialised logit matrix; NaN on ignored rows."""
+    E, C, x = _problem(rng, 40, 12, 90, ignore=(3, 7))
+    o = O.indexed_logits(E, C, x)
+    ok = x != O.IGNORE_INDEX
+    full = (torch.tensor(E) @ torch.tensor(C).T).numpy()
+    assert np.allclose(o[ok], full[np.nonzero(ok)[0], x[ok]], rtol=1e-14)
+    assert np.all(np.isnan(o[~ok]))
+    f = O.forward(E, C, x, reduction="none")
+    assert np.allclose(f["target_logit"][ok], o[ok], rtol=1e-14)
+
+
+def test_fwd_bwd_rows_is_the_sub_batch(rng):
+    """The timed CPU sample (a standalone sub-batch) equals torch cross_entropy
+    on that sub-batch's materialised logits."""
+    E, C, x = _problem(rng, 30, 8, 70, ignore=(2,))
+    rows = np.array([0, 2, 5, 11, 29])
+    loss, dE, dC = O.fwd_bwd_rows(E, C, x, rows, reduction="mean")
+    Et = torch.tensor(E[rows], requires_grad=True)
+    Ct = torch.tensor(C, requires_grad=True)
+    ref = torch.nn.functional.cross_entropy(Et @ Ct.T, torch.tensor(x[rows]), reduction="mean")
+    ref.backward()
+    assert loss == pytest.approx(ref.item(), rel=1e-13)
+    assert np.allclose(dE, Et.grad.numpy(), rtol=1e-12, atol=1e-15)
+    assert np.allclose(dC, Ct.grad.numpy(), rtol=1e-12, atol=1e-15)
+
+
+def test_widen_bf16_is_exact():
+    """bf16 -> float64 widening: bit patterns of known values."""
+    bits = np.array([0x3F80, 0xC000, 0x0000, 0x8000, 0x3E80, 0x7F7F], dtype=np.uint16)
+    assert O.widen_bf16(bits).tolist()[:5] == [1.0, -2.0, 0.0, -0.0, 0.25]
+    assert O.widen_bf16(bits)[5] == float(np.float32(3.3895313892515355e38))
