@@ -129,6 +129,33 @@ cce_status cce_backward(const void* E, const void* C, const int64_t* x, const fl
                         int reduction, float filter_eps, void* dE, void* dC, void* workspace,
                         size_t ws_bytes, int32_t* dev_err, int64_t* dev_stats, void* stream);
 
+/*
+ * Forward pass that allocates nothing and takes no workspace.  The pages
+ * have no counterpart to this call: it exists for callers that cannot
+ * allocate device memory where they need the loss -- code inside a CUDA-graph
+ * capture that must not allocate, runtimes whose device memory is entirely
+ * owned by their own pool, or hosts that forbid allocation on the hot path.
+ * Instead of a caller workspace it uses a scratch array of
+ * CCE_NOALLOC_SCRATCH_BYTES that the library declares in device memory; every
+ * GPU that loads the library holds that array until the process exits.
+ *
+ * Arguments, layouts, results and checks are those of cce_forward (it runs
+ * the same kernels), minus workspace/ws_bytes.  Returns CCE_ERR_WORKSPACE,
+ * launching nothing, when cce_forward_workspace_bytes(N, D, V) exceeds
+ * CCE_NOALLOC_SCRATCH_BYTES (16 MiB; query that function to know whether a
+ * size fits -- the five benchmark workloads, up to N = 65,536 tokens, need at
+ * most 10 MiB).  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture starts.  All calls share the one
+ * array: calls whose GPU work overlaps (e.g. on two streams at once) race and
+ * must be serialised by the caller.  It never calls cudaMalloc, cudaFree or
+ * any allocating routine.
+ */
+#define CCE_NOALLOC_SCRATCH_BYTES (16u << 20)
+cce_status cce_forward_noalloc(const void* E, const void* C, const int64_t* x, int64_t N, int64_t D, int64_t V,
+                               int64_t ignore_index, int reduction, float* loss, float* lse, int32_t* dev_err,
+                               void* stream);
+
 /* Memory accounting (host arithmetic, no GPU).  Reproduces the page's memory
  * table ("Cut Cross-Entropy: Training Loss Without the Logit Matrix ...",
  * section "The memory numbers hold up"): the fp32 N x V logit buffer that the
