@@ -224,7 +224,7 @@ FwdLayout fwd_layout(int64_t N, int64_t V) {
 }
 
 struct BwdLayout {
-  size_t count, bitmap, gbuf, deacc, total;
+  size_t count, bitmap, bitmapT, gbuf, deacc, total;
   int64_t vc, bm_ld, n128;
 };
 
@@ -237,6 +237,8 @@ BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V) {
   L.count = o;
   o = align_up(o + sizeof(int), ALIGN);
   L.bitmap = o;
+  o = align_up(o + static_cast<size_t>(L.n128 * L.bm_ld), ALIGN);
+  L.bitmapT = o;
   o = align_up(o + static_cast<size_t>(L.n128 * L.bm_ld), ALIGN);
   L.gbuf = o;
   o = align_up(o + static_cast<size_t>(N) * L.vc * 2, ALIGN);
@@ -546,10 +548,14 @@ cce_status cce_backward(const void* E, const void* C, const int64_t* x, const fl
     p->reduction = reduction;
     p->eps = filter_eps;
     p->bitmap = bitmap;
+    p->bitmapT = ws + W.bitmapT;
     p->bm_ld = static_cast<int>(W.bm_ld);
     p->dev_err = dev_err;
   }
   g.k_blocks = static_cast<int>(cdiv(D, BK));
+  // Raster groups whose E rows (group_n * 128 * D * 2 bytes) stay around 32 MiB.
+  g.group_n = static_cast<int>(std::max<int64_t>(
+      1, std::min<int64_t>(cdiv(N, BM), std::max<int64_t>(8, (int64_t(32) << 20) / (BM * 2 * D)))));
   c.k_blocks = static_cast<int>(cdiv(N, BK));
   c.n_tiles = static_cast<int>(cdiv(D, BN));
   d.n_tiles = c.n_tiles;

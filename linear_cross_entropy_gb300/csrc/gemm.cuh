@@ -62,9 +62,15 @@ __device__ __forceinline__ void for_each_tile(const GemmArgs& a, F&& f) {
       }
     }
   } else if constexpr (MODE == MODE_BWD_G) {
+    // Grouped raster: groups of group_n token blocks; inside a group the
+    // token block varies fastest, then the vocabulary tile.  CTAs running at
+    // the same time share a few C tiles and a group's E rows stay in L2.
     const int total = a.n_blocks * a.v_tiles;
+    const int per_group = a.group_n * a.v_tiles;
     for (int i = blockIdx.x; i < total; i += gridDim.x) {
-      if (!f(Tile{i % a.n_blocks, i / a.n_blocks, 0, true, true})) return;
+      const int g = i / per_group, j = i - g * per_group;
+      const int gn = min(a.group_n, a.n_blocks - g * a.group_n);
+      if (!f(Tile{g * a.group_n + j % gn, j / gn, 0, true, true})) return;
     }
   } else {
     const int total = a.m_tiles * a.n_tiles;
@@ -78,8 +84,8 @@ __device__ __forceinline__ void for_each_tile(const GemmArgs& a, F&& f) {
 // chunk columns.)  FWD and BWD_G never skip.
 template <int MODE>
 __device__ __forceinline__ bool kblock_skipped(const GemmArgs& a, const Tile& t, int kb) {
-  if constexpr (MODE == MODE_DC) {
-    return __ldg(a.bitmap + static_cast<size_t>(kb >> 1) * a.bm_ld + (a.chunk_v0 >> 7) + t.m) == 0;
+  if constexpr (MODE == MODE_DC) {  // contiguous along K: L1 hits
+    return __ldg(a.bitmapT + static_cast<size_t>((a.chunk_v0 >> 7) + t.m) * a.n_blocks + (kb >> 1)) == 0;
   } else if constexpr (MODE == MODE_DE) {
     return __ldg(a.bitmap + static_cast<size_t>(t.m) * a.bm_ld + (a.chunk_v0 >> 7) + (kb >> 1)) == 0;
   } else {
@@ -92,8 +98,8 @@ template <int MODE>
 __device__ __forceinline__ bool tile_empty(const GemmArgs& a, const Tile& t) {
   int any = 0;
   if constexpr (MODE == MODE_DC) {
-    const int col = (a.chunk_v0 >> 7) + t.m;
-    for (int r = lane_id(); r < a.n_blocks; r += 32) any |= __ldg(a.bitmap + static_cast<size_t>(r) * a.bm_ld + col);
+    const uint8_t* row = a.bitmapT + static_cast<size_t>((a.chunk_v0 >> 7) + t.m) * a.n_blocks;
+    for (int r = lane_id(); r < a.n_blocks; r += 32) any |= __ldg(row + r);
   } else if constexpr (MODE == MODE_DE) {
     const int ncols = (a.chunk_w + FILTER_TILE - 1) / FILTER_TILE;
     const uint8_t* row = a.bitmap + static_cast<size_t>(t.m) * a.bm_ld + (a.chunk_v0 >> 7);
@@ -432,7 +438,10 @@ __device__ __forceinline__ bool epi_bwd_g(const GemmArgs& a, const SmemLayout& L
     }
     if (e.q == 0 && lane == 0) {
       const int vt128 = (vt0 >> 7) + h;
-      if (vt128 < a.bm_ld) a.bitmap[static_cast<size_t>(t.m) * a.bm_ld + vt128] = keep ? 1 : 0;
+      if (vt128 < a.bm_ld) {
+        a.bitmap[static_cast<size_t>(t.m) * a.bm_ld + vt128] = keep ? 1 : 0;
+        a.bitmapT[static_cast<size_t>(vt128) * a.n_blocks + t.m] = keep ? 1 : 0;
+      }
     }
   }
   return ok;

@@ -49,8 +49,10 @@ struct GemmArgs {
   const int* count;
   int reduction;
   float eps;
-  uint8_t* bitmap;  // [ceil(N/128)][bm_ld] tile survival
-  int bm_ld;        // ceil(V / 128)
+  uint8_t* bitmap;   // [ceil(N/128)][bm_ld] tile survival, token-block major
+  uint8_t* bitmapT;  // [bm_ld][ceil(N/128)] the same, vocabulary-block major (read along K by dC)
+  int bm_ld;         // ceil(V / 128)
+  int group_n;       // BWD_G: token blocks per raster group
   int32_t* dev_err;
 };
 

@@ -70,7 +70,7 @@ def test_workspace_queries(lib, N, D, V):
     if V > 256:
         assert r["bwd_chunk_cols"] < V
     assert N * r["bwd_chunk_cols"] * 2 <= max(512 << 20, N * 256 * 2)
-    assert b <= N * D * 4 + N * r["bwd_chunk_cols"] * 2 + (N // 128 + 1) * (V // 128 + 1) + 4096
+    assert b <= N * D * 4 + N * r["bwd_chunk_cols"] * 2 + 2 * (N // 128 + 1) * (V // 128 + 1) + 4096
     assert f < N * V * 4 or V < 1024
 
 
