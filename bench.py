@@ -38,7 +38,7 @@ METRIC = "CCE fwd+bwd tokens/s and % of bf16 tensor peak; peak extra HBM bytes"
 UNIT = "tokens/s"
 DEFAULT_CONFIG = "qwen"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-GEMM_PHASES = ("fwd_lse_gemm", "bwd_recompute_g", "bwd_dC_gemm", "bwd_dE_gemm")
+GEMM_PHASES = ("fwd_lse_gemm", "bwd_recompute_g", "bwd_grad_gemm")
 SOURCE_FILES = ("linear_cross_entropy_gb300/csrc/gemm.cuh", "linear_cross_entropy_gb300/csrc/ptx.cuh",
                 "linear_cross_entropy_gb300/csrc/gemm_args.h")
 WORKLOAD_NAMES = {
@@ -290,7 +290,7 @@ def run_gpu(args, rank, world, local_rank):
     # roofline of the dominant GEMM phase, timed live with the library's events
     peaks, peak_src = load_peaks()
     flops = {"fwd_lse_gemm": 2.0 * N * D * V, "bwd_recompute_g": 2.0 * N * D * V,
-             "bwd_dC_gemm": 2.0 * N * D * V * kept, "bwd_dE_gemm": 2.0 * N * D * V * kept}
+             "bwd_grad_gemm": 4.0 * N * D * V * kept}
     phase_rep = {}
     for name, ms in phases.ms.items():
         n_l = phases.launches[name]

@@ -188,8 +188,8 @@ uint64_t cce_kernel_launch_count(void);
  * cce_profile_read synchronises on those events and returns, per phase, the
  * summed milliseconds and the number of launches since the last reset.
  * Phases: 0 fwd_lse_gemm, 1 fwd_combine, 2 bwd_prep, 3 bwd_recompute_g,
- * 4 bwd_dC_gemm, 5 bwd_dE_gemm, 6 bwd_finalize. */
-#define CCE_NUM_PHASES 7
+ * 4 bwd_grad_gemm (dC and dE of a vocabulary chunk, one launch), 5 bwd_finalize. */
+#define CCE_NUM_PHASES 6
 cce_status cce_profile_enable(int enable);
 cce_status cce_profile_reset(void);
 cce_status cce_profile_read(double* ms /* host [CCE_NUM_PHASES] */, int64_t* launches /* host [CCE_NUM_PHASES] */);

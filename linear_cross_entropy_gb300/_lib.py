@@ -21,7 +21,7 @@ STATUS_NAMES = {
 RED = {"none": 0, "sum": 1, "mean": 2}
 DEVERR_TARGET_RANGE = 1
 DEVERR_TIMEOUT = 2
-NUM_PHASES = 7
+NUM_PHASES = 6
 
 
 class CCEError(RuntimeError):

@@ -199,8 +199,25 @@ int64_t bwd_chunk_cols(int64_t N, int64_t V) {
   return std::min(vc, vpad);
 }
 
+// Width of the D tiles of the gradient GEMMs: the multiple of 32 (128..256, or
+// D rounded up to 32 when D < 128) that wastes the fewest MMA columns,
+// preferring wider tiles.
+int grad_tile_width(int64_t D) {
+  if (D < 128) return static_cast<int>(cdiv(D, 32) * 32);
+  int best = BN;
+  int64_t best_pad = cdiv(D, BN) * BN;
+  for (int bn = BN - 32; bn >= 128; bn -= 32) {
+    const int64_t pad = cdiv(D, bn) * bn;
+    if (pad < best_pad) {
+      best = bn;
+      best_pad = pad;
+    }
+  }
+  return best;
+}
+
 struct FwdLayout {
-  size_t part_m, part_s, tgt, blk_sum, blk_cnt, total;
+  size_t counter, part_m, part_s, tgt, blk_sum, blk_cnt, total;
   int S, nblk;
 };
 
@@ -209,6 +226,8 @@ FwdLayout fwd_layout(int64_t N, int64_t V) {
   L.S = fwd_splits(N, V);
   L.nblk = static_cast<int>(cdiv(N, COMBINE_THREADS));
   size_t o = 0;
+  L.counter = o;
+  o = align_up(o + sizeof(int), ALIGN);
   L.part_m = o;
   o = align_up(o + sizeof(float) * L.S * N, ALIGN);
   L.part_s = o;
@@ -224,8 +243,8 @@ FwdLayout fwd_layout(int64_t N, int64_t V) {
 }
 
 struct BwdLayout {
-  size_t count, bitmap, bitmapT, gbuf, deacc, total;
-  int64_t vc, bm_ld, n128;
+  size_t count, counters, bitmap, bitmapT, gbuf, deacc, total;
+  int64_t vc, bm_ld, n128, nchunks;
 };
 
 BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V) {
@@ -233,9 +252,12 @@ BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V) {
   L.vc = bwd_chunk_cols(N, V);
   L.bm_ld = cdiv(V, 128);
   L.n128 = cdiv(N, 128);
+  L.nchunks = cdiv(V, L.vc);
   size_t o = 0;
   L.count = o;
   o = align_up(o + sizeof(int), ALIGN);
+  L.counters = o;  // two scheduler counters per chunk
+  o = align_up(o + sizeof(int) * 2 * static_cast<size_t>(L.nchunks), ALIGN);
   L.bitmap = o;
   o = align_up(o + static_cast<size_t>(L.n128 * L.bm_ld), ALIGN);
   L.bitmapT = o;
@@ -307,15 +329,17 @@ cce_status device_check(int* sms) {
   return CCE_OK;
 }
 
-// 2-D row-major tensor map with a 128-byte-swizzled box (inner box = 128 B).
+// 2-D row-major tensor map; the box's inner extent is the swizzle span (128 B
+// by default, 64 B for the dC store box).
 bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* ptr, uint64_t inner,
-               uint64_t outer, uint64_t pitch_elems, uint32_t box_inner, uint32_t box_outer) {
+               uint64_t outer, uint64_t pitch_elems, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {pitch_elems * esize};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
   CUresult r = g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -457,10 +481,14 @@ cce_status cce_forward(const void* E, const void* C, const int64_t* x, int64_t N
   a.part_s = reinterpret_cast<float*>(ws + W.part_s);
   a.tgt = reinterpret_cast<float*>(ws + W.tgt);
   a.dev_err = dev_err;
+  a.counter = reinterpret_cast<int*>(ws + W.counter);
   const int units = a.n_blocks * a.splits;
+  a.items = units;
   {
     PhaseScope ps(0, s);
-    cudaError_t e = launch_gemm(MODE_FWD, a, std::min(units, sms), s);
+    cudaError_t e = cudaMemsetAsync(a.counter, 0, sizeof(int), s);
+    if (e != cudaSuccess) return cuda_status(e);
+    e = launch_gemm(MODE_FWD, a, std::min(units, sms), s);
     g_launches++;
     if (e != cudaSuccess) return cuda_status(e);
   }
@@ -518,24 +546,22 @@ cce_status cce_backward(const void* E, const void* C, const int64_t* x, const fl
 
   GemmArgs g;  // recompute + G
   std::memset(&g, 0, sizeof(g));
-  GemmArgs c;  // dC
-  std::memset(&c, 0, sizeof(c));
-  GemmArgs d;  // dE
-  std::memset(&d, 0, sizeof(d));
+  GemmArgs r;  // dC and dE of the chunk
+  std::memset(&r, 0, sizeof(r));
   const uint64_t vc = static_cast<uint64_t>(W.vc);
   bool ok = true;
   ok &= make_tmap(&g.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, E, D, N, D, BK, BM);
   ok &= make_tmap(&g.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, D, V, D, BK, BN);
   ok &= make_tmap(&g.tmOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, gbuf, vc, N, vc, 64, 32);
-  ok &= make_tmap(&c.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, gbuf, vc, N, vc, 64, 64);
-  ok &= make_tmap(&c.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, E, D, N, D, 64, 64);
-  ok &= make_tmap(&c.tmOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dC, D, V, D, 64, 32);
-  ok &= make_tmap(&d.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, gbuf, vc, N, vc, 64, BM);
-  ok &= make_tmap(&d.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, D, V, D, 64, 64);
-  ok &= make_tmap(&d.tmOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, deacc, D, N, D, 32, 32);
+  ok &= make_tmap(&r.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, gbuf, vc, N, vc, 64, 64);
+  ok &= make_tmap(&r.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, E, D, N, D, 64, 64);
+  ok &= make_tmap(&r.tmOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dC, D, V, D, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+  ok &= make_tmap(&r.tmA2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, gbuf, vc, N, vc, 64, BM);
+  ok &= make_tmap(&r.tmB2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, D, V, D, 64, 64);
+  ok &= make_tmap(&r.tmOut2, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, deacc, D, N, D, 32, 32);
   if (!ok) return CCE_ERR_CUDA;
 
-  for (GemmArgs* p : {&g, &c, &d}) {
+  for (GemmArgs* p : {&g, &r}) {
     p->N = static_cast<int>(N);
     p->D = static_cast<int>(D);
     p->V = static_cast<int>(V);
@@ -556,45 +582,47 @@ cce_status cce_backward(const void* E, const void* C, const int64_t* x, const fl
   // Raster groups whose E rows (group_n * 128 * D * 2 bytes) stay around 32 MiB.
   g.group_n = static_cast<int>(std::max<int64_t>(
       1, std::min<int64_t>(cdiv(N, BM), std::max<int64_t>(8, (int64_t(32) << 20) / (BM * 2 * D)))));
-  c.k_blocks = static_cast<int>(cdiv(N, BK));
-  c.n_tiles = static_cast<int>(cdiv(D, BN));
-  d.n_tiles = c.n_tiles;
-  d.m_tiles = static_cast<int>(cdiv(N, BM));
+  r.bn = grad_tile_width(D);
+  r.n_tiles = static_cast<int>(cdiv(D, r.bn));
+  r.dc_k_blocks = static_cast<int>(cdiv(N, BK));
 
-  const int64_t nchunks = cdiv(V, W.vc);
-  for (int64_t ch = 0; ch < nchunks; ++ch) {
+  int* counters = reinterpret_cast<int*>(ws + W.counters);
+  {
+    cudaError_t e = cudaMemsetAsync(counters, 0, sizeof(int) * 2 * static_cast<size_t>(W.nchunks), s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  for (int64_t ch = 0; ch < W.nchunks; ++ch) {
     const int v0 = static_cast<int>(ch * W.vc);
     const int w = static_cast<int>(std::min<int64_t>(W.vc, V - v0));
-    for (GemmArgs* p : {&g, &c, &d}) {
+    for (GemmArgs* p : {&g, &r}) {
       p->chunk_v0 = v0;
       p->chunk_w = w;
     }
     g.v_tiles = static_cast<int>(cdiv(w, BN));
-    c.m_tiles = static_cast<int>(cdiv(w, BM));
-    d.k_blocks = static_cast<int>(cdiv(w, BK));
-    d.first_chunk = (ch == 0) ? 1 : 0;
+    g.items = g.n_blocks * g.v_tiles;
+    g.counter = counters + 2 * ch;
+    r.dc_m_tiles = static_cast<int>(cdiv(w, BM));
+    r.de_k_blocks = static_cast<int>(cdiv(w, BK));
+    r.dc_first = r.dc_k_blocks >= r.de_k_blocks ? 1 : 0;  // longest tiles first
+    r.first_chunk = (ch == 0) ? 1 : 0;
+    r.items = (r.dc_m_tiles + r.n_blocks) * r.n_tiles;
+    r.counter = counters + 2 * ch + 1;
     cudaError_t e;
     {
       PhaseScope ps(3, s);
-      e = launch_gemm(MODE_BWD_G, g, static_cast<int>(std::min<int64_t>(sms, int64_t(g.n_blocks) * g.v_tiles)), s);
+      e = launch_gemm(MODE_BWD_G, g, std::min(sms, g.items), s);
       g_launches++;
       if (e != cudaSuccess) return cuda_status(e);
     }
     {
       PhaseScope ps(4, s);
-      e = launch_gemm(MODE_DC, c, static_cast<int>(std::min<int64_t>(sms, int64_t(c.m_tiles) * c.n_tiles)), s);
-      g_launches++;
-      if (e != cudaSuccess) return cuda_status(e);
-    }
-    {
-      PhaseScope ps(5, s);
-      e = launch_gemm(MODE_DE, d, static_cast<int>(std::min<int64_t>(sms, int64_t(d.m_tiles) * d.n_tiles)), s);
+      e = launch_gemm(MODE_GRAD, r, std::min(sms, r.items), s);
       g_launches++;
       if (e != cudaSuccess) return cuda_status(e);
     }
   }
   {
-    PhaseScope ps(6, s);
+    PhaseScope ps(5, s);
     const size_t n4 = static_cast<size_t>(N) * D / 4;
     const int blocks = static_cast<int>(std::min<size_t>(static_cast<size_t>(sms) * 8, (n4 + 255) / 256));
     finalize_de_kernel<<<std::max(blocks, 1), 256, 0, s>>>(reinterpret_cast<const float4*>(deacc), x,
@@ -653,8 +681,8 @@ cce_status cce_profile_read(double* ms, int64_t* launches) {
 }
 
 const char* cce_profile_phase_name(int phase) {
-  static const char* names[CCE_NUM_PHASES] = {"fwd_lse_gemm",  "fwd_combine", "bwd_prep",   "bwd_recompute_g",
-                                               "bwd_dC_gemm",   "bwd_dE_gemm", "bwd_finalize"};
+  static const char* names[CCE_NUM_PHASES] = {"fwd_lse_gemm",    "fwd_combine",   "bwd_prep",
+                                               "bwd_recompute_g", "bwd_grad_gemm", "bwd_finalize"};
   if (phase < 0 || phase >= CCE_NUM_PHASES) return "";
   return names[phase];
 }

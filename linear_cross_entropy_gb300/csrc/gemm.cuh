@@ -1,12 +1,12 @@
-// Persistent, warp-specialised tcgen05 GEMM with four epilogues -- the four
+// Persistent, warp-specialised tcgen05 GEMM with three epilogue modes -- the
 // dense contractions of Cut Cross-Entropy on one template:
 //
 //   MODE_FWD   A = E [N,D] (K-major), B = C [V,D] (K-major).  Epilogue: each
 //              row folds its logit tile into a running (max, sumexp) over the
-//              CTA's vocabulary split and captures the target logit when its
-//              column passes ("Cut Your Losses in Large-Vocabulary Language
-//              Models", "Memory-Efficient Linear-Log-Sum-Exp, Forward Pass
-//              (Algorithm 2)" and "Memory-Efficient Indexed Matrix
+//              work item's vocabulary split and captures the target logit when
+//              its column passes ("Cut Your Losses in Large-Vocabulary
+//              Language Models", "Memory-Efficient Linear-Log-Sum-Exp, Forward
+//              Pass (Algorithm 2)" and "Memory-Efficient Indexed Matrix
 //              Multiplication (Algorithm 1)"; the online fold of the
 //              "cut-cross-entropy" card's "Method").  Writes per-(row, split)
 //              partials; a separate kernel combines them in a fixed order.
@@ -16,21 +16,23 @@
 //              flag), then G * w rounded to bf16 and stored to the chunk
 //              buffer for surviving 128x128 tiles only ("The Combined Backward
 //              Pass (Algorithm 4)", "Gradient Filtering").
-//   MODE_DC    dC[chunk rows] = G_chunk^T E: A = G_chunk (MN-major), B = E
-//              (MN-major), K = tokens; K-blocks of skipped tiles are not
-//              loaded and issue no MMA.  Each CTA owns its dC rows: written
-//              once in bf16, no atomics.
-//   MODE_DE    dE_acc (+)= G_chunk C_chunk: A = G_chunk (K-major), B = C
-//              (MN-major), K = chunk columns; fp32 tiles stored (first chunk)
-//              or reduce-added by TMA (later chunks) -- one writer per tile
-//              per chunk, chunks in stream order, so the result is
-//              deterministic.
+//   MODE_GRAD  Both gradient contractions of the chunk in one launch:
+//              KIND_DC tiles: dC[chunk rows] = G_chunk^T E (A = G MN-major,
+//              B = E MN-major, K = tokens), each tile owns its dC rows and
+//              writes them once in bf16, no atomics.  KIND_DE tiles: dE_acc
+//              (+)= G_chunk C_chunk (A = G K-major, B = C MN-major, K = chunk
+//              columns), fp32 tiles stored (first chunk) or reduce-added by
+//              TMA (later chunks): one writer per tile per chunk, chunks in
+//              stream order, so the result is deterministic.  K-blocks of
+//              skipped filter tiles are not loaded and issue no MMA.
 //
-// Roles (192 threads): warp 0 lane 0 issues TMA loads into a 4-stage ring;
-// warp 1 owns TMEM (512 columns = two 128x256 fp32 accumulators) and lane 0
-// issues tcgen05.mma; warps 2..5 are the epilogue (warp w reads TMEM lanes
-// 32*(w%4) .. +31, i.e. tile rows).  The accumulator is double-buffered so the
-// epilogue of one tile overlaps the MMAs of the next.
+// Roles (192 threads): warp 0 lane 0 is the scheduler and TMA producer (a
+// 4-stage ring of 48 KiB stages); warp 1 owns TMEM (512 columns = two 128x256
+// fp32 accumulators) and lane 0 issues tcgen05.mma; warps 2..5 are the
+// epilogue (warp w reads TMEM lanes 32*(w%4) .. +31, i.e. tile rows).  Work
+// items are handed out dynamically (atomicAdd on a counter) and passed to the
+// MMA and epilogue warps through a small ring in shared memory, so every CTA
+// stays busy until the work runs out; the longest tiles are handed out first.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -42,70 +44,76 @@
 namespace cce {
 
 struct Tile {
+  int kind;   // KIND_MAIN (FWD, BWD_G), KIND_DC or KIND_DE (GRAD)
   int m;      // A-row block (128)
   int n;      // B-row block (256) or output column block
   int split;  // FWD
   bool first, last;  // FWD: first / last tile of a (row block, split) unit
 };
 
-// The tile sequence of this CTA; every role walks the same sequence.
+// Calls f(tile) for every tile of work item `item`; false if f asked to stop.
 template <int MODE, typename F>
-__device__ __forceinline__ void for_each_tile(const GemmArgs& a, F&& f) {
+__device__ __forceinline__ bool for_each_tile_of_item(const GemmArgs& a, int item, F&& f) {
   if constexpr (MODE == MODE_FWD) {
-    const int units = a.n_blocks * a.splits;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const int m = u % a.n_blocks, s = u / a.n_blocks;
-      const int t0 = static_cast<int>(static_cast<long long>(s) * a.v_tiles / a.splits);
-      const int t1 = static_cast<int>(static_cast<long long>(s + 1) * a.v_tiles / a.splits);
-      for (int t = t0; t < t1; ++t) {
-        if (!f(Tile{m, t, s, t == t0, t == t1 - 1})) return;
-      }
+    const int m = item % a.n_blocks, s = item / a.n_blocks;
+    const int t0 = static_cast<int>(static_cast<long long>(s) * a.v_tiles / a.splits);
+    const int t1 = static_cast<int>(static_cast<long long>(s + 1) * a.v_tiles / a.splits);
+    for (int t = t0; t < t1; ++t) {
+      if (!f(Tile{KIND_MAIN, m, t, s, t == t0, t == t1 - 1})) return false;
     }
+    return true;
   } else if constexpr (MODE == MODE_BWD_G) {
     // Grouped raster: groups of group_n token blocks; inside a group the
     // token block varies fastest, then the vocabulary tile.  CTAs running at
     // the same time share a few C tiles and a group's E rows stay in L2.
-    const int total = a.n_blocks * a.v_tiles;
     const int per_group = a.group_n * a.v_tiles;
-    for (int i = blockIdx.x; i < total; i += gridDim.x) {
-      const int g = i / per_group, j = i - g * per_group;
-      const int gn = min(a.group_n, a.n_blocks - g * a.group_n);
-      if (!f(Tile{g * a.group_n + j % gn, j / gn, 0, true, true})) return;
-    }
+    const int g = item / per_group, j = item - g * per_group;
+    const int gn = min(a.group_n, a.n_blocks - g * a.group_n);
+    return f(Tile{KIND_MAIN, g * a.group_n + j % gn, j / gn, 0, true, true});
   } else {
-    const int total = a.m_tiles * a.n_tiles;
-    for (int i = blockIdx.x; i < total; i += gridDim.x) {
-      if (!f(Tile{i / a.n_tiles, i % a.n_tiles, 0, true, true})) return;
+    const int dc_tiles = a.dc_m_tiles * a.n_tiles;
+    const int de_tiles = a.n_blocks * a.n_tiles;
+    int i = item, kind;
+    if (a.dc_first) {
+      kind = i < dc_tiles ? KIND_DC : KIND_DE;
+      if (kind == KIND_DE) i -= dc_tiles;
+    } else {
+      kind = i < de_tiles ? KIND_DE : KIND_DC;
+      if (kind == KIND_DC) i -= de_tiles;
     }
+    // the column (D) tile varies fastest: neighbouring CTAs share the A operand
+    return f(Tile{kind, i / a.n_tiles, i % a.n_tiles, 0, true, true});
   }
 }
 
-// Is K-block kb of tile t skipped by the filter?  (DC: K = tokens; DE: K =
-// chunk columns.)  FWD and BWD_G never skip.
+template <int MODE>
+__device__ __forceinline__ int kblocks_of(const GemmArgs& a, const Tile& t) {
+  if constexpr (MODE == MODE_GRAD) return t.kind == KIND_DC ? a.dc_k_blocks : a.de_k_blocks;
+  return a.k_blocks;
+}
+
+// Is K-block kb of tile t skipped by the filter?  (dC: K = tokens, read from
+// the vocabulary-major map; dE: K = chunk columns.)  FWD and BWD_G never skip.
 template <int MODE>
 __device__ __forceinline__ bool kblock_skipped(const GemmArgs& a, const Tile& t, int kb) {
-  if constexpr (MODE == MODE_DC) {  // contiguous along K: L1 hits
-    return __ldg(a.bitmapT + static_cast<size_t>((a.chunk_v0 >> 7) + t.m) * a.n_blocks + (kb >> 1)) == 0;
-  } else if constexpr (MODE == MODE_DE) {
+  if constexpr (MODE == MODE_GRAD) {
+    if (t.kind == KIND_DC)
+      return __ldg(a.bitmapT + static_cast<size_t>((a.chunk_v0 >> 7) + t.m) * a.n_blocks + (kb >> 1)) == 0;
     return __ldg(a.bitmap + static_cast<size_t>(t.m) * a.bm_ld + (a.chunk_v0 >> 7) + (kb >> 1)) == 0;
-  } else {
-    return false;
   }
+  return false;
 }
 
 // Warp-wide: does the output tile have no surviving K-block at all?
-template <int MODE>
 __device__ __forceinline__ bool tile_empty(const GemmArgs& a, const Tile& t) {
   int any = 0;
-  if constexpr (MODE == MODE_DC) {
+  if (t.kind == KIND_DC) {
     const uint8_t* row = a.bitmapT + static_cast<size_t>((a.chunk_v0 >> 7) + t.m) * a.n_blocks;
     for (int r = lane_id(); r < a.n_blocks; r += 32) any |= __ldg(row + r);
-  } else if constexpr (MODE == MODE_DE) {
+  } else {
     const int ncols = (a.chunk_w + FILTER_TILE - 1) / FILTER_TILE;
     const uint8_t* row = a.bitmap + static_cast<size_t>(t.m) * a.bm_ld + (a.chunk_v0 >> 7);
     for (int j = lane_id(); j < ncols; j += 32) any |= __ldg(row + j);
-  } else {
-    any = 1;
   }
   return __any_sync(0xffffffffu, any) == 0;
 }
@@ -116,8 +124,14 @@ __device__ __forceinline__ float ex2(float v) {
   return r;
 }
 
-// Byte offset of 16-byte chunk c of row r inside a 128-byte-swizzled box.
+// Byte offset of 16-byte chunk c of row r inside a 128-byte-swizzled box
+// (128-byte rows, box 1024-byte aligned).
 __device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
+
+// The same for a 64-byte-swizzled box (64-byte rows, box 512-byte aligned).
+__device__ __forceinline__ uint32_t swz64(uint32_t r, uint32_t c) {
+  return r * 64u + ((c ^ ((r >> 1) & 3u)) << 4);
+}
 
 struct SmemLayout {
   uint8_t* stages;
@@ -128,9 +142,12 @@ struct SmemLayout {
   uint64_t* tmem_empty;
   uint64_t* vote;
   uint64_t* drain;
+  uint64_t* ring_full;
+  uint64_t* ring_empty;
   uint32_t* tmem_base;
   int* abort_flag;
-  int* flags;  // [2 parity][2 half][4 warps]
+  int* flags;     // [2 parity][2 half][4 warps]
+  int* ring_ids;  // [RING]
 };
 
 __device__ __forceinline__ SmemLayout carve_smem(uint8_t* raw) {
@@ -138,19 +155,33 @@ __device__ __forceinline__ SmemLayout carve_smem(uint8_t* raw) {
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
   L.stages = base;
   L.epi = base + STAGES * STAGE_BYTES;
-  uint8_t* b = L.epi + NUM_EPI_WARPS * EPI_WARP_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(b);
-  L.full = bars;                  // STAGES
-  L.empty = bars + STAGES;        // STAGES
-  L.tmem_full = bars + 2 * STAGES;      // 2
-  L.tmem_empty = bars + 2 * STAGES + 2;  // 2
-  L.vote = bars + 2 * STAGES + 4;        // 2
-  L.drain = bars + 2 * STAGES + 6;       // 1
-  uint8_t* tail = reinterpret_cast<uint8_t*>(bars + 2 * STAGES + 7);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(L.epi + NUM_EPI_WARPS * EPI_WARP_BYTES);
+  L.full = bars;                          // STAGES
+  L.empty = L.full + STAGES;              // STAGES
+  L.tmem_full = L.empty + STAGES;         // 2
+  L.tmem_empty = L.tmem_full + 2;         // 2
+  L.vote = L.tmem_empty + 2;              // 2
+  L.drain = L.vote + 2;                   // 1
+  L.ring_full = L.drain + 1;              // RING
+  L.ring_empty = L.ring_full + RING;      // RING
+  uint8_t* tail = reinterpret_cast<uint8_t*>(L.ring_empty + RING);
   L.tmem_base = reinterpret_cast<uint32_t*>(tail);
   L.abort_flag = reinterpret_cast<int*>(tail + 4);
-  L.flags = reinterpret_cast<int*>(tail + 8);  // 16 ints
+  L.flags = reinterpret_cast<int*>(tail + 8);      // 16 ints
+  L.ring_ids = reinterpret_cast<int*>(tail + 72);  // RING ints
   return L;
+}
+
+// ------------------------------------------------------- work-item ring
+// Consumer side: the k-th work item, or -1 when the work has run out (or the
+// CTA aborted).  Single thread.
+__device__ __forceinline__ int ring_take(const SmemLayout& L, int k, const GemmArgs& a) {
+  const int slot = k % RING;
+  const uint32_t par = static_cast<uint32_t>((k / RING) & 1);
+  if (!wait_bounded(&L.ring_full[slot], par, L.abort_flag, a.dev_err)) return -1;
+  const int item = *reinterpret_cast<volatile int*>(&L.ring_ids[slot]);
+  mbar_arrive(&L.ring_empty[slot]);
+  return item;
 }
 
 // ---------------------------------------------------------------- producer
@@ -160,34 +191,47 @@ __device__ __forceinline__ void producer_loop(const GemmArgs& a, const SmemLayou
   int stage = 0;
   uint32_t phase = 0;
   uint32_t issued_mask = 0, issued_par = 0;  // per stage: ever issued, parity of last issue
-  for_each_tile<MODE>(a, [&](const Tile& t) -> bool {
-    for (int kb = 0; kb < a.k_blocks; ++kb) {
-      if (kblock_skipped<MODE>(a, t, kb)) continue;
-      if (!wait_bounded(&L.empty[stage], phase ^ 1u, abort_flag, a.dev_err)) return false;
-      uint8_t* sA = L.stages + stage * STAGE_BYTES;
-      uint8_t* sB = sA + A_STAGE_BYTES;
-      mbar_arrive_expect_tx(&L.full[stage], STAGE_BYTES);
-      const int k0 = kb * BK;
-      if constexpr (MODE == MODE_FWD || MODE == MODE_BWD_G) {
-        tma_load_2d(&a.tmA, &L.full[stage], sA, k0, t.m * BM);
-        tma_load_2d(&a.tmB, &L.full[stage], sB, k0, a.chunk_v0 + t.n * BN);
-      } else if constexpr (MODE == MODE_DC) {
-        for (int j = 0; j < BM / 64; ++j) tma_load_2d(&a.tmA, &L.full[stage], sA + j * 8192, t.m * BM + j * 64, k0);
-        for (int j = 0; j < BN / 64; ++j) tma_load_2d(&a.tmB, &L.full[stage], sB + j * 8192, t.n * BN + j * 64, k0);
-      } else {  // MODE_DE
-        tma_load_2d(&a.tmA, &L.full[stage], sA, k0, t.m * BM);
-        for (int j = 0; j < BN / 64; ++j)
-          tma_load_2d(&a.tmB, &L.full[stage], sB + j * 8192, t.n * BN + j * 64, a.chunk_v0 + k0);
+  for (int k = 0;; ++k) {
+    const int slot = k % RING;
+    if (!wait_bounded(&L.ring_empty[slot], static_cast<uint32_t>(((k / RING) & 1) ^ 1), abort_flag, a.dev_err))
+      break;
+    int item = atomicAdd(a.counter, 1);
+    if (item >= a.items) item = -1;
+    L.ring_ids[slot] = item;
+    mbar_arrive(&L.ring_full[slot]);  // release: the id is visible to the waiting consumers
+    if (item < 0) break;
+    const bool ok = for_each_tile_of_item<MODE>(a, item, [&](const Tile& t) -> bool {
+      const int nk = kblocks_of<MODE>(a, t);
+      for (int kb = 0; kb < nk; ++kb) {
+        if (kblock_skipped<MODE>(a, t, kb)) continue;
+        if (!wait_bounded(&L.empty[stage], phase ^ 1u, abort_flag, a.dev_err)) return false;
+        uint8_t* sA = L.stages + stage * STAGE_BYTES;
+        uint8_t* sB = sA + A_STAGE_BYTES;
+        uint64_t* fb = &L.full[stage];
+        mbar_arrive_expect_tx(fb, STAGE_BYTES);
+        const int k0 = kb * BK;
+        if (MODE != MODE_GRAD) {
+          tma_load_2d(&a.tmA, fb, sA, k0, t.m * BM);
+          tma_load_2d(&a.tmB, fb, sB, k0, a.chunk_v0 + t.n * BN);
+        } else if (t.kind == KIND_DC) {
+          for (int j = 0; j < BM / 64; ++j) tma_load_2d(&a.tmA, fb, sA + j * 8192, t.m * BM + j * 64, k0);
+          for (int j = 0; j < BN / 64; ++j) tma_load_2d(&a.tmB, fb, sB + j * 8192, t.n * a.bn + j * 64, k0);
+        } else {
+          tma_load_2d(&a.tmA2, fb, sA, k0, t.m * BM);
+          for (int j = 0; j < BN / 64; ++j)
+            tma_load_2d(&a.tmB2, fb, sB + j * 8192, t.n * a.bn + j * 64, a.chunk_v0 + k0);
+        }
+        issued_mask |= 1u << stage;
+        issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
-      issued_mask |= 1u << stage;
-      issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-      if (++stage == STAGES) {
-        stage = 0;
-        phase ^= 1u;
-      }
-    }
-    return true;
-  });
+      return true;
+    });
+    if (!ok) break;
+  }
   if (*abort_flag) {
     // Let every copy this thread issued land before the CTA exits.
     for (int s = 0; s < STAGES; ++s) {
@@ -202,53 +246,60 @@ __device__ __forceinline__ void producer_loop(const GemmArgs& a, const SmemLayou
 // --------------------------------------------------------------------- MMA
 template <int MODE>
 __device__ __forceinline__ void mma_loop(const GemmArgs& a, const SmemLayout& L, uint32_t tmem_base) {
-  constexpr bool A_MN = (MODE == MODE_DC);
-  constexpr bool B_MN = (MODE == MODE_DC || MODE == MODE_DE);
-  constexpr uint32_t IDESC = idesc_bf16(BM, BN, A_MN, B_MN);
-  constexpr uint32_t A_LBO = A_MN ? 8192u : 16u;
-  constexpr uint32_t B_LBO = B_MN ? 8192u : 16u;
-  constexpr uint64_t A_KSTEP = A_MN ? (2048u >> 4) : (32u >> 4);  // one K=16 step, encoded
-  constexpr uint64_t B_KSTEP = B_MN ? (2048u >> 4) : (32u >> 4);
   volatile int* abort_flag = L.abort_flag;
   int stage = 0;
   uint32_t phase = 0;
   int acc = 0;
   uint32_t acc_phase = 0;
   bool issued_any = false;
-  for_each_tile<MODE>(a, [&](const Tile& t) -> bool {
-    if (!wait_bounded(&L.tmem_empty[acc], acc_phase ^ 1u, abort_flag, a.dev_err)) return false;
-    tc_fence_after();
-    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-    bool any = false;
-    for (int kb = 0; kb < a.k_blocks; ++kb) {
-      if (kblock_skipped<MODE>(a, t, kb)) continue;
-      if (!wait_bounded(&L.full[stage], phase, abort_flag, a.dev_err)) return false;
+  for (int k = 0;; ++k) {
+    const int item = ring_take(L, k, a);
+    if (item < 0) break;
+    const bool ok = for_each_tile_of_item<MODE>(a, item, [&](const Tile& t) -> bool {
+      // Operand majorness and tile width of this tile.
+      const bool a_mn = (MODE == MODE_GRAD) && t.kind == KIND_DC;
+      const bool b_mn = (MODE == MODE_GRAD);
+      const int n = (MODE == MODE_GRAD) ? a.bn : BN;
+      const uint32_t idesc = idesc_bf16(BM, n, a_mn, b_mn);
+      const uint32_t a_lbo = a_mn ? 8192u : 16u, b_lbo = b_mn ? 8192u : 16u;
+      const uint64_t a_step = a_mn ? (2048u >> 4) : (32u >> 4);  // one K=16 step, encoded
+      const uint64_t b_step = b_mn ? (2048u >> 4) : (32u >> 4);
+      if (!wait_bounded(&L.tmem_empty[acc], acc_phase ^ 1u, abort_flag, a.dev_err)) return false;
       tc_fence_after();
-      const uint32_t sA = smem_u32(L.stages + stage * STAGE_BYTES);
-      const uint32_t sB = sA + A_STAGE_BYTES;
-      const uint64_t adesc = smem_desc_sw128(sA, A_LBO, 1024u);
-      const uint64_t bdesc = smem_desc_sw128(sB, B_LBO, 1024u);
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+      const int nk = kblocks_of<MODE>(a, t);
+      bool any = false;
+      for (int kb = 0; kb < nk; ++kb) {
+        if (kblock_skipped<MODE>(a, t, kb)) continue;
+        if (!wait_bounded(&L.full[stage], phase, abort_flag, a.dev_err)) return false;
+        tc_fence_after();
+        const uint32_t sA = smem_u32(L.stages + stage * STAGE_BYTES);
+        const uint32_t sB = sA + A_STAGE_BYTES;
+        const uint64_t adesc = smem_desc_sw128(sA, a_lbo, 1024u);
+        const uint64_t bdesc = smem_desc_sw128(sB, b_lbo, 1024u);
 #pragma unroll
-      for (int k = 0; k < BK / 16; ++k) {
-        mma_bf16(d_tmem, adesc + A_KSTEP * k, bdesc + B_KSTEP * k, IDESC, (any || k > 0) ? 1u : 0u);
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          mma_bf16(d_tmem, adesc + a_step * kk, bdesc + b_step * kk, idesc, (any || kk > 0) ? 1u : 0u);
+        }
+        any = true;
+        issued_any = true;
+        mma_commit(&L.empty[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
-      any = true;
-      issued_any = true;
-      mma_commit(&L.empty[stage]);
-      if (++stage == STAGES) {
-        stage = 0;
-        phase ^= 1u;
+      if (any) {
+        mma_commit(&L.tmem_full[acc]);
+      } else {
+        mbar_arrive(&L.tmem_full[acc]);  // nothing to wait for: the epilogue writes zeros
       }
-    }
-    if (any) {
-      mma_commit(&L.tmem_full[acc]);
-    } else {
-      mbar_arrive(&L.tmem_full[acc]);  // nothing to wait for: the epilogue writes zeros
-    }
-    acc ^= 1;
-    if (acc == 0) acc_phase ^= 1u;
-    return true;
-  });
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+      return true;
+    });
+    if (!ok) break;
+  }
   if (*abort_flag && issued_any) {
     mma_commit(L.drain);  // fires once every MMA issued so far has finished
     volatile int dummy = 0;
@@ -260,7 +311,7 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& a, const SmemLayout& L,
 struct EpiCtx {
   uint32_t taddr;  // TMEM address of this warp's lane quadrant, accumulator column 0
   int q;           // lane quadrant = tile rows 32q .. 32q + 31
-  uint8_t* buf;    // this warp's 8 KiB staging area
+  uint8_t* buf;    // this warp's 8 KiB staging area (two 4 KiB halves)
   int iter;        // tiles processed so far by this warp
   int last_buf;    // staging half read by the most recent bulk group (-1: none)
 };
@@ -447,14 +498,16 @@ __device__ __forceinline__ bool epi_bwd_g(const GemmArgs& a, const SmemLayout& L
   return ok;
 }
 
-// DC: bf16 output tile, rows = vocabulary (chunk_v0 + 128m ...), cols = D.
+// GRAD, KIND_DC: bf16 output tile, rows = vocabulary (chunk_v0 + 128m ...),
+// cols = D tile of width bn, stored in 32-column boxes (64-byte swizzle).
 __device__ __forceinline__ void epi_dc(const GemmArgs& a, const SmemLayout& L, const Tile& t, int acc, EpiCtx& e) {
   const uint32_t lane = lane_id();
-  const bool empty = tile_empty<MODE_DC>(a, t);
+  const bool empty = tile_empty(a, t);
   const uint32_t tbase = e.taddr + static_cast<uint32_t>(acc * BN);
   const int gy = a.chunk_v0 + t.m * BM + e.q * 32;
+  const int x0 = t.n * a.bn;
   // boxes that start inside dC (no store may start outside the tensor)
-  const int nbox = (gy < a.V) ? min(BN / 64, (a.D - t.n * BN + 63) / 64) : 0;
+  const int nbox = (gy < a.V) ? min(a.bn / 32, (a.D - x0 + 31) / 32) : 0;
 #pragma unroll 1
   for (int j = 0; j < nbox; ++j) {
     const int b = j & 1;
@@ -462,30 +515,24 @@ __device__ __forceinline__ void epi_dc(const GemmArgs& a, const SmemLayout& L, c
     staging_acquire(e, b);
     const uint32_t sb = smem_u32(buf);
     if (!empty) {
-      uint32_t r0[32], r1[32];
-      tmem_ld32(tbase + 64 * j, r0);
-      tmem_ld32(tbase + 64 * j + 32, r1);
+      uint32_t r[32];
+      tmem_ld32(tbase + 32 * j, r);
       tmem_ld_wait();
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        st_shared_v4(sb + swz(lane, u), pack_bf16x2(__uint_as_float(r0[8 * u + 0]), __uint_as_float(r0[8 * u + 1])),
-                     pack_bf16x2(__uint_as_float(r0[8 * u + 2]), __uint_as_float(r0[8 * u + 3])),
-                     pack_bf16x2(__uint_as_float(r0[8 * u + 4]), __uint_as_float(r0[8 * u + 5])),
-                     pack_bf16x2(__uint_as_float(r0[8 * u + 6]), __uint_as_float(r0[8 * u + 7])));
-        st_shared_v4(sb + swz(lane, 4 + u),
-                     pack_bf16x2(__uint_as_float(r1[8 * u + 0]), __uint_as_float(r1[8 * u + 1])),
-                     pack_bf16x2(__uint_as_float(r1[8 * u + 2]), __uint_as_float(r1[8 * u + 3])),
-                     pack_bf16x2(__uint_as_float(r1[8 * u + 4]), __uint_as_float(r1[8 * u + 5])),
-                     pack_bf16x2(__uint_as_float(r1[8 * u + 6]), __uint_as_float(r1[8 * u + 7])));
+        st_shared_v4(sb + swz64(lane, u), pack_bf16x2(__uint_as_float(r[8 * u + 0]), __uint_as_float(r[8 * u + 1])),
+                     pack_bf16x2(__uint_as_float(r[8 * u + 2]), __uint_as_float(r[8 * u + 3])),
+                     pack_bf16x2(__uint_as_float(r[8 * u + 4]), __uint_as_float(r[8 * u + 5])),
+                     pack_bf16x2(__uint_as_float(r[8 * u + 6]), __uint_as_float(r[8 * u + 7])));
       }
     } else {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) st_shared_v4(sb + swz(lane, u), 0u, 0u, 0u, 0u);
+      for (int u = 0; u < 4; ++u) st_shared_v4(sb + swz64(lane, u), 0u, 0u, 0u, 0u);
     }
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      tma_store_2d(&a.tmOut, buf, t.n * BN + 64 * j, gy);
+      tma_store_2d(&a.tmOut, buf, x0 + 32 * j, gy);
       bulk_commit();
     }
     e.last_buf = b;
@@ -493,18 +540,20 @@ __device__ __forceinline__ void epi_dc(const GemmArgs& a, const SmemLayout& L, c
   release_tmem(L, acc);
 }
 
-// DE: fp32 output tile, rows = tokens, cols = D; store (first chunk) or reduce-add.
+// GRAD, KIND_DE: fp32 output tile, rows = tokens, cols = D tile; store (first
+// chunk) or reduce-add, in 32-column boxes (128-byte swizzle).
 __device__ __forceinline__ void epi_de(const GemmArgs& a, const SmemLayout& L, const Tile& t, int acc, EpiCtx& e) {
   const uint32_t lane = lane_id();
-  const bool empty = tile_empty<MODE_DE>(a, t);
+  const bool empty = tile_empty(a, t);
   if (empty && !a.first_chunk) {  // adding zero: nothing to do
     release_tmem(L, acc);
     return;
   }
   const uint32_t tbase = e.taddr + static_cast<uint32_t>(acc * BN);
   const int gy = t.m * BM + e.q * 32;
+  const int x0 = t.n * a.bn;
   // boxes that start inside dE (no store or reduce may start outside the tensor)
-  const int nbox = (gy < a.N) ? min(BN / 32, (a.D - t.n * BN + 31) / 32) : 0;
+  const int nbox = (gy < a.N) ? min(a.bn / 32, (a.D - x0 + 31) / 32) : 0;
 #pragma unroll 1
   for (int j = 0; j < nbox; ++j) {
     const int b = j & 1;
@@ -525,9 +574,9 @@ __device__ __forceinline__ void epi_de(const GemmArgs& a, const SmemLayout& L, c
     __syncwarp();
     if (lane == 0) {
       if (a.first_chunk) {
-        tma_store_2d(&a.tmOut, buf, t.n * BN + 32 * j, gy);
+        tma_store_2d(&a.tmOut2, buf, x0 + 32 * j, gy);
       } else {
-        tma_reduce_add_2d(&a.tmOut, buf, t.n * BN + 32 * j, gy);
+        tma_reduce_add_2d(&a.tmOut2, buf, x0 + 32 * j, gy);
       }
       bulk_commit();
     }
@@ -548,24 +597,33 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& a, const SmemLayou
   FwdState st{NEG_BIG, 0.0f};
   int acc = 0;
   uint32_t acc_phase = 0;
-  for_each_tile<MODE>(a, [&](const Tile& t) -> bool {
-    if (!warp_wait_bounded(&L.tmem_full[acc], acc_phase, L.abort_flag, a.dev_err)) return false;
-    tc_fence_after();
-    bool ok = true;
-    if constexpr (MODE == MODE_FWD) {
-      epi_fwd(a, L, t, acc, e, st);
-    } else if constexpr (MODE == MODE_BWD_G) {
-      ok = epi_bwd_g(a, L, t, acc, e);
-    } else if constexpr (MODE == MODE_DC) {
-      epi_dc(a, L, t, acc, e);
-    } else {
-      epi_de(a, L, t, acc, e);
-    }
-    ++e.iter;
-    acc ^= 1;
-    if (acc == 0) acc_phase ^= 1u;
-    return ok;
-  });
+  for (int k = 0;; ++k) {
+    int item = 0;
+    if (lane_id() == 0) item = ring_take(L, k, a);
+    item = __shfl_sync(0xffffffffu, item, 0);
+    if (item < 0) break;
+    const bool ok = for_each_tile_of_item<MODE>(a, item, [&](const Tile& t) -> bool {
+      if (!warp_wait_bounded(&L.tmem_full[acc], acc_phase, L.abort_flag, a.dev_err)) return false;
+      tc_fence_after();
+      bool r = true;
+      if constexpr (MODE == MODE_FWD) {
+        epi_fwd(a, L, t, acc, e, st);
+      } else if constexpr (MODE == MODE_BWD_G) {
+        r = epi_bwd_g(a, L, t, acc, e);
+      } else {
+        if (t.kind == KIND_DC) {
+          epi_dc(a, L, t, acc, e);
+        } else {
+          epi_de(a, L, t, acc, e);
+        }
+      }
+      ++e.iter;
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+      return r;
+    });
+    if (!ok) break;
+  }
   if (lane_id() == 0) bulk_wait_all();
   __syncwarp();
 }
@@ -585,6 +643,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cce_gemm_kernel(const __grid_c
       mbar_init(&L.tmem_empty[i], NUM_EPI_WARPS);
       mbar_init(&L.vote[i], NUM_EPI_WARPS);
     }
+    for (int i = 0; i < RING; ++i) {
+      mbar_init(&L.ring_full[i], 1);
+      mbar_init(&L.ring_empty[i], 1 + NUM_EPI_WARPS);  // the MMA thread and every epilogue warp
+    }
     mbar_init(L.drain, 1);
     *L.abort_flag = 0;
     fence_mbar_init();
@@ -593,6 +655,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cce_gemm_kernel(const __grid_c
     tma_prefetch_desc(&a.tmA);
     tma_prefetch_desc(&a.tmB);
     if (MODE != MODE_FWD) tma_prefetch_desc(&a.tmOut);
+    if (MODE == MODE_GRAD) {
+      tma_prefetch_desc(&a.tmA2);
+      tma_prefetch_desc(&a.tmB2);
+      tma_prefetch_desc(&a.tmOut2);
+    }
   }
   if (warp == 1) {
     tmem_alloc(L.tmem_base, TMEM_COLS);

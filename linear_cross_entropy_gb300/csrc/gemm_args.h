@@ -17,28 +17,49 @@ constexpr int NUM_EPI_WARPS = 4;
 constexpr int EPI_WARP_BYTES = 8192;
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int BAR_BYTES = 256;
+constexpr int RING = 4;  // depth of the work-item ring between the scheduler and the consumers
+constexpr int BAR_BYTES = 512;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_EPI_WARPS * EPI_WARP_BYTES + BAR_BYTES;
 constexpr int FILTER_TILE = 128;  // filter decisions are per 128 tokens x 128 vocab
 
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float NEG_BIG = -3.0e38f;  // finite "minus infinity" for the running max
 
-enum Mode { MODE_FWD = 0, MODE_BWD_G = 1, MODE_DC = 2, MODE_DE = 3 };
+// MODE_GRAD runs the two gradient contractions of one vocabulary chunk in
+// one launch; each of its tiles is of kind KIND_DC or KIND_DE.
+enum Mode { MODE_FWD = 0, MODE_BWD_G = 1, MODE_GRAD = 2 };
+enum Kind { KIND_MAIN = 0, KIND_DC = 1, KIND_DE = 2 };
 
 struct GemmArgs {
-  CUtensorMap tmA;    // loads of operand A
-  CUtensorMap tmB;    // loads of operand B
-  CUtensorMap tmOut;  // BWD_G: G chunk; DC: dC; DE: dE accumulator
+  // FWD / BWD_G: A = E, B = C, Out = G chunk (BWD_G).  GRAD: the dC kind's
+  // A = G chunk (MN-major boxes), B = E (MN-major boxes), Out = dC.
+  CUtensorMap tmA;
+  CUtensorMap tmB;
+  CUtensorMap tmOut;
+  // GRAD: the dE kind's A = G chunk (K-major boxes), B = C (MN-major boxes),
+  // Out = dE accumulator (fp32).
+  CUtensorMap tmA2;
+  CUtensorMap tmB2;
+  CUtensorMap tmOut2;
   int N, D, V;
   int n_blocks;  // ceil(N / 128)
-  int k_blocks;  // BK steps along the contraction
+  int k_blocks;  // FWD / BWD_G: ceil(D / 64)
   int splits;    // FWD: vocabulary splits
   int v_tiles;   // FWD: ceil(V / 256); BWD_G: 256-wide tiles in the chunk
   int chunk_v0;  // BWD: first vocabulary row of the chunk (multiple of 256)
   int chunk_w;   // BWD: vocabulary rows in the chunk
-  int m_tiles, n_tiles;  // DC / DE output tile grid
-  int first_chunk;       // DE: store (1) or reduce-add (0)
+  int group_n;   // BWD_G: token blocks per raster group
+  // GRAD
+  int bn;           // width of a D tile (multiple of 32, <= 256)
+  int n_tiles;      // ceil(D / bn)
+  int dc_m_tiles;   // ceil(chunk_w / 128)
+  int dc_k_blocks;  // ceil(N / 64)
+  int de_k_blocks;  // ceil(chunk_w / 64)
+  int dc_first;     // 1: dC tiles are handed out first (they have the longer K)
+  int first_chunk;  // dE: store (1) or reduce-add (0)
+  // dynamic scheduling: work items are handed out by atomicAdd on *counter
+  int* counter;     // zeroed before the launch
+  int items;
   const int64_t* x;
   long long ignore_index;
   float* part_m;  // FWD: [splits][N] running max (log2 units)
@@ -52,7 +73,6 @@ struct GemmArgs {
   uint8_t* bitmap;   // [ceil(N/128)][bm_ld] tile survival, token-block major
   uint8_t* bitmapT;  // [bm_ld][ceil(N/128)] the same, vocabulary-block major (read along K by dC)
   int bm_ld;         // ceil(V / 128)
-  int group_n;       // BWD_G: token blocks per raster group
   int32_t* dev_err;
 };
 

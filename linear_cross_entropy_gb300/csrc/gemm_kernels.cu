@@ -1,4 +1,4 @@
-// Instantiations and launcher of the four tcgen05 GEMM kernels.
+// Instantiations and launcher of the three tcgen05 GEMM kernels.
 #include "gemm.cuh"
 #include "internal.h"
 
@@ -13,8 +13,7 @@ cudaError_t prepare_gemm_kernels() {
   cudaError_t e;
   if ((e = set_smem<MODE_FWD>()) != cudaSuccess) return e;
   if ((e = set_smem<MODE_BWD_G>()) != cudaSuccess) return e;
-  if ((e = set_smem<MODE_DC>()) != cudaSuccess) return e;
-  return set_smem<MODE_DE>();
+  return set_smem<MODE_GRAD>();
 }
 
 cudaError_t launch_gemm(int mode, const GemmArgs& args, int grid, cudaStream_t stream) {
@@ -22,8 +21,7 @@ cudaError_t launch_gemm(int mode, const GemmArgs& args, int grid, cudaStream_t s
   switch (mode) {
     case MODE_FWD: cce_gemm_kernel<MODE_FWD><<<g, b, SMEM_BYTES, stream>>>(args); break;
     case MODE_BWD_G: cce_gemm_kernel<MODE_BWD_G><<<g, b, SMEM_BYTES, stream>>>(args); break;
-    case MODE_DC: cce_gemm_kernel<MODE_DC><<<g, b, SMEM_BYTES, stream>>>(args); break;
-    case MODE_DE: cce_gemm_kernel<MODE_DE><<<g, b, SMEM_BYTES, stream>>>(args); break;
+    case MODE_GRAD: cce_gemm_kernel<MODE_GRAD><<<g, b, SMEM_BYTES, stream>>>(args); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
