@@ -22,7 +22,7 @@ exactly.  numpy's transcendental functions (whose last bit may differ between
 x86 and Arm builds) are never used; ``_log`` and ``_exp`` below are written
 out from their series.  Large tensors are drawn in independent blocks of
 2**22 elements, each seeded by (seed, stream, block), so the result does not
-depend on how many worker processes draw them.
+depend on how many worker threads draw them.
 """
 from __future__ import annotations
 
@@ -30,8 +30,7 @@ import dataclasses
 import hashlib
 import math
 import os
-from concurrent.futures import ProcessPoolExecutor
-import multiprocessing as mp
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -159,8 +158,9 @@ def normal_bf16(seed: int, stream: int, n: int, sigma: float) -> np.ndarray:
     if workers <= 1 or nblocks <= 2:
         parts = [_normal_block(j) for j in jobs]
     else:
-        # spawn: never fork a process that may already hold a CUDA context.
-        with ProcessPoolExecutor(max_workers=workers, mp_context=mp.get_context("spawn")) as ex:
+        # Threads, not processes: numpy releases the GIL in its array loops,
+        # and no process is forked from one that may hold a CUDA context.
+        with ThreadPoolExecutor(max_workers=workers) as ex:
             parts = list(ex.map(_normal_block, jobs))
     return np.concatenate(parts) if parts else np.zeros(0, np.uint16)
 

@@ -24,7 +24,10 @@ namespace {
 
 constexpr int REF_SMS = 152;          // split count heuristic assumes this many SMs
 constexpr size_t ALIGN = 256;         // sub-buffer alignment inside a workspace
-constexpr size_t G_CHUNK_BUDGET = size_t(512) << 20;  // bytes of the backward G chunk buffer
+#ifndef CCE_G_CHUNK_BUDGET_MIB
+#define CCE_G_CHUNK_BUDGET_MIB 512
+#endif
+constexpr size_t G_CHUNK_BUDGET = size_t(CCE_G_CHUNK_BUDGET_MIB) << 20;  // bytes of the backward G chunk buffer
 constexpr int64_t MIN_CHUNK = 2048, MAX_CHUNK = 32768;
 constexpr int COMBINE_THREADS = 256;
 
@@ -199,21 +202,13 @@ int64_t bwd_chunk_cols(int64_t N, int64_t V) {
   return std::min(vc, vpad);
 }
 
-// Width of the D tiles of the gradient GEMMs: the multiple of 32 (128..256, or
-// D rounded up to 32 when D < 128) that wastes the fewest MMA columns,
-// preferring wider tiles.
-int grad_tile_width(int64_t D) {
-  if (D < 128) return static_cast<int>(cdiv(D, 32) * 32);
-  int best = BN;
-  int64_t best_pad = cdiv(D, BN) * BN;
-  for (int bn = BN - 32; bn >= 128; bn -= 32) {
-    const int64_t pad = cdiv(D, bn) * bn;
-    if (pad < best_pad) {
-      best = bn;
-      best_pad = pad;
-    }
-  }
-  return best;
+// Width of the D tiles of the gradient GEMMs.  Measured on GB300: MMAs with
+// N = 256 run fastest (N = 224 about 10% slower per column, N = 192 and 128
+// far slower), so tiles are 256 wide even when that pads D (D = 896: 1024),
+// and only narrower when D itself is smaller (rounded up to `step`).
+int grad_tile_width(int64_t D, int step) {
+  if (D >= BN) return BN;
+  return static_cast<int>(cdiv(D, step) * step);
 }
 
 struct FwdLayout {
@@ -340,6 +335,20 @@ bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void*
   cuuint32_t es[2] = {1, 1};
   CUresult r = g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// bf16 [rows][D] viewed as {64 d, rows, D / 64 groups} with box {64, 64,
+// groups}: one TMA instruction brings all 64-column groups of an MN-major
+// operand stage (D % 64 == 0, so the view never reaches past a row).
+bool make_tmap_mn3(CUtensorMap* m, const void* ptr, uint64_t D, uint64_t rows, uint32_t groups = 4) {
+  cuuint64_t dims[3] = {64, rows, D / 64};
+  cuuint64_t strides[2] = {D * 2, 128};
+  cuuint32_t box[3] = {64, 64, groups};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -553,11 +562,17 @@ cce_status cce_backward(const void* E, const void* C, const int64_t* x, const fl
   ok &= make_tmap(&g.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, E, D, N, D, BK, BM);
   ok &= make_tmap(&g.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, D, V, D, BK, BN);
   ok &= make_tmap(&g.tmOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, gbuf, vc, N, vc, 64, 32);
-  ok &= make_tmap(&r.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, gbuf, vc, N, vc, 64, 64);
-  ok &= make_tmap(&r.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, E, D, N, D, 64, 64);
+  r.b3d = (D % 64 == 0) ? 1 : 0;
+  ok &= make_tmap_mn3(&r.tmA, gbuf, vc, N, BM / 64);  // G chunk, MN-major A of dC (vc % 256 == 0)
+  if (r.b3d) {
+    ok &= make_tmap_mn3(&r.tmB, E, D, N);
+    ok &= make_tmap_mn3(&r.tmB2, C, D, V);
+  } else {
+    ok &= make_tmap(&r.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, E, D, N, D, 64, 64);
+    ok &= make_tmap(&r.tmB2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, D, V, D, 64, 64);
+  }
   ok &= make_tmap(&r.tmOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dC, D, V, D, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
   ok &= make_tmap(&r.tmA2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, gbuf, vc, N, vc, 64, BM);
-  ok &= make_tmap(&r.tmB2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, D, V, D, 64, 64);
   ok &= make_tmap(&r.tmOut2, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, deacc, D, N, D, 32, 32);
   if (!ok) return CCE_ERR_CUDA;
 
@@ -582,7 +597,7 @@ cce_status cce_backward(const void* E, const void* C, const int64_t* x, const fl
   // Raster groups whose E rows (group_n * 128 * D * 2 bytes) stay around 32 MiB.
   g.group_n = static_cast<int>(std::max<int64_t>(
       1, std::min<int64_t>(cdiv(N, BM), std::max<int64_t>(8, (int64_t(32) << 20) / (BM * 2 * D)))));
-  r.bn = grad_tile_width(D);
+  r.bn = grad_tile_width(D, r.b3d ? 64 : 32);
   r.n_tiles = static_cast<int>(cdiv(D, r.bn));
   r.dc_k_blocks = static_cast<int>(cdiv(N, BK));
 

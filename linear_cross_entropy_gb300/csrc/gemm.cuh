@@ -18,7 +18,9 @@
 //              Pass (Algorithm 4)", "Gradient Filtering").
 //   MODE_GRAD  Both gradient contractions of the chunk in one launch:
 //              KIND_DC tiles: dC[chunk rows] = G_chunk^T E (A = G MN-major,
-//              B = E MN-major, K = tokens), each tile owns its dC rows and
+//              B = E MN-major, K = tokens; each MN-major operand arrives in one
+//              3-D TMA box per stage -- B when D % 64 == 0, else in four 2-D
+//              boxes, which cost about 15% of the MMA rate), each tile owns its dC rows and
 //              writes them once in bf16, no atomics.  KIND_DE tiles: dE_acc
 //              (+)= G_chunk C_chunk (A = G K-major, B = C MN-major, K = chunk
 //              columns), fp32 tiles stored (first chunk) or reduce-added by
@@ -214,12 +216,20 @@ __device__ __forceinline__ void producer_loop(const GemmArgs& a, const SmemLayou
           tma_load_2d(&a.tmA, fb, sA, k0, t.m * BM);
           tma_load_2d(&a.tmB, fb, sB, k0, a.chunk_v0 + t.n * BN);
         } else if (t.kind == KIND_DC) {
-          for (int j = 0; j < BM / 64; ++j) tma_load_2d(&a.tmA, fb, sA + j * 8192, t.m * BM + j * 64, k0);
-          for (int j = 0; j < BN / 64; ++j) tma_load_2d(&a.tmB, fb, sB + j * 8192, t.n * a.bn + j * 64, k0);
+          tma_load_3d(&a.tmA, fb, sA, 0, k0, (t.m * BM) >> 6);  // both 64-column groups of A
+          if (a.b3d) {  // the four 64-column groups of B in one instruction
+            tma_load_3d(&a.tmB, fb, sB, 0, k0, (t.n * a.bn) >> 6);
+          } else {
+            for (int j = 0; j < BN / 64; ++j) tma_load_2d(&a.tmB, fb, sB + j * 8192, t.n * a.bn + j * 64, k0);
+          }
         } else {
           tma_load_2d(&a.tmA2, fb, sA, k0, t.m * BM);
-          for (int j = 0; j < BN / 64; ++j)
-            tma_load_2d(&a.tmB2, fb, sB + j * 8192, t.n * a.bn + j * 64, a.chunk_v0 + k0);
+          if (a.b3d) {
+            tma_load_3d(&a.tmB2, fb, sB, 0, a.chunk_v0 + k0, (t.n * a.bn) >> 6);
+          } else {
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(&a.tmB2, fb, sB + j * 8192, t.n * a.bn + j * 64, a.chunk_v0 + k0);
+          }
         }
         issued_mask |= 1u << stage;
         issued_par = (issued_par & ~(1u << stage)) | (phase << stage);

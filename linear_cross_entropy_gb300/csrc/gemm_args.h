@@ -36,8 +36,8 @@ struct GemmArgs {
   CUtensorMap tmA;
   CUtensorMap tmB;
   CUtensorMap tmOut;
-  // GRAD: the dE kind's A = G chunk (K-major boxes), B = C (MN-major boxes),
-  // Out = dE accumulator (fp32).
+  // GRAD: the dE kind's A = G chunk (K-major boxes), B = C (MN-major: 3-D view
+  // {64 d, V, D/64} or 64x64 boxes), Out = dE accumulator (fp32).
   CUtensorMap tmA2;
   CUtensorMap tmB2;
   CUtensorMap tmOut2;
@@ -50,7 +50,8 @@ struct GemmArgs {
   int chunk_w;   // BWD: vocabulary rows in the chunk
   int group_n;   // BWD_G: token blocks per raster group
   // GRAD
-  int bn;           // width of a D tile (multiple of 32, <= 256)
+  int bn;           // width of a D tile (multiple of 32, <= 256; of 64 when b3d)
+  int b3d;          // 1: the MN-major B operands come in one 3-D box per stage (D % 64 == 0)
   int n_tiles;      // ceil(D / bn)
   int dc_m_tiles;   // ceil(chunk_w / 128)
   int dc_k_blocks;  // ceil(N / 64)
