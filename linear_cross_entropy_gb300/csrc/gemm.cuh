@@ -353,9 +353,9 @@ struct FwdState {
 
 __device__ __forceinline__ void fold_chunk(const uint32_t (&r)[32], int col0, int V, long long xr, float& run_m,
                                            float& run_s, float& tval, bool& tfound) {
-  const int nvalid = min(32, V - col0);
+  const int nvalid = min(32, V - col0);  // < 32 only in the last tile of a ragged vocabulary
   const long long rel = xr - col0;
-  if (rel >= 0 && rel < nvalid) {  // the target column passes: capture its logit
+  if (rel >= 0 && rel < nvalid) {  // the target column passes: capture its logit (rare)
     const int ri = static_cast<int>(rel);
     float tv = 0.0f;
 #pragma unroll
@@ -363,17 +363,28 @@ __device__ __forceinline__ void fold_chunk(const uint32_t (&r)[32], int col0, in
     tval = tv;
     tfound = true;
   }
-  float y[32];
+  // max of the raw logits; scaling by log2(e) afterwards gives the same value
+  // (rounding is monotonic), so each element costs one max, one FMA, one exp2
+  // and one add.
   float cmax = NEG_BIG;
+  if (nvalid == 32) {
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    y[j] = (j < nvalid) ? __uint_as_float(r[j]) * LOG2E : -INFINITY;
-    cmax = fmaxf(cmax, y[j]);
+    for (int j = 0; j < 32; ++j) cmax = fmaxf(cmax, __uint_as_float(r[j]));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < nvalid) cmax = fmaxf(cmax, __uint_as_float(r[j]));
   }
-  const float nm = fmaxf(run_m, cmax);
+  const float nm = fmaxf(run_m, cmax * LOG2E);
   float s = run_s * ex2(run_m - nm);
+  if (nvalid == 32) {
 #pragma unroll
-  for (int j = 0; j < 32; ++j) s += ex2(y[j] - nm);
+    for (int j = 0; j < 32; ++j) s += ex2(fmaf(__uint_as_float(r[j]), LOG2E, -nm));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < nvalid) s += ex2(fmaf(__uint_as_float(r[j]), LOG2E, -nm));
+  }
   run_s = s;
   run_m = nm;
 }
@@ -415,13 +426,15 @@ __device__ __forceinline__ bool epi_bwd_g(const GemmArgs& a, const SmemLayout& L
                                           EpiCtx& e) {
   const uint32_t lane = lane_id();
   const int row = t.m * BM + e.q * 32 + static_cast<int>(lane);
+  // Rows that take no part (ignored, out-of-range target, beyond N) get
+  // LSE = +inf: every exp2 is then exactly 0 and no one-hot is subtracted, so
+  // their G is 0 without a per-element test.
   long long xr = -1;
-  bool valid = false;
-  float lse2 = 0.0f, w = 0.0f;
+  float lse2 = INFINITY, w = 0.0f;
   if (row < a.N) {
-    xr = static_cast<long long>(__ldg(a.x + row));
-    valid = (xr != a.ignore_index) && xr >= 0 && xr < a.V;
-    if (valid) {
+    const long long xi = static_cast<long long>(__ldg(a.x + row));
+    if ((xi != a.ignore_index) && xi >= 0 && xi < a.V) {
+      xr = xi;
       lse2 = __ldg(a.lse + row) * LOG2E;
       if (a.reduction == CCE_RED_NONE) {
         w = __ldg(a.grad_out + row);
@@ -442,7 +455,7 @@ __device__ __forceinline__ bool epi_bwd_g(const GemmArgs& a, const SmemLayout& L
     if (lane == 0) bulk_wait_read<0>();  // staging buffer free again
     __syncwarp();
     e.last_buf = -1;
-    bool surv = false;
+    float amax = 0.0f;  // largest unscaled |G| this thread saw in the half
 #pragma unroll 1
     for (int cc = 0; cc < 4; ++cc) {
       const int c = 4 * h + cc;
@@ -450,20 +463,25 @@ __device__ __forceinline__ bool epi_bwd_g(const GemmArgs& a, const SmemLayout& L
       uint32_t r[32];
       tmem_ld32(tbase + 32 * c, r);
       tmem_ld_wait();
+      float g[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) g[j] = ex2(fmaf(__uint_as_float(r[j]), LOG2E, -lse2));
+      if (col0 + 32 > a.V) {  // ragged last tile: columns past V are zero (uniform branch)
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (col0 + j >= a.V) g[j] = 0.0f;
+      }
+      const long long rel = xr - col0;
+      if (rel >= 0 && rel < 32) {  // the target column: subtract the one-hot (rare)
+        const int ri = static_cast<int>(rel);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) g[j] = (j == ri) ? g[j] - 1.0f : g[j];
+      }
       uint32_t pk[16];
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
-        float g2[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int col = col0 + j + u;
-          float g = ex2(fmaf(__uint_as_float(r[j + u]), LOG2E, -lse2));
-          if (static_cast<long long>(col) == xr) g -= 1.0f;
-          if (!valid || col >= a.V) g = 0.0f;
-          surv |= fabsf(g) >= a.eps;
-          g2[u] = g * w;
-        }
-        pk[j / 2] = pack_bf16x2(g2[0], g2[1]);
+        amax = fmaxf(amax, fmaxf(fabsf(g[j]), fabsf(g[j + 1])));
+        pk[j / 2] = pack_bf16x2(g[j] * w, g[j + 1] * w);
       }
       const uint32_t box = sbuf + static_cast<uint32_t>((cc >> 1) * 4096);
 #pragma unroll
@@ -471,6 +489,7 @@ __device__ __forceinline__ bool epi_bwd_g(const GemmArgs& a, const SmemLayout& L
         st_shared_v4(box + swz(lane, (cc & 1) * 4 + u), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
       }
     }
+    const bool surv = amax >= a.eps;
     if (h == 1) release_tmem(L, acc);
     // Tile-wide vote: every epilogue warp contributes, one mbarrier phase per tile.
     const int any = __any_sync(0xffffffffu, surv) ? 1 : 0;
