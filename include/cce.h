@@ -174,6 +174,13 @@ typedef struct {
 
 cce_status cce_memory_accounting(int64_t N, int64_t D, int64_t V, cce_memory_report* out /* host */);
 
+/* Self-test of the failure path of every in-kernel wait.  Launches one
+ * thread that waits, through the same bounded wait the GEMM pipelines use, on
+ * an mbarrier nothing arrives on; after timeout_us (1 .. 10^7) microseconds the
+ * wait gives up and ORs CCE_DEVERR_TIMEOUT into *dev_err (device memory).  No
+ * fault, no hang: the context stays usable.  Asynchronous on `stream`. */
+cce_status cce_selftest_wait_timeout(int32_t* dev_err, uint32_t timeout_us, void* stream);
+
 /* Human-readable name of a status. */
 const char* cce_status_string(cce_status s);
 

@@ -68,6 +68,8 @@ def load() -> ctypes.CDLL:
     lib.cce_backward.restype = ctypes.c_int
     lib.cce_forward_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, ctypes.c_int, vp, vp, vp, vp]
     lib.cce_forward_noalloc.restype = ctypes.c_int
+    lib.cce_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint32, vp]
+    lib.cce_selftest_wait_timeout.restype = ctypes.c_int
     lib.cce_memory_accounting.argtypes = [i64, i64, i64, ctypes.POINTER(MemoryReport)]
     lib.cce_memory_accounting.restype = ctypes.c_int
     lib.cce_status_string.argtypes = [ctypes.c_int]

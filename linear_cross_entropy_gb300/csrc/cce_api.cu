@@ -655,6 +655,18 @@ cce_status cce_backward(const void* E, const void* C, const int64_t* x, const fl
   return CCE_OK;
 }
 
+cce_status cce_selftest_wait_timeout(int32_t* dev_err, uint32_t timeout_us, void* stream) {
+  if (!dev_err) return CCE_ERR_NULL;
+  if (timeout_us == 0 || timeout_us > 10000000u) return CCE_ERR_ARG;
+  int sms = 0;
+  cce_status st = device_check(&sms);
+  if (st != CCE_OK) return st;
+  cudaError_t e = launch_selftest_wait_timeout(dev_err, static_cast<uint64_t>(timeout_us) * 1000u,
+                                               static_cast<cudaStream_t>(stream));
+  g_launches++;
+  return cuda_status(e);
+}
+
 cce_status cce_profile_enable(int enable) {
   std::lock_guard<std::mutex> lk(g_mu);
   g_prof = enable != 0;

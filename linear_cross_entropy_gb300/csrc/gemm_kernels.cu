@@ -16,6 +16,23 @@ cudaError_t prepare_gemm_kernels() {
   return set_smem<MODE_GRAD>();
 }
 
+// One thread waits on an mbarrier that nothing ever arrives on, through the
+// same bounded wait the GEMM pipelines use; the wait must run out and report
+// CCE_DEVERR_TIMEOUT instead of hanging.
+__global__ void selftest_wait_timeout_kernel(int32_t* dev_err, uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  mbar_init(&bar, 1);
+  abort_flag = 0;
+  fence_mbar_init();
+  wait_bounded_ns(&bar, 0, &abort_flag, dev_err, timeout_ns);
+}
+
+cudaError_t launch_selftest_wait_timeout(int32_t* dev_err, uint64_t timeout_ns, cudaStream_t stream) {
+  selftest_wait_timeout_kernel<<<1, 1, 0, stream>>>(dev_err, timeout_ns);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gemm(int mode, const GemmArgs& args, int grid, cudaStream_t stream) {
   const dim3 g(static_cast<unsigned>(grid)), b(NUM_THREADS);
   switch (mode) {

@@ -62,22 +62,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits until the phase with the given parity of *bar has completed.  Returns
-// false (and raises *abort_flag) if the wait ran out, or if another role of the
-// CTA already aborted.  Call from a single thread.
-__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                             int32_t* dev_err) {
+// false (and raises *abort_flag) if the wait ran out after timeout_ns, or if
+// another role of the CTA already aborted.  Call from a single thread.
+__device__ __forceinline__ bool wait_bounded_ns(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                int32_t* dev_err, uint64_t timeout_ns) {
   const uint32_t b = smem_u32(bar);
   if (mbar_try_wait(b, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
     if (mbar_try_wait(b, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer() - t0 > CCE_WAIT_TIMEOUT_NS) {
+    if (globaltimer() - t0 > timeout_ns) {
       *abort_flag = 1;
       if (dev_err) atomicOr(reinterpret_cast<int*>(dev_err), CCE_DEVERR_TIMEOUT);
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                             int32_t* dev_err) {
+  return wait_bounded_ns(bar, parity, abort_flag, dev_err, CCE_WAIT_TIMEOUT_NS);
 }
 
 // Warp-uniform bounded wait: lane 0 waits, the result is broadcast.
