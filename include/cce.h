@@ -156,6 +156,42 @@ cce_status cce_forward_noalloc(const void* E, const void* C, const int64_t* x, i
                                int64_t ignore_index, int reduction, float* loss, float* lse, int32_t* dev_err,
                                void* stream);
 
+/*
+ * Forward with logit softcapping.  cce_forward is cce_forward_ex with
+ * softcap = 0.  With softcap > 0 every logit a becomes softcap * tanh(a /
+ * softcap) before the log-sum-exp and the target capture (Gemma 2's final
+ * logits; "Cut Your Losses ...", Table A2 times softcapping as a stage of the
+ * backward).  softcap must be finite and >= 0, else CCE_ERR_ARG.
+ */
+cce_status cce_forward_ex(const void* E, const void* C, const int64_t* x, int64_t N, int64_t D, int64_t V,
+                          int64_t ignore_index, int reduction, float softcap, float* loss, float* lse,
+                          void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream);
+
+/*
+ * Backward with softcapping and per-output filtering.  cce_backward is
+ * cce_backward_ex with softcap = 0 and CCE_FILTER_BOTH.  softcap must match
+ * the forward's; the gradient then carries the slope 1 - tanh^2(a / softcap),
+ * while the filter still tests |softmax - onehot| before that slope.
+ * filter_flags chooses which gradients skip the filtered tiles ("Cut Your
+ * Losses ...", "Numerical Stability Variants"):
+ *   CCE_FILTER_BOTH  dE and dC skip them (plain CCE);
+ *   CCE_FILTER_DE    only dE skips them; dC is computed from every tile, so no
+ *                    vocabulary row is starved of gradient (CCE-Kahan-FullC, the
+ *                    pages' pretraining setting; accumulation is fp32 here, so
+ *                    no Kahan compensation is needed);
+ *   CCE_FILTER_DC    only dC skips them (CCE-Kahan-FullE);
+ *   0                neither (same as filter_eps = 0).
+ * The survival map and dev_stats always describe the filter decisions.  Any
+ * other flag bit returns CCE_ERR_ARG.
+ */
+#define CCE_FILTER_DE 1
+#define CCE_FILTER_DC 2
+#define CCE_FILTER_BOTH 3
+cce_status cce_backward_ex(const void* E, const void* C, const int64_t* x, const float* lse,
+                           const float* grad_out, int64_t N, int64_t D, int64_t V, int64_t ignore_index,
+                           int reduction, float softcap, float filter_eps, int filter_flags, void* dE, void* dC,
+                           void* workspace, size_t ws_bytes, int32_t* dev_err, int64_t* dev_stats, void* stream);
+
 /* Memory accounting (host arithmetic, no GPU).  Reproduces the page's memory
  * table ("Cut Cross-Entropy: Training Loss Without the Logit Matrix ...",
  * section "The memory numbers hold up"): the fp32 N x V logit buffer that the

@@ -85,9 +85,10 @@ def _raise_dev_err(dev_err):
         raise CCEError(8, "target index outside [0, V) and not ignore_index")
 
 
-def cce_forward(E, C, x, ignore_index=-100, reduction="mean", *, stream=None, check_errors=True,
+def cce_forward(E, C, x, ignore_index=-100, reduction="mean", *, softcap=0.0, stream=None, check_errors=True,
                 workspace=None, dev_err=None):
-    """Returns (loss, lse).  loss is [N] for reduction='none', else a 0-d tensor."""
+    """Returns (loss, lse).  loss is [N] for reduction='none', else a 0-d tensor.
+    softcap > 0 caps the logits as softcap * tanh(logit / softcap)."""
     _check_inputs(E, C, x)
     N, D = E.shape
     V = C.shape[0]
@@ -102,17 +103,25 @@ def cce_forward(E, C, x, ignore_index=-100, reduction="mean", *, stream=None, ch
     if dev_err is None:
         dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
     with torch.cuda.device(dev):
-        st = lib.cce_forward(_ptr(E), _ptr(C), _ptr(x), N, D, V, int(ignore_index), red, _ptr(loss), _ptr(lse),
-                             _ptr(workspace), workspace.numel(), _ptr(dev_err), _stream_handle(stream))
+        st = lib.cce_forward_ex(_ptr(E), _ptr(C), _ptr(x), N, D, V, int(ignore_index), red, float(softcap),
+                                _ptr(loss), _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(dev_err),
+                                _stream_handle(stream))
     _lib.check(st, "cce_forward")
     if check_errors:
         _raise_dev_err(dev_err)
     return (loss if red == 0 else loss.reshape(())), lse
 
 
+FILTER_OUTPUTS = {"both": 3, "dE": 1, "dC": 2, "none": 0}
+
+
 def cce_backward(E, C, x, lse, grad_out, ignore_index=-100, reduction="mean", filter_eps=FILTER_EPS, *,
-                 stream=None, check_errors=True, workspace=None, dev_err=None, stats=False, dE=None, dC=None):
-    """Returns (dE, dC) or (dE, dC, {tiles, skipped}) with stats=True."""
+                 filter_outputs="both", softcap=0.0, stream=None, check_errors=True, workspace=None,
+                 dev_err=None, stats=False, dE=None, dC=None):
+    """Returns (dE, dC) or (dE, dC, {tiles, skipped}) with stats=True.
+
+    filter_outputs: which gradients skip the filtered tiles -- "both" (plain
+    CCE), "dE" (dC from every tile: CCE-Kahan-FullC), "dC" (FullE) or "none"."""
     _check_inputs(E, C, x)
     N, D = E.shape
     V = C.shape[0]
@@ -134,9 +143,10 @@ def cce_backward(E, C, x, lse, grad_out, ignore_index=-100, reduction="mean", fi
         dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
     st_t = torch.zeros(2, dtype=torch.int64, device=dev) if stats else None
     with torch.cuda.device(dev):
-        st = lib.cce_backward(_ptr(E), _ptr(C), _ptr(x), _ptr(lse), _ptr(g), N, D, V, int(ignore_index), red,
-                              float(filter_eps), _ptr(dE), _ptr(dC), _ptr(workspace), workspace.numel(),
-                              _ptr(dev_err), _ptr(st_t), _stream_handle(stream))
+        st = lib.cce_backward_ex(_ptr(E), _ptr(C), _ptr(x), _ptr(lse), _ptr(g), N, D, V, int(ignore_index), red,
+                                 float(softcap), float(filter_eps), FILTER_OUTPUTS[filter_outputs], _ptr(dE), _ptr(dC),
+                                 _ptr(workspace), workspace.numel(), _ptr(dev_err), _ptr(st_t),
+                                 _stream_handle(stream))
     _lib.check(st, "cce_backward")
     if check_errors:
         _raise_dev_err(dev_err)
@@ -148,26 +158,31 @@ def cce_backward(E, C, x, lse, grad_out, ignore_index=-100, reduction="mean", fi
 
 class LinearCrossEntropyFunction(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, E, C, x, ignore_index, reduction, filter_eps):
-        loss, lse = cce_forward(E, C, x, ignore_index, reduction)
+    def forward(ctx, E, C, x, ignore_index, reduction, filter_eps, filter_outputs, softcap):
+        loss, lse = cce_forward(E, C, x, ignore_index, reduction, softcap=softcap)
         ctx.save_for_backward(E, C, x, lse)
-        ctx.cfg = (ignore_index, reduction, filter_eps)
+        ctx.cfg = (ignore_index, reduction, filter_eps, filter_outputs, softcap)
         return loss
 
     @staticmethod
     def backward(ctx, grad_loss):
         E, C, x, lse = ctx.saved_tensors
-        ignore_index, reduction, filter_eps = ctx.cfg
-        dE, dC = cce_backward(E, C, x, lse, grad_loss, ignore_index, reduction, filter_eps)
-        return dE, dC, None, None, None, None
+        ignore_index, reduction, filter_eps, filter_outputs, softcap = ctx.cfg
+        dE, dC = cce_backward(E, C, x, lse, grad_loss, ignore_index, reduction, filter_eps,
+                              filter_outputs=filter_outputs, softcap=softcap)
+        return dE, dC, None, None, None, None, None, None
 
 
-def linear_cross_entropy(E, C, x, ignore_index=-100, reduction="mean", filter_eps=FILTER_EPS):
+def linear_cross_entropy(E, C, x, ignore_index=-100, reduction="mean", filter_eps=FILTER_EPS,
+                         filter_outputs="both", softcap=0.0):
     """Cross-entropy of the logits E @ C^T against targets x, never materialised.
 
     E [N, D] bf16 (hidden states), C [V, D] bf16 (classifier weight), x [N]
-    int64.  filter_eps is the backward's tile-skip threshold (0 disables)."""
-    return LinearCrossEntropyFunction.apply(E, C, x, ignore_index, reduction, filter_eps)
+    int64.  filter_eps is the backward's tile-skip threshold (0 disables);
+    filter_outputs picks which gradients it applies to ("both", "dE", "dC",
+    "none"); softcap > 0 caps the logits as softcap * tanh(logit / softcap)."""
+    return LinearCrossEntropyFunction.apply(E, C, x, ignore_index, reduction, filter_eps, filter_outputs,
+                                            softcap)
 
 
 @dataclass

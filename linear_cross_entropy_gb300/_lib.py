@@ -66,6 +66,12 @@ def load() -> ctypes.CDLL:
     lib.cce_backward.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_int, ctypes.c_float,
                                  vp, vp, vp, sz, vp, vp, vp]
     lib.cce_backward.restype = ctypes.c_int
+    lib.cce_forward_ex.argtypes = [vp, vp, vp, i64, i64, i64, i64, ctypes.c_int, ctypes.c_float, vp, vp, vp, sz,
+                                   vp, vp]
+    lib.cce_forward_ex.restype = ctypes.c_int
+    lib.cce_backward_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_int, ctypes.c_float,
+                                    ctypes.c_float, ctypes.c_int, vp, vp, vp, sz, vp, vp, vp]
+    lib.cce_backward_ex.restype = ctypes.c_int
     lib.cce_forward_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, ctypes.c_int, vp, vp, vp, vp]
     lib.cce_forward_noalloc.restype = ctypes.c_int
     lib.cce_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint32, vp]

@@ -456,12 +456,20 @@ cce_status cce_memory_accounting(int64_t N, int64_t D, int64_t V, cce_memory_rep
 cce_status cce_forward(const void* E, const void* C, const int64_t* x, int64_t N, int64_t D, int64_t V,
                        int64_t ignore_index, int reduction, float* loss, float* lse, void* workspace,
                        size_t ws_bytes, int32_t* dev_err, void* stream) {
+  return cce_forward_ex(E, C, x, N, D, V, ignore_index, reduction, 0.0f, loss, lse, workspace, ws_bytes, dev_err,
+                        stream);
+}
+
+cce_status cce_forward_ex(const void* E, const void* C, const int64_t* x, int64_t N, int64_t D, int64_t V,
+                          int64_t ignore_index, int reduction, float softcap, float* loss, float* lse,
+                          void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream) {
   if (!E || !C || !x || !loss || !lse || !workspace) return CCE_ERR_NULL;
   if (!sizes_ok(N, D, V)) return CCE_ERR_SHAPE;
   if (!aligned16(E) || !aligned16(C) || !aligned16(loss) || !aligned16(lse) || !aligned16(workspace) ||
       (reinterpret_cast<uintptr_t>(x) & 7u))
     return CCE_ERR_ALIGN;
   if (reduction != CCE_RED_NONE && reduction != CCE_RED_SUM && reduction != CCE_RED_MEAN) return CCE_ERR_ARG;
+  if (!(softcap >= 0.0f) || !std::isfinite(softcap)) return CCE_ERR_ARG;
   const FwdLayout W = fwd_layout(N, V);
   if (ws_bytes < W.total) return CCE_ERR_WORKSPACE;
   int sms = 0;
@@ -489,6 +497,8 @@ cce_status cce_forward(const void* E, const void* C, const int64_t* x, int64_t N
   a.part_m = reinterpret_cast<float*>(ws + W.part_m);
   a.part_s = reinterpret_cast<float*>(ws + W.part_s);
   a.tgt = reinterpret_cast<float*>(ws + W.tgt);
+  a.softcap = softcap;
+  a.inv_softcap = softcap > 0.0f ? 1.0f / softcap : 0.0f;
   a.dev_err = dev_err;
   a.counter = reinterpret_cast<int*>(ws + W.counter);
   const int units = a.n_blocks * a.splits;
@@ -524,6 +534,14 @@ cce_status cce_backward(const void* E, const void* C, const int64_t* x, const fl
                         int64_t N, int64_t D, int64_t V, int64_t ignore_index, int reduction, float filter_eps,
                         void* dE, void* dC, void* workspace, size_t ws_bytes, int32_t* dev_err,
                         int64_t* dev_stats, void* stream) {
+  return cce_backward_ex(E, C, x, lse, grad_out, N, D, V, ignore_index, reduction, 0.0f, filter_eps,
+                         CCE_FILTER_BOTH, dE, dC, workspace, ws_bytes, dev_err, dev_stats, stream);
+}
+
+cce_status cce_backward_ex(const void* E, const void* C, const int64_t* x, const float* lse, const float* grad_out,
+                           int64_t N, int64_t D, int64_t V, int64_t ignore_index, int reduction, float softcap,
+                           float filter_eps, int filter_flags, void* dE, void* dC, void* workspace, size_t ws_bytes,
+                           int32_t* dev_err, int64_t* dev_stats, void* stream) {
   if (!E || !C || !x || !lse || !grad_out || !dE || !dC || !workspace) return CCE_ERR_NULL;
   if (!sizes_ok(N, D, V)) return CCE_ERR_SHAPE;
   if (!aligned16(E) || !aligned16(C) || !aligned16(lse) || !aligned16(dE) || !aligned16(dC) ||
@@ -532,6 +550,8 @@ cce_status cce_backward(const void* E, const void* C, const int64_t* x, const fl
     return CCE_ERR_ALIGN;
   if (reduction != CCE_RED_NONE && reduction != CCE_RED_SUM && reduction != CCE_RED_MEAN) return CCE_ERR_ARG;
   if (!(filter_eps >= 0.0f) || !std::isfinite(filter_eps)) return CCE_ERR_ARG;
+  if (filter_flags & ~CCE_FILTER_BOTH) return CCE_ERR_ARG;
+  if (!(softcap >= 0.0f) || !std::isfinite(softcap)) return CCE_ERR_ARG;
   const BwdLayout W = bwd_layout(N, D, V);
   if (ws_bytes < W.total) return CCE_ERR_WORKSPACE;
   int sms = 0;
@@ -588,6 +608,10 @@ cce_status cce_backward(const void* E, const void* C, const int64_t* x, const fl
     p->count = count;
     p->reduction = reduction;
     p->eps = filter_eps;
+    p->softcap = softcap;
+    p->inv_softcap = softcap > 0.0f ? 1.0f / softcap : 0.0f;
+    p->filter_de = (filter_flags & CCE_FILTER_DE) ? 1 : 0;
+    p->filter_dc = (filter_flags & CCE_FILTER_DC) ? 1 : 0;
     p->bitmap = bitmap;
     p->bitmapT = ws + W.bitmapT;
     p->bm_ld = static_cast<int>(W.bm_ld);

@@ -99,8 +99,11 @@ __device__ __forceinline__ int kblocks_of(const GemmArgs& a, const Tile& t) {
 template <int MODE>
 __device__ __forceinline__ bool kblock_skipped(const GemmArgs& a, const Tile& t, int kb) {
   if constexpr (MODE == MODE_GRAD) {
-    if (t.kind == KIND_DC)
+    if (t.kind == KIND_DC) {
+      if (!a.filter_dc) return false;
       return __ldg(a.bitmapT + static_cast<size_t>((a.chunk_v0 >> 7) + t.m) * a.n_blocks + (kb >> 1)) == 0;
+    }
+    if (!a.filter_de) return false;
     return __ldg(a.bitmap + static_cast<size_t>(t.m) * a.bm_ld + (a.chunk_v0 >> 7) + (kb >> 1)) == 0;
   }
   return false;
@@ -108,6 +111,7 @@ __device__ __forceinline__ bool kblock_skipped(const GemmArgs& a, const Tile& t,
 
 // Warp-wide: does the output tile have no surviving K-block at all?
 __device__ __forceinline__ bool tile_empty(const GemmArgs& a, const Tile& t) {
+  if (!(t.kind == KIND_DC ? a.filter_dc : a.filter_de)) return false;  // this output is not filtered
   int any = 0;
   if (t.kind == KIND_DC) {
     const uint8_t* row = a.bitmapT + static_cast<size_t>((a.chunk_v0 >> 7) + t.m) * a.n_blocks;
@@ -351,6 +355,13 @@ struct FwdState {
   float run_m, run_s;
 };
 
+// Softcapped logits: a' = cap * tanh(a / cap), in place (tanhf: accurate to a
+// few ulp, which the 1e-5 LSE bar needs).
+__device__ __forceinline__ void softcap_chunk(uint32_t (&r)[32], float cap, float inv_cap) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(cap * tanhf(__uint_as_float(r[j]) * inv_cap));
+}
+
 __device__ __forceinline__ void fold_chunk(const uint32_t (&r)[32], int col0, int V, long long xr, float& run_m,
                                            float& run_s, float& tval, bool& tfound) {
   const int nvalid = min(32, V - col0);  // < 32 only in the last tile of a ragged vocabulary
@@ -389,6 +400,7 @@ __device__ __forceinline__ void fold_chunk(const uint32_t (&r)[32], int col0, in
   run_m = nm;
 }
 
+template <bool CAP>
 __device__ __forceinline__ void epi_fwd(const GemmArgs& a, const SmemLayout& L, const Tile& t, int acc,
                                         EpiCtx& e, FwdState& st) {
   const int row = t.m * BM + e.q * 32 + static_cast<int>(lane_id());
@@ -410,6 +422,10 @@ __device__ __forceinline__ void epi_fwd(const GemmArgs& a, const SmemLayout& L, 
     tmem_ld32(tbase + 32 * c, r0);
     tmem_ld32(tbase + 32 * (c + 1), r1);
     tmem_ld_wait();
+    if constexpr (CAP) {
+      softcap_chunk(r0, a.softcap, a.inv_softcap);
+      softcap_chunk(r1, a.softcap, a.inv_softcap);
+    }
     fold_chunk(r0, col0, a.V, xr, st.run_m, st.run_s, tval, tfound);
     if (col0 + 32 < a.V) fold_chunk(r1, col0 + 32, a.V, xr, st.run_m, st.run_s, tval, tfound);
   }
@@ -422,6 +438,7 @@ __device__ __forceinline__ void epi_fwd(const GemmArgs& a, const SmemLayout& L, 
 }
 
 // BWD_G: G = exp(A - LSE) - onehot, filter vote per 128-column half, bf16 store.
+template <bool CAP>
 __device__ __forceinline__ bool epi_bwd_g(const GemmArgs& a, const SmemLayout& L, const Tile& t, int acc,
                                           EpiCtx& e) {
   const uint32_t lane = lane_id();
@@ -464,8 +481,21 @@ __device__ __forceinline__ bool epi_bwd_g(const GemmArgs& a, const SmemLayout& L
       tmem_ld32(tbase + 32 * c, r);
       tmem_ld_wait();
       float g[32];
+      float slope[32];  // d(capped logit) / d(logit); 1 without a cap
+      if constexpr (CAP) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) g[j] = ex2(fmaf(__uint_as_float(r[j]), LOG2E, -lse2));
+        for (int j = 0; j < 32; ++j) {
+          const float th = tanhf(__uint_as_float(r[j]) * a.inv_softcap);
+          slope[j] = 1.0f - th * th;
+          g[j] = ex2(fmaf(a.softcap * th, LOG2E, -lse2));
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          slope[j] = 1.0f;
+          g[j] = ex2(fmaf(__uint_as_float(r[j]), LOG2E, -lse2));
+        }
+      }
       if (col0 + 32 > a.V) {  // ragged last tile: columns past V are zero (uniform branch)
 #pragma unroll
         for (int j = 0; j < 32; ++j)
@@ -480,8 +510,8 @@ __device__ __forceinline__ bool epi_bwd_g(const GemmArgs& a, const SmemLayout& L
       uint32_t pk[16];
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
-        amax = fmaxf(amax, fmaxf(fabsf(g[j]), fabsf(g[j + 1])));
-        pk[j / 2] = pack_bf16x2(g[j] * w, g[j + 1] * w);
+        amax = fmaxf(amax, fmaxf(fabsf(g[j]), fabsf(g[j + 1])));  // the filter tests |G| before the slope
+        pk[j / 2] = pack_bf16x2(g[j] * slope[j] * w, g[j + 1] * slope[j + 1] * w);
       }
       const uint32_t box = sbuf + static_cast<uint32_t>((cc >> 1) * 4096);
 #pragma unroll
@@ -505,7 +535,8 @@ __device__ __forceinline__ bool epi_bwd_g(const GemmArgs& a, const SmemLayout& L
     int kv = 0;
     if (lane == 0) kv = fl[0] | fl[1] | fl[2] | fl[3];  // lane 0 performed the acquiring wait
     const bool keep = __shfl_sync(0xffffffffu, kv, 0) != 0;
-    if (keep) {
+    // A skipped tile's G is still needed when one of the outputs is unfiltered.
+    if (keep || !(a.filter_de && a.filter_dc)) {
       fence_proxy_async_smem();
       __syncwarp();
       const int gx = t.n * BN + 128 * h;  // column inside the chunk buffer
@@ -614,7 +645,7 @@ __device__ __forceinline__ void epi_de(const GemmArgs& a, const SmemLayout& L, c
   release_tmem(L, acc);
 }
 
-template <int MODE>
+template <int MODE, bool CAP>
 __device__ __forceinline__ void epilogue_loop(const GemmArgs& a, const SmemLayout& L, uint32_t tmem_base,
                                               int warp) {
   EpiCtx e;
@@ -636,9 +667,9 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& a, const SmemLayou
       tc_fence_after();
       bool r = true;
       if constexpr (MODE == MODE_FWD) {
-        epi_fwd(a, L, t, acc, e, st);
+        epi_fwd<CAP>(a, L, t, acc, e, st);
       } else if constexpr (MODE == MODE_BWD_G) {
-        r = epi_bwd_g(a, L, t, acc, e);
+        r = epi_bwd_g<CAP>(a, L, t, acc, e);
       } else {
         if (t.kind == KIND_DC) {
           epi_dc(a, L, t, acc, e);
@@ -657,7 +688,9 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& a, const SmemLayou
   __syncwarp();
 }
 
-template <int MODE>
+// CAP: logit softcapping in the FWD / BWD_G epilogues (a separate
+// instantiation, so the common path carries none of its registers).
+template <int MODE, bool CAP = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1) cce_gemm_kernel(const __grid_constant__ GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const SmemLayout L = carve_smem(smem_raw);
@@ -704,7 +737,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cce_gemm_kernel(const __grid_c
   } else if (warp == 1) {
     if (lane_id() == 0) mma_loop<MODE>(a, L, tmem_base);
   } else {
-    epilogue_loop<MODE>(a, L, tmem_base, warp);
+    epilogue_loop<MODE, CAP>(a, L, tmem_base, warp);
   }
 
   tc_fence_before();

@@ -71,6 +71,10 @@ struct GemmArgs {
   const int* count;
   int reduction;
   float eps;
+  float softcap;      // > 0: logits are softcap * tanh(logit / softcap)
+  float inv_softcap;  // 1 / softcap
+  int filter_de;  // 1: dE skips the K-blocks of skipped filter tiles
+  int filter_dc;  // 1: dC skips them (0: dC uses every tile, as CCE-Kahan-FullC)
   uint8_t* bitmap;   // [ceil(N/128)][bm_ld] tile survival, token-block major
   uint8_t* bitmapT;  // [bm_ld][ceil(N/128)] the same, vocabulary-block major (read along K by dC)
   int bm_ld;         // ceil(V / 128)

@@ -4,16 +4,18 @@
 
 namespace cce {
 
-template <int MODE>
+template <int MODE, bool CAP>
 static cudaError_t set_smem() {
-  return cudaFuncSetAttribute(cce_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  return cudaFuncSetAttribute(cce_gemm_kernel<MODE, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
 }
 
 cudaError_t prepare_gemm_kernels() {
   cudaError_t e;
-  if ((e = set_smem<MODE_FWD>()) != cudaSuccess) return e;
-  if ((e = set_smem<MODE_BWD_G>()) != cudaSuccess) return e;
-  return set_smem<MODE_GRAD>();
+  if ((e = set_smem<MODE_FWD, false>()) != cudaSuccess) return e;
+  if ((e = set_smem<MODE_FWD, true>()) != cudaSuccess) return e;
+  if ((e = set_smem<MODE_BWD_G, false>()) != cudaSuccess) return e;
+  if ((e = set_smem<MODE_BWD_G, true>()) != cudaSuccess) return e;
+  return set_smem<MODE_GRAD, false>();
 }
 
 // One thread waits on an mbarrier that nothing ever arrives on, through the
@@ -35,10 +37,23 @@ cudaError_t launch_selftest_wait_timeout(int32_t* dev_err, uint64_t timeout_ns, 
 
 cudaError_t launch_gemm(int mode, const GemmArgs& args, int grid, cudaStream_t stream) {
   const dim3 g(static_cast<unsigned>(grid)), b(NUM_THREADS);
+  const bool cap = args.softcap > 0.0f;
   switch (mode) {
-    case MODE_FWD: cce_gemm_kernel<MODE_FWD><<<g, b, SMEM_BYTES, stream>>>(args); break;
-    case MODE_BWD_G: cce_gemm_kernel<MODE_BWD_G><<<g, b, SMEM_BYTES, stream>>>(args); break;
-    case MODE_GRAD: cce_gemm_kernel<MODE_GRAD><<<g, b, SMEM_BYTES, stream>>>(args); break;
+    case MODE_FWD:
+      if (cap) {
+        cce_gemm_kernel<MODE_FWD, true><<<g, b, SMEM_BYTES, stream>>>(args);
+      } else {
+        cce_gemm_kernel<MODE_FWD, false><<<g, b, SMEM_BYTES, stream>>>(args);
+      }
+      break;
+    case MODE_BWD_G:
+      if (cap) {
+        cce_gemm_kernel<MODE_BWD_G, true><<<g, b, SMEM_BYTES, stream>>>(args);
+      } else {
+        cce_gemm_kernel<MODE_BWD_G, false><<<g, b, SMEM_BYTES, stream>>>(args);
+      }
+      break;
+    case MODE_GRAD: cce_gemm_kernel<MODE_GRAD, false><<<g, b, SMEM_BYTES, stream>>>(args); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

@@ -32,6 +32,11 @@ Passages followed (page title, section):
 * "cut-cross-entropy" kernel card -- "Correctness": ignore_index rows add no
   loss and get exactly zero gradient; a fully masked batch has zero loss and
   zero gradients; reductions none / sum / mean.
+* Logit softcapping (Gemma 2's final logits; the paper's backward-pass
+  breakdown, "Cut Your Losses ...", Table A2, times it as its own stage):
+  with cap > 0 the logits are a'_iv = cap tanh(a_iv / cap); LSE, loss and
+  G = softmax(a') - onehot use a', and the gradient reaching E and C is
+  G (1 - tanh^2(a / cap)).  The filter tests |G| before that factor.
 * Reading where the pages are silent: mean divides by the number of
   non-ignored rows, clamped to at least 1 (the chunked-CE code on the
   "fused-linear-cross-entropy" page clamps the count the same way); the LSE of
@@ -75,13 +80,23 @@ def logits(E: np.ndarray, C: np.ndarray) -> np.ndarray:
     return E @ C.T
 
 
+def softcap_logits(A: np.ndarray, softcap: float) -> np.ndarray:
+    """a' = cap tanh(a / cap) (identity when cap == 0)."""
+    return A if not softcap else softcap * np.tanh(A / softcap)
+
+
+def softcap_slope(A: np.ndarray, softcap: float):
+    """d a' / d a = 1 - tanh^2(a / cap) (1 when cap == 0)."""
+    return 1.0 if not softcap else 1.0 - np.tanh(A / softcap) ** 2
+
+
 def log_sum_exp(A: np.ndarray) -> np.ndarray:
     """Row-wise LSE_i = m_i + log sum_v exp(a_iv - m_i)."""
     m = A.max(axis=1)
     return m + np.log(np.exp(A - m[:, None]).sum(axis=1))
 
 
-def forward(E, C, x, ignore_index=IGNORE_INDEX, reduction="mean", rows=None):
+def forward(E, C, x, ignore_index=IGNORE_INDEX, reduction="mean", rows=None, softcap=0.0):
     """Forward pass for the listed rows (all rows when rows is None).
 
     Returns a dict with per-row ``lse``, ``target_logit`` (NaN on ignored
@@ -97,7 +112,7 @@ def forward(E, C, x, ignore_index=IGNORE_INDEX, reduction="mean", rows=None):
     tgt = np.full(len(idx), np.nan)
     for r0, r1 in _row_blocks(len(idx), V):
         rr = idx[r0:r1]
-        A = logits(E[rr], C)
+        A = softcap_logits(logits(E[rr], C), softcap)
         lse[r0:r1] = log_sum_exp(A)
         xr = x[rr]
         ok = xr != ignore_index
@@ -115,14 +130,14 @@ def forward(E, C, x, ignore_index=IGNORE_INDEX, reduction="mean", rows=None):
     return out
 
 
-def indexed_logits(E, C, x, ignore_index=IGNORE_INDEX):
+def indexed_logits(E, C, x, ignore_index=IGNORE_INDEX, softcap=0.0):
     """o_i = C[x_i] . E_i, the indexed matrix product (NaN on ignored rows)."""
     E = np.asarray(E, np.float64)
     C = np.asarray(C, np.float64)
     x = np.asarray(x, np.int64)
     ok = x != ignore_index
     out = np.full(E.shape[0], np.nan)
-    out[ok] = np.einsum("nd,nd->n", E[ok], C[x[ok]])
+    out[ok] = softcap_logits(np.einsum("nd,nd->n", E[ok], C[x[ok]]), softcap)
     return out
 
 
@@ -154,13 +169,15 @@ def row_weights(x, ignore_index, reduction, grad_out, count=None):
     raise ValueError(reduction)
 
 
-def grad_logits(A, lse, x_rows, v0=0, ignore_index=IGNORE_INDEX):
-    """G = exp(A - LSE) - onehot(x) for a block of logits.
+def grad_logits(A, lse, x_rows, v0=0, ignore_index=IGNORE_INDEX, softcap=0.0):
+    """G = exp(A' - LSE) - onehot(x) for a block of raw logits A (A' = the
+    softcapped logits; A' = A without a cap).
 
     A holds rows (tokens) x columns v0 .. v0 + A.shape[1] - 1 of the logit
-    matrix; ignored rows are all zero.
+    matrix; ignored rows are all zero.  This is the gradient with respect to
+    A'; the filter tests it.
     """
-    G = np.exp(A - np.asarray(lse)[:, None])
+    G = np.exp(softcap_logits(A, softcap) - np.asarray(lse)[:, None])
     x_rows = np.asarray(x_rows, np.int64)
     r = np.nonzero((x_rows >= v0) & (x_rows < v0 + A.shape[1]))[0]
     G[r, x_rows[r] - v0] -= 1.0
@@ -168,21 +185,23 @@ def grad_logits(A, lse, x_rows, v0=0, ignore_index=IGNORE_INDEX):
     return G
 
 
-def backward_dE(E, C, x, lse_rows, w_rows, rows, ignore_index=IGNORE_INDEX):
-    """dE_i = w_i sum_v G_iv C_v for the listed rows (lse/w given per listed row)."""
+def backward_dE(E, C, x, lse_rows, w_rows, rows, ignore_index=IGNORE_INDEX, softcap=0.0):
+    """dE_i = w_i sum_v G_iv s_iv C_v for the listed rows (lse/w given per
+    listed row; s = softcap slope, 1 without a cap)."""
     E = np.asarray(E, np.float64)
     C = np.asarray(C, np.float64)
     rows = np.asarray(rows, np.int64)
     out = np.empty((len(rows), E.shape[1]))
     for r0, r1 in _row_blocks(len(rows), C.shape[0]):
         rr = rows[r0:r1]
-        G = grad_logits(logits(E[rr], C), lse_rows[r0:r1], x[rr], 0, ignore_index)
+        A = logits(E[rr], C)
+        G = grad_logits(A, lse_rows[r0:r1], x[rr], 0, ignore_index, softcap) * softcap_slope(A, softcap)
         out[r0:r1] = np.asarray(w_rows[r0:r1])[:, None] * (G @ C)
     return out
 
 
-def backward_dC(E, C, x, lse, w, vrows, ignore_index=IGNORE_INDEX):
-    """dC_v = sum_i w_i G_iv E_i for the listed vocabulary rows.
+def backward_dC(E, C, x, lse, w, vrows, ignore_index=IGNORE_INDEX, softcap=0.0):
+    """dC_v = sum_i w_i G_iv s_iv E_i for the listed vocabulary rows.
 
     Needs LSE and w for every token row i.
     """
@@ -191,27 +210,30 @@ def backward_dC(E, C, x, lse, w, vrows, ignore_index=IGNORE_INDEX):
     x = np.asarray(x, np.int64)
     vrows = np.asarray(vrows, np.int64)
     A = logits(E, C[vrows])                      # [N, len(vrows)]
-    G = np.exp(A - np.asarray(lse)[:, None])
+    G = np.exp(softcap_logits(A, softcap) - np.asarray(lse)[:, None])
     G -= (x[:, None] == vrows[None, :]).astype(np.float64)
     G[x == ignore_index] = 0.0
+    G *= softcap_slope(A, softcap)
     return (np.asarray(w)[:, None] * G).T @ E
 
 
-def backward(E, C, x, lse, w, ignore_index=IGNORE_INDEX):
+def backward(E, C, x, lse, w, ignore_index=IGNORE_INDEX, softcap=0.0):
     """Full dE [N, D] and dC [V, D] (small problems: materialises G)."""
     E = np.asarray(E, np.float64)
     C = np.asarray(C, np.float64)
-    G = grad_logits(logits(E, C), lse, x, 0, ignore_index)
+    A = logits(E, C)
+    G = grad_logits(A, lse, x, 0, ignore_index, softcap) * softcap_slope(A, softcap)
     Gw = np.asarray(w)[:, None] * G
     return Gw @ C, Gw.T @ E
 
 
-def tile_survival(E, C, x, lse, BN, BV, eps=FILTER_EPS, ignore_index=IGNORE_INDEX):
+def tile_survival(E, C, x, lse, BN, BV, eps=FILTER_EPS, ignore_index=IGNORE_INDEX, softcap=0.0):
     """Filter decision per (BN x BV) tile: True when some in-range entry has
-    |G_iv| >= eps (unscaled G; ignored rows contribute nothing)."""
+    |G_iv| >= eps (unscaled G = softmax - onehot, before any softcap slope;
+    ignored rows contribute nothing)."""
     E = np.asarray(E, np.float64)
     C = np.asarray(C, np.float64)
-    return tile_keep(grad_logits(logits(E, C), lse, x, 0, ignore_index), BN, BV, eps)
+    return tile_keep(grad_logits(logits(E, C), lse, x, 0, ignore_index, softcap), BN, BV, eps)
 
 
 def tile_keep(G, BN, BV, eps=FILTER_EPS):
@@ -226,16 +248,22 @@ def tile_keep(G, BN, BV, eps=FILTER_EPS):
     return keep
 
 
-def backward_filtered(E, C, x, lse, w, BN, BV, eps=FILTER_EPS, ignore_index=IGNORE_INDEX):
-    """dE, dC with the contributions of skipped tiles removed; also returns
-    the survival map.  With eps = 0 no tile is skipped."""
+def backward_filtered(E, C, x, lse, w, BN, BV, eps=FILTER_EPS, ignore_index=IGNORE_INDEX,
+                      filter_dE=True, filter_dC=True, softcap=0.0):
+    """dE, dC with the contributions of skipped tiles removed from the
+    outputs whose filter is on; also returns the survival map.  With eps = 0
+    no tile is skipped.  filter_dE only ("Cut Your Losses ...", "Numerical
+    Stability Variants": CCE-Kahan-FullC computes dC from every tile) and
+    filter_dC only (CCE-Kahan-FullE)."""
     E = np.asarray(E, np.float64)
     C = np.asarray(C, np.float64)
-    G = grad_logits(logits(E, C), lse, x, 0, ignore_index)
-    keep = tile_survival(E, C, x, lse, BN, BV, eps, ignore_index)
+    A = logits(E, C)
+    G = grad_logits(A, lse, x, 0, ignore_index, softcap)
+    keep = tile_keep(G, BN, BV, eps)
     mask = np.repeat(np.repeat(keep, BN, axis=0), BV, axis=1)[:G.shape[0], :G.shape[1]]
-    Gw = np.asarray(w)[:, None] * np.where(mask, G, 0.0)
-    return Gw @ C, Gw.T @ E, keep
+    Gw = np.asarray(w)[:, None] * G * softcap_slope(A, softcap)
+    Gf = np.where(mask, Gw, 0.0)
+    return (Gf if filter_dE else Gw) @ C, (Gf if filter_dC else Gw).T @ E, keep
 
 
 def from_bits(E_bits, C_bits):
@@ -243,13 +271,13 @@ def from_bits(E_bits, C_bits):
     return widen_bf16(E_bits), widen_bf16(C_bits)
 
 
-def fwd_bwd_rows(E, C, x, rows, ignore_index=IGNORE_INDEX, reduction="mean", grad_out=1.0):
+def fwd_bwd_rows(E, C, x, rows, ignore_index=IGNORE_INDEX, reduction="mean", grad_out=1.0, softcap=0.0):
     """Forward + backward of the sub-problem made of the listed token rows
     (a standalone batch): returns (loss, dE_rows, dC).  Used to time the
     oracle on a bounded sample of a workload."""
     rows = np.asarray(rows, np.int64)
     Es, xs = np.asarray(E)[rows], np.asarray(x)[rows]
-    f = forward(Es, C, xs, ignore_index, reduction)
+    f = forward(Es, C, xs, ignore_index, reduction, softcap=softcap)
     w = row_weights(xs, ignore_index, reduction, grad_out, f["count"])
-    dE, dC = backward(Es, C, xs, f["lse"], w, ignore_index)
+    dE, dC = backward(Es, C, xs, f["lse"], w, ignore_index, softcap)
     return f["loss"], dE, dC

@@ -136,3 +136,14 @@ def test_binding_refuses_cpu_tensors(lib):
     x = torch.zeros(4, dtype=torch.int64)
     with pytest.raises(ValueError, match="CUDA"):
         cce.cce_forward(E, C, x)
+
+
+def test_extended_entry_points_reject_bad_options(lib):
+    vp = ctypes.c_void_p
+    args = [vp(FAKE), vp(FAKE), vp(FAKE), 256, 128, 4096, -100, 2]
+    for cap in (-1.0, float("nan"), float("inf")):
+        assert lib.cce_forward_ex(*args, cap, vp(FAKE), vp(FAKE), vp(FAKE), 1 << 40, vp(0), vp(0)) == 4
+    bargs = [vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), 256, 128, 4096, -100, 2]
+    tail = [vp(FAKE), vp(FAKE), vp(FAKE), 1 << 40, vp(0), vp(0), vp(0)]
+    assert lib.cce_backward_ex(*bargs, 0.0, 2.0 ** -12, 4, *tail) == 4      # unknown flag bit
+    assert lib.cce_backward_ex(*bargs, -3.0, 2.0 ** -12, 3, *tail) == 4     # negative softcap

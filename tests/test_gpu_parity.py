@@ -184,3 +184,50 @@ def test_no_n_by_v_allocation():
     extra = torch.cuda.max_memory_allocated() - base
     outputs = dE.numel() * 2 + dC.numel() * 2 + lse.numel() * 4 + 4
     assert extra - outputs < N * V * 2, (extra, outputs)
+
+
+@pytest.mark.parametrize("outputs,fde,fdc", [("dE", True, False), ("dC", False, True), ("none", False, False)])
+def test_per_output_filter_flags(outputs, fde, fdc):
+    """Per-output filtering (the pages' CCE-Kahan-FullC / FullE variants) on
+    the frequent-token workload, against the oracle with the same flags."""
+    import linear_cross_entropy_gb300 as cce
+    from tests.gpu_util import to_device, bf16_to_f64
+    N, D, V = 512, 128, 6000
+    E, C, x = W.frequent_token_inputs(N, D, V, n_freq=256, seed=3)
+    Et, Ct, xt = to_device(E, C, x)
+    loss, lse = cce.cce_forward(Et, Ct, xt)
+    dE, dC, st = cce.cce_backward(Et, Ct, xt, lse, torch.ones(1, device="cuda"), filter_outputs=outputs,
+                                  stats=True)
+    Ef, Cf = O.from_bits(E, C)
+    f = O.forward(Ef, Cf, x, reduction="mean")
+    w = O.row_weights(x, -100, "mean", 1.0, f["count"])
+    rE, rC, keep = O.backward_filtered(Ef, Cf, x, f["lse"], w, 128, 128, O.FILTER_EPS, filter_dE=fde,
+                                       filter_dC=fdc)
+    assert rel_fro(bf16_to_f64(dE), rE) <= TOL_GRAD
+    assert rel_fro(bf16_to_f64(dC), rC) <= TOL_GRAD
+    assert st["skipped"] == int((~keep).sum()) > 0
+
+
+@pytest.mark.parametrize("filter_on", [False, True])
+def test_softcap_against_oracle(filter_on):
+    """Gemma-2-style logit softcapping (cap 30 on peaked logits, so the cap bites)."""
+    import linear_cross_entropy_gb300 as cce
+    from tests.gpu_util import to_device, bf16_to_f64
+    cap = 30.0
+    N, D, V = 384, 128, 3000
+    w, (E, C, x) = make(W.small("s", N, D, V, c_scale=40.0, boost=20.0, ignore_frac=0.05))
+    Et, Ct, xt = to_device(E, C, x)
+    eps = O.FILTER_EPS if filter_on else 0.0
+    loss, lse = cce.cce_forward(Et, Ct, xt, softcap=cap)
+    dE, dC = cce.cce_backward(Et, Ct, xt, lse, torch.ones(1, device="cuda"), filter_eps=eps, softcap=cap)
+    Ef, Cf = O.from_bits(E, C)
+    f = O.forward(Ef, Cf, x, reduction="mean", softcap=cap)
+    assert np.max(np.abs(Ef @ Cf.T)) > cap  # the cap changes the logits
+    wts = O.row_weights(x, -100, "mean", 1.0, f["count"])
+    rE, rC = O.backward(Ef, Cf, x, f["lse"], wts, softcap=cap)
+    lse_err = np.max(np.abs(lse.double().cpu().numpy() - f["lse"]) / np.abs(f["lse"]))
+    assert lse_err <= 1e-5, lse_err
+    assert abs(loss.item() - f["loss"]) <= 1e-5 * abs(f["loss"])
+    tol = TOL_GRAD_FILTERED if filter_on else TOL_GRAD
+    assert rel_fro(bf16_to_f64(dE), rE) <= tol
+    assert rel_fro(bf16_to_f64(dC), rC) <= tol

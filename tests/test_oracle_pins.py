@@ -322,16 +322,16 @@ def test_true_oracle_passes_pin_suite(rng):
     assert _pin_suite(O, rng) == []
 
 
-def _wrong_sign_onehot(A, lse, x_rows, v0=0, ignore_index=-100):
-    G = np.exp(A - np.asarray(lse)[:, None])
+def _wrong_sign_onehot(A, lse, x_rows, v0=0, ignore_index=-100, softcap=0.0):
+    G = np.exp(O.softcap_logits(A, softcap) - np.asarray(lse)[:, None])
     r = np.nonzero(x_rows != ignore_index)[0]
     G[r, x_rows[r] - v0] += 1.0
     G[x_rows == ignore_index] = 0.0
     return G
 
 
-def _dropped_onehot(A, lse, x_rows, v0=0, ignore_index=-100):
-    G = np.exp(A - np.asarray(lse)[:, None])
+def _dropped_onehot(A, lse, x_rows, v0=0, ignore_index=-100, softcap=0.0):
+    G = np.exp(O.softcap_logits(A, softcap) - np.asarray(lse)[:, None])
     G[x_rows == ignore_index] = 0.0
     return G
 
@@ -393,3 +393,72 @@ def test_widen_bf16_is_exact():
     bits = np.array([0x3F80, 0xC000, 0x0000, 0x8000, 0x3E80, 0x7F7F], dtype=np.uint16)
     assert O.widen_bf16(bits).tolist()[:5] == [1.0, -2.0, 0.0, -0.0, 0.25]
     assert O.widen_bf16(bits)[5] == float(np.float32(3.3895313892515355e38))
+
+
+def test_per_output_filter_flags(rng):
+    """FullC (filter dE only) leaves dC exactly unfiltered; FullE the reverse;
+    both off equals the unfiltered backward."""
+    E, C, x = _problem(rng, 200, 16, 700, scale=3.0, ignore=(1, 150))
+    f = O.forward(E, C, x, reduction="mean")
+    w = O.row_weights(x, -100, "mean", 1.0, f["count"])
+    dE, dC = O.backward(E, C, x, f["lse"], w)
+    dEf, dCf, keep = O.backward_filtered(E, C, x, f["lse"], w, 16, 16, eps=1e-3)
+    assert 0.05 < keep.mean() < 0.95
+    a_dE, a_dC, _ = O.backward_filtered(E, C, x, f["lse"], w, 16, 16, eps=1e-3, filter_dC=False)
+    assert np.array_equal(a_dE, dEf) and np.allclose(a_dC, dC, rtol=1e-13, atol=1e-16)
+    b_dE, b_dC, _ = O.backward_filtered(E, C, x, f["lse"], w, 16, 16, eps=1e-3, filter_dE=False)
+    assert np.allclose(b_dE, dE, rtol=1e-13, atol=1e-16) and np.array_equal(b_dC, dCf)
+    c_dE, c_dC, _ = O.backward_filtered(E, C, x, f["lse"], w, 16, 16, eps=1e-3, filter_dE=False,
+                                        filter_dC=False)
+    assert np.allclose(c_dE, dE, rtol=1e-13, atol=1e-16) and np.allclose(c_dC, dC, rtol=1e-13, atol=1e-16)
+
+
+# ----------------------------------------------------------- softcapping
+@pytest.mark.parametrize("reduction", ["none", "sum", "mean"])
+def test_softcap_matches_torch(rng, reduction):
+    """cap * tanh(logits / cap), cross-entropy and autograd in torch fp64."""
+    cap = 5.0
+    E, C, x = _problem(rng, 48, 16, 200, scale=2.0, ignore=(3, 9))
+    Et = torch.tensor(E, requires_grad=True)
+    Ct = torch.tensor(C, requires_grad=True)
+    A = cap * torch.tanh((Et @ Ct.T) / cap)
+    ref = torch.nn.functional.cross_entropy(A, torch.tensor(x), reduction=reduction)
+    g = rng.standard_normal(48) if reduction == "none" else 1.0
+    ref.backward(torch.tensor(g) if reduction == "none" else None)
+    f = O.forward(E, C, x, reduction=reduction, softcap=cap)
+    w = O.row_weights(x, -100, reduction, g, f["count"])
+    dE, dC = O.backward(E, C, x, f["lse"], w, softcap=cap)
+    assert np.allclose(f["loss"], ref.detach().numpy(), rtol=1e-13, atol=1e-13)
+    assert np.allclose(dE, Et.grad.numpy(), rtol=1e-11, atol=1e-14)
+    assert np.allclose(dC, Ct.grad.numpy(), rtol=1e-11, atol=1e-14)
+    rows = np.array([0, 3, 20])
+    assert np.allclose(O.backward_dE(E, C, x, f["lse"][rows], w[rows], rows, softcap=cap), dE[rows], rtol=1e-12)
+    vr = np.array([1, 50, 199])
+    assert np.allclose(O.backward_dC(E, C, x, f["lse"], w, vr, softcap=cap), dC[vr], rtol=1e-11, atol=1e-15)
+
+
+def test_softcap_finite_differences(rng):
+    cap = 3.0
+    E, C, x = _problem(rng, 4, 5, 9, scale=2.0, ignore=(1,))
+    f = O.forward(E, C, x, reduction="sum", softcap=cap)
+    w = O.row_weights(x, -100, "sum", 1.0)
+    dE, dC = O.backward(E, C, x, f["lse"], w, softcap=cap)
+    h = 1e-6
+    for M, dM in ((E, dE), (C, dC)):
+        for idx in np.ndindex(*M.shape):
+            old = M[idx]
+            M[idx] = old + h
+            lp = O.forward(E, C, x, reduction="sum", softcap=cap)["loss"]
+            M[idx] = old - h
+            lm = O.forward(E, C, x, reduction="sum", softcap=cap)["loss"]
+            M[idx] = old
+            assert (lp - lm) / (2 * h) == pytest.approx(dM[idx], rel=1e-6, abs=1e-8)
+
+
+def test_softcap_bounds_the_logits(rng):
+    """Every capped logit lies in (-cap, cap), so LSE <= cap + log V."""
+    cap = 2.0
+    E, C, x = _problem(rng, 10, 4, 50, scale=10.0)
+    f = O.forward(E, C, x, reduction="none", softcap=cap)
+    assert np.all(f["lse"] < cap + math.log(50))
+    assert np.all(np.abs(f["target_logit"]) < cap)
