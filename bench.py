@@ -289,8 +289,12 @@ def run_gpu(args, rank, world, local_rank):
 
     # roofline of the dominant GEMM phase, timed live with the library's events
     peaks, peak_src = load_peaks()
-    flops = {"fwd_lse_gemm": 2.0 * N * D * V, "bwd_recompute_g": 2.0 * N * D * V,
-             "bwd_grad_gemm": 4.0 * N * D * V * kept}
+    # Algorithmic work of each GEMM phase: the backward runs over the rows that
+    # take part (ignored rows are compacted away) and, for dC / dE, over the
+    # filter tiles kept.
+    n_part = int((x != W.IGNORE_INDEX).sum())
+    flops = {"fwd_lse_gemm": 2.0 * N * D * V, "bwd_recompute_g": 2.0 * n_part * D * V,
+             "bwd_grad_gemm": 4.0 * n_part * D * V * kept}
     phase_rep = {}
     for name, ms in phases.ms.items():
         n_l = phases.launches[name]
@@ -318,8 +322,11 @@ def run_gpu(args, rank, world, local_rank):
                    "reduction": red, "filter_eps": eps, "ignore_frac": w.ignore_frac,
                    "l2": f"inputs larger than L2 (C is {C.numel() * 2 / 1e6:.0f} MB)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
+        # the pages' metric: 8 N D V over all N tokens, whatever the filter or
+        # the ignored rows save
         "tflops_8NDV": round(total_flops / (agg["ms_per_step"] / 1e3) / 1e12, 1),
         "frac_of_bf16_peak_8NDV": round(total_flops / (agg["ms_per_step"] / 1e3) / 1e12 / peak, 4),
+        "rows_taking_part": n_part,
         "tiles_skipped_frac": round(st["skipped"] / max(st["tiles"], 1), 4),
         "peak_extra_hbm_bytes": int(peak_extra),
         "roofline": roofline, "phases": phase_rep, "e2e": e2e, "gpu_launches": int(launches),

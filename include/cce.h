@@ -122,7 +122,12 @@ cce_status cce_forward(const void* E, const void* C, const int64_t* x, int64_t N
  *                 atomics); vocab rows whose tiles were all skipped are 0.
  *   workspace     >= cce_backward_workspace_bytes(N, D, V) bytes, scratch.
  *   dev_stats     optional device int64[2] (written): {tiles, skipped tiles}
- *                 over the ceil(N/128) x ceil(V/128) filter tiles.
+ *                 over the filter tiles.
+ * Rows that take no part (ignored, or with an out-of-range target) are
+ * compacted away on the device before the GEMMs ("Cut Your Losses ...",
+ * Table A1: removing ignored tokens), so a filter tile is 128 consecutive
+ * participating rows x 128 vocabulary entries, and there are
+ * ceil(n/128) x ceil(V/128) tiles for n participating rows.
  */
 cce_status cce_backward(const void* E, const void* C, const int64_t* x, const float* lse,
                         const float* grad_out, int64_t N, int64_t D, int64_t V, int64_t ignore_index,

@@ -111,14 +111,22 @@ __global__ void finish_loss_kernel(const double* __restrict__ blk_sum, const int
   }
 }
 
-// One block: number of non-ignored rows (mean reduction) and target range check.
-__global__ void count_kernel(const int64_t* __restrict__ x, int N, int V, long long ignore_index, int* count,
-                             int32_t* dev_err) {
-  __shared__ int sc[1024];
+// One block: order-preserving compaction of the rows that take part in the
+// backward (non-ignored, in-range target).  pos[r] = compact index or -1;
+// ridx[k] = original row; *count = number of such rows (the mean's divisor).
+// Out-of-range targets are flagged and dropped like ignored rows.
+constexpr int COMPACT_THREADS = 1024;
+
+__global__ void compact_kernel(const int64_t* __restrict__ x, int N, int V, long long ignore_index,
+                               int* __restrict__ pos, int* __restrict__ ridx, int* count, int32_t* dev_err) {
+  __shared__ int scan[COMPACT_THREADS];
+  const int t = threadIdx.x;
+  const int per = (N + COMPACT_THREADS - 1) / COMPACT_THREADS;
+  const int r0 = min(N, t * per), r1 = min(N, r0 + per);
   int c = 0;
   bool bad = false;
-  for (int i = threadIdx.x; i < N; i += blockDim.x) {
-    const long long xi = static_cast<long long>(x[i]);
+  for (int r = r0; r < r1; ++r) {
+    const long long xi = static_cast<long long>(x[r]);
     if (xi == ignore_index) continue;
     if (xi < 0 || xi >= V) {
       bad = true;
@@ -127,28 +135,72 @@ __global__ void count_kernel(const int64_t* __restrict__ x, int N, int V, long l
     ++c;
   }
   if (bad && dev_err) atomicOr(reinterpret_cast<int*>(dev_err), CCE_DEVERR_TARGET_RANGE);
-  sc[threadIdx.x] = c;
+  scan[t] = c;
   __syncthreads();
-  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
-    if (static_cast<int>(threadIdx.x) < w) sc[threadIdx.x] += sc[threadIdx.x + w];
+  for (int off = 1; off < COMPACT_THREADS; off <<= 1) {  // inclusive scan (Hillis-Steele)
+    const int v = t >= off ? scan[t - off] : 0;
+    __syncthreads();
+    scan[t] += v;
     __syncthreads();
   }
-  if (threadIdx.x == 0) *count = sc[0];
+  int k = scan[t] - c;
+  for (int r = r0; r < r1; ++r) {
+    const long long xi = static_cast<long long>(x[r]);
+    const bool take = xi != ignore_index && xi >= 0 && xi < V;
+    pos[r] = take ? k : -1;
+    if (take) ridx[k++] = r;
+  }
+  if (t == COMPACT_THREADS - 1) *count = scan[t];
 }
 
-// dE (bf16) from the fp32 accumulator; ignored / invalid rows are exactly +0.
-__global__ void finalize_de_kernel(const float4* __restrict__ acc, const int64_t* __restrict__ x, int N, int D,
-                                   int V, long long ignore_index, uint2* __restrict__ dE) {
+// Compact copies of the rows that take part: E_c [k] = E[ridx[k]] and the
+// per-row x, LSE and (reduction none) grad_out.  Rows from the count up to the
+// next multiple of 128 are zero rows with an ignored target, so the last
+// token block of every GEMM sees zeros.  One warp per row, 16-byte copies.
+__global__ void gather_rows_kernel(const uint4* __restrict__ E, const int64_t* __restrict__ x,
+                                   const float* __restrict__ lse, const float* __restrict__ g,
+                                   const int* __restrict__ ridx, const int* __restrict__ count, int N, int D,
+                                   long long ignore_index, uint4* __restrict__ Ec, int64_t* __restrict__ xc,
+                                   float* __restrict__ lsec, float* __restrict__ gc) {
+  const int n = *count;
+  const int nz = min(N, (n + 127) / 128 * 128);
+  const int lane = threadIdx.x & 31;
+  const int per_row = D / 8;  // 16-byte chunks
+  for (int k = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); k < nz; k += gridDim.x * (blockDim.x / 32)) {
+    uint4* dst = Ec + static_cast<size_t>(k) * per_row;
+    if (k < n) {
+      const int r = ridx[k];
+      const uint4* src = E + static_cast<size_t>(r) * per_row;
+      for (int j = lane; j < per_row; j += 32) dst[j] = src[j];
+      if (lane == 0) {
+        xc[k] = x[r];
+        lsec[k] = lse[r];
+        if (gc) gc[k] = g[r];
+      }
+    } else {
+      for (int j = lane; j < per_row; j += 32) dst[j] = make_uint4(0u, 0u, 0u, 0u);
+      if (lane == 0) {
+        xc[k] = ignore_index;
+        lsec[k] = 0.0f;
+        if (gc) gc[k] = 0.0f;
+      }
+    }
+  }
+}
+
+// dE (bf16) from the compact fp32 accumulator, scattered back to the original
+// rows; rows that took no part are exactly +0.
+__global__ void finalize_de_kernel(const float4* __restrict__ acc, const int* __restrict__ pos, int N, int D,
+                                   uint2* __restrict__ dE) {
   const size_t per_row = static_cast<size_t>(D) / 4;
   const size_t total = static_cast<size_t>(N) * per_row;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const size_t row = i / per_row;
-    const long long xi = static_cast<long long>(x[row]);
-    const bool valid = xi != ignore_index && xi >= 0 && xi < V;
+    const int p = pos[row];  // compact row, or -1 for a row that took no part
     uint2 out = make_uint2(0u, 0u);
-    if (valid) {
-      const float4 v = acc[i];
+    if (p >= 0) {
+      const float4 v = acc[static_cast<size_t>(p) * per_row + (i - row * per_row)];
       __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
       __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
       std::memcpy(&out.x, &lo, 4);
@@ -158,8 +210,11 @@ __global__ void finalize_de_kernel(const float4* __restrict__ acc, const int64_t
   }
 }
 
-__global__ void stats_kernel(const uint8_t* __restrict__ bitmap, long long n, int64_t* stats) {
+// Filter statistics over the token blocks of the compact rows.
+__global__ void stats_kernel(const uint8_t* __restrict__ bitmap, const int* __restrict__ count, int bm_ld,
+                             int64_t* stats) {
   __shared__ long long sz[1024];
+  const long long n = static_cast<long long>((*count + 127) / 128) * bm_ld;
   long long z = 0;
   for (long long i = threadIdx.x; i < n; i += blockDim.x) z += bitmap[i] == 0 ? 1 : 0;
   sz[threadIdx.x] = z;
@@ -238,7 +293,7 @@ FwdLayout fwd_layout(int64_t N, int64_t V) {
 }
 
 struct BwdLayout {
-  size_t count, counters, bitmap, bitmapT, gbuf, deacc, total;
+  size_t count, counters, pos, ridx, xc, lsec, gc, ec, bitmap, bitmapT, gbuf, deacc, total;
   int64_t vc, bm_ld, n128, nchunks;
 };
 
@@ -253,6 +308,18 @@ BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V) {
   o = align_up(o + sizeof(int), ALIGN);
   L.counters = o;  // two scheduler counters per chunk
   o = align_up(o + sizeof(int) * 2 * static_cast<size_t>(L.nchunks), ALIGN);
+  L.pos = o;  // compaction map and compact copies of the rows that take part
+  o = align_up(o + sizeof(int) * static_cast<size_t>(N), ALIGN);
+  L.ridx = o;
+  o = align_up(o + sizeof(int) * static_cast<size_t>(N), ALIGN);
+  L.xc = o;
+  o = align_up(o + sizeof(int64_t) * static_cast<size_t>(N), ALIGN);
+  L.lsec = o;
+  o = align_up(o + sizeof(float) * static_cast<size_t>(N), ALIGN);
+  L.gc = o;
+  o = align_up(o + sizeof(float) * static_cast<size_t>(N), ALIGN);
+  L.ec = o;
+  o = align_up(o + static_cast<size_t>(N) * D * 2, ALIGN);
   L.bitmap = o;
   o = align_up(o + static_cast<size_t>(L.n128 * L.bm_ld), ALIGN);
   L.bitmapT = o;
@@ -564,10 +631,25 @@ cce_status cce_backward_ex(const void* E, const void* C, const int64_t* x, const
   void* gbuf = ws + W.gbuf;
   float* deacc = reinterpret_cast<float*>(ws + W.deacc);
 
+  // Compact away the rows that take no part ("Cut Your Losses ...", Table A1:
+  // removing ignored tokens); the GEMMs below read the count from the device.
+  int* pos = reinterpret_cast<int*>(ws + W.pos);
+  int* ridx = reinterpret_cast<int*>(ws + W.ridx);
+  int64_t* xc = reinterpret_cast<int64_t*>(ws + W.xc);
+  float* lsec = reinterpret_cast<float*>(ws + W.lsec);
+  float* gc = reinterpret_cast<float*>(ws + W.gc);
+  void* Ec = ws + W.ec;
   {
     PhaseScope ps(2, s);
-    count_kernel<<<1, 1024, 0, s>>>(x, static_cast<int>(N), static_cast<int>(V), static_cast<long long>(ignore_index),
-                                    count, dev_err);
+    compact_kernel<<<1, COMPACT_THREADS, 0, s>>>(x, static_cast<int>(N), static_cast<int>(V),
+                                                 static_cast<long long>(ignore_index), pos, ridx, count, dev_err);
+    g_launches++;
+    const int rows_per_block = 8;
+    const int blocks = static_cast<int>(std::min<int64_t>(int64_t(sms) * 16, cdiv(N, rows_per_block)));
+    gather_rows_kernel<<<std::max(blocks, 1), 32 * rows_per_block, 0, s>>>(
+        static_cast<const uint4*>(E), x, lse, grad_out, ridx, count, static_cast<int>(N), static_cast<int>(D),
+        static_cast<long long>(ignore_index), static_cast<uint4*>(Ec), xc, lsec,
+        reduction == CCE_RED_NONE ? gc : nullptr);
     g_launches++;
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_status(e);
@@ -579,16 +661,16 @@ cce_status cce_backward_ex(const void* E, const void* C, const int64_t* x, const
   std::memset(&r, 0, sizeof(r));
   const uint64_t vc = static_cast<uint64_t>(W.vc);
   bool ok = true;
-  ok &= make_tmap(&g.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, E, D, N, D, BK, BM);
+  ok &= make_tmap(&g.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Ec, D, N, D, BK, BM);
   ok &= make_tmap(&g.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, D, V, D, BK, BN);
   ok &= make_tmap(&g.tmOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, gbuf, vc, N, vc, 64, 32);
   r.b3d = (D % 64 == 0) ? 1 : 0;
   ok &= make_tmap_mn3(&r.tmA, gbuf, vc, N, BM / 64);  // G chunk, MN-major A of dC (vc % 256 == 0)
   if (r.b3d) {
-    ok &= make_tmap_mn3(&r.tmB, E, D, N);
+    ok &= make_tmap_mn3(&r.tmB, Ec, D, N);
     ok &= make_tmap_mn3(&r.tmB2, C, D, V);
   } else {
-    ok &= make_tmap(&r.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, E, D, N, D, 64, 64);
+    ok &= make_tmap(&r.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Ec, D, N, D, 64, 64);
     ok &= make_tmap(&r.tmB2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, D, V, D, 64, 64);
   }
   ok &= make_tmap(&r.tmOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dC, D, V, D, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
@@ -601,11 +683,12 @@ cce_status cce_backward_ex(const void* E, const void* C, const int64_t* x, const
     p->D = static_cast<int>(D);
     p->V = static_cast<int>(V);
     p->n_blocks = static_cast<int>(cdiv(N, BM));
-    p->x = x;
+    p->x = xc;  // every per-row input in compact order
     p->ignore_index = ignore_index;
-    p->lse = lse;
-    p->grad_out = grad_out;
+    p->lse = lsec;
+    p->grad_out = reduction == CCE_RED_NONE ? gc : grad_out;
     p->count = count;
+    p->n_dev = count;
     p->reduction = reduction;
     p->eps = filter_eps;
     p->softcap = softcap;
@@ -623,7 +706,6 @@ cce_status cce_backward_ex(const void* E, const void* C, const int64_t* x, const
       1, std::min<int64_t>(cdiv(N, BM), std::max<int64_t>(8, (int64_t(32) << 20) / (BM * 2 * D)))));
   r.bn = grad_tile_width(D, r.b3d ? 64 : 32);
   r.n_tiles = static_cast<int>(cdiv(D, r.bn));
-  r.dc_k_blocks = static_cast<int>(cdiv(N, BK));
 
   int* counters = reinterpret_cast<int*>(ws + W.counters);
   {
@@ -638,24 +720,22 @@ cce_status cce_backward_ex(const void* E, const void* C, const int64_t* x, const
       p->chunk_w = w;
     }
     g.v_tiles = static_cast<int>(cdiv(w, BN));
-    g.items = g.n_blocks * g.v_tiles;
     g.counter = counters + 2 * ch;
     r.dc_m_tiles = static_cast<int>(cdiv(w, BM));
     r.de_k_blocks = static_cast<int>(cdiv(w, BK));
-    r.dc_first = r.dc_k_blocks >= r.de_k_blocks ? 1 : 0;  // longest tiles first
+    r.dc_first = cdiv(N, BK) >= r.de_k_blocks ? 1 : 0;  // longest tiles first
     r.first_chunk = (ch == 0) ? 1 : 0;
-    r.items = (r.dc_m_tiles + r.n_blocks) * r.n_tiles;
     r.counter = counters + 2 * ch + 1;
     cudaError_t e;
     {
       PhaseScope ps(3, s);
-      e = launch_gemm(MODE_BWD_G, g, std::min(sms, g.items), s);
+      e = launch_gemm(MODE_BWD_G, g, std::min(sms, g.n_blocks * g.v_tiles), s);
       g_launches++;
       if (e != cudaSuccess) return cuda_status(e);
     }
     {
       PhaseScope ps(4, s);
-      e = launch_gemm(MODE_GRAD, r, std::min(sms, r.items), s);
+      e = launch_gemm(MODE_GRAD, r, std::min(sms, (r.dc_m_tiles + r.n_blocks) * r.n_tiles), s);
       g_launches++;
       if (e != cudaSuccess) return cuda_status(e);
     }
@@ -664,13 +744,12 @@ cce_status cce_backward_ex(const void* E, const void* C, const int64_t* x, const
     PhaseScope ps(5, s);
     const size_t n4 = static_cast<size_t>(N) * D / 4;
     const int blocks = static_cast<int>(std::min<size_t>(static_cast<size_t>(sms) * 8, (n4 + 255) / 256));
-    finalize_de_kernel<<<std::max(blocks, 1), 256, 0, s>>>(reinterpret_cast<const float4*>(deacc), x,
+    finalize_de_kernel<<<std::max(blocks, 1), 256, 0, s>>>(reinterpret_cast<const float4*>(deacc), pos,
                                                            static_cast<int>(N), static_cast<int>(D),
-                                                           static_cast<int>(V), static_cast<long long>(ignore_index),
                                                            static_cast<uint2*>(dE));
     g_launches++;
     if (dev_stats) {
-      stats_kernel<<<1, 1024, 0, s>>>(bitmap, static_cast<long long>(W.n128 * W.bm_ld), dev_stats);
+      stats_kernel<<<1, 1024, 0, s>>>(bitmap, count, static_cast<int>(W.bm_ld), dev_stats);
       g_launches++;
     }
     cudaError_t e = cudaGetLastError();

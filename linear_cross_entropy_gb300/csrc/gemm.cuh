@@ -53,9 +53,33 @@ struct Tile {
   bool first, last;  // FWD: first / last tile of a (row block, split) unit
 };
 
+// Work sizes that depend on the device-side row count (BWD_G / GRAD run over
+// the compacted rows).  Every role computes them from the same value.
+struct Dims {
+  int nb;     // token blocks of 128 taking part
+  int dc_kb;  // K-blocks of the dC contraction (tokens / 64)
+  int items;  // work items of the launch
+};
+
+template <int MODE>
+__device__ __forceinline__ Dims dims_of(const GemmArgs& a) {
+  const int n = a.n_dev ? *a.n_dev : a.N;
+  Dims d;
+  d.nb = (n + BM - 1) / BM;
+  d.dc_kb = (n + BK - 1) / BK;
+  if constexpr (MODE == MODE_FWD) {
+    d.items = a.items;
+  } else if constexpr (MODE == MODE_BWD_G) {
+    d.items = d.nb * a.v_tiles;
+  } else {
+    d.items = (a.dc_m_tiles + d.nb) * a.n_tiles;
+  }
+  return d;
+}
+
 // Calls f(tile) for every tile of work item `item`; false if f asked to stop.
 template <int MODE, typename F>
-__device__ __forceinline__ bool for_each_tile_of_item(const GemmArgs& a, int item, F&& f) {
+__device__ __forceinline__ bool for_each_tile_of_item(const GemmArgs& a, const Dims& dm, int item, F&& f) {
   if constexpr (MODE == MODE_FWD) {
     const int m = item % a.n_blocks, s = item / a.n_blocks;
     const int t0 = static_cast<int>(static_cast<long long>(s) * a.v_tiles / a.splits);
@@ -70,11 +94,11 @@ __device__ __forceinline__ bool for_each_tile_of_item(const GemmArgs& a, int ite
     // the same time share a few C tiles and a group's E rows stay in L2.
     const int per_group = a.group_n * a.v_tiles;
     const int g = item / per_group, j = item - g * per_group;
-    const int gn = min(a.group_n, a.n_blocks - g * a.group_n);
+    const int gn = min(a.group_n, dm.nb - g * a.group_n);
     return f(Tile{KIND_MAIN, g * a.group_n + j % gn, j / gn, 0, true, true});
   } else {
     const int dc_tiles = a.dc_m_tiles * a.n_tiles;
-    const int de_tiles = a.n_blocks * a.n_tiles;
+    const int de_tiles = dm.nb * a.n_tiles;
     int i = item, kind;
     if (a.dc_first) {
       kind = i < dc_tiles ? KIND_DC : KIND_DE;
@@ -89,8 +113,8 @@ __device__ __forceinline__ bool for_each_tile_of_item(const GemmArgs& a, int ite
 }
 
 template <int MODE>
-__device__ __forceinline__ int kblocks_of(const GemmArgs& a, const Tile& t) {
-  if constexpr (MODE == MODE_GRAD) return t.kind == KIND_DC ? a.dc_k_blocks : a.de_k_blocks;
+__device__ __forceinline__ int kblocks_of(const GemmArgs& a, const Dims& dm, const Tile& t) {
+  if constexpr (MODE == MODE_GRAD) return t.kind == KIND_DC ? dm.dc_kb : a.de_k_blocks;
   return a.k_blocks;
 }
 
@@ -110,12 +134,12 @@ __device__ __forceinline__ bool kblock_skipped(const GemmArgs& a, const Tile& t,
 }
 
 // Warp-wide: does the output tile have no surviving K-block at all?
-__device__ __forceinline__ bool tile_empty(const GemmArgs& a, const Tile& t) {
+__device__ __forceinline__ bool tile_empty(const GemmArgs& a, const Dims& dm, const Tile& t) {
   if (!(t.kind == KIND_DC ? a.filter_dc : a.filter_de)) return false;  // this output is not filtered
   int any = 0;
   if (t.kind == KIND_DC) {
     const uint8_t* row = a.bitmapT + static_cast<size_t>((a.chunk_v0 >> 7) + t.m) * a.n_blocks;
-    for (int r = lane_id(); r < a.n_blocks; r += 32) any |= __ldg(row + r);
+    for (int r = lane_id(); r < dm.nb; r += 32) any |= __ldg(row + r);
   } else {
     const int ncols = (a.chunk_w + FILTER_TILE - 1) / FILTER_TILE;
     const uint8_t* row = a.bitmap + static_cast<size_t>(t.m) * a.bm_ld + (a.chunk_v0 >> 7);
@@ -197,17 +221,18 @@ __device__ __forceinline__ void producer_loop(const GemmArgs& a, const SmemLayou
   int stage = 0;
   uint32_t phase = 0;
   uint32_t issued_mask = 0, issued_par = 0;  // per stage: ever issued, parity of last issue
+  const Dims dm = dims_of<MODE>(a);
   for (int k = 0;; ++k) {
     const int slot = k % RING;
     if (!wait_bounded(&L.ring_empty[slot], static_cast<uint32_t>(((k / RING) & 1) ^ 1), abort_flag, a.dev_err))
       break;
     int item = atomicAdd(a.counter, 1);
-    if (item >= a.items) item = -1;
+    if (item >= dm.items) item = -1;
     L.ring_ids[slot] = item;
     mbar_arrive(&L.ring_full[slot]);  // release: the id is visible to the waiting consumers
     if (item < 0) break;
-    const bool ok = for_each_tile_of_item<MODE>(a, item, [&](const Tile& t) -> bool {
-      const int nk = kblocks_of<MODE>(a, t);
+    const bool ok = for_each_tile_of_item<MODE>(a, dm, item, [&](const Tile& t) -> bool {
+      const int nk = kblocks_of<MODE>(a, dm, t);
       for (int kb = 0; kb < nk; ++kb) {
         if (kblock_skipped<MODE>(a, t, kb)) continue;
         if (!wait_bounded(&L.empty[stage], phase ^ 1u, abort_flag, a.dev_err)) return false;
@@ -266,10 +291,11 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& a, const SmemLayout& L,
   int acc = 0;
   uint32_t acc_phase = 0;
   bool issued_any = false;
+  const Dims dm = dims_of<MODE>(a);
   for (int k = 0;; ++k) {
     const int item = ring_take(L, k, a);
     if (item < 0) break;
-    const bool ok = for_each_tile_of_item<MODE>(a, item, [&](const Tile& t) -> bool {
+    const bool ok = for_each_tile_of_item<MODE>(a, dm, item, [&](const Tile& t) -> bool {
       // Operand majorness and tile width of this tile.
       const bool a_mn = (MODE == MODE_GRAD) && t.kind == KIND_DC;
       const bool b_mn = (MODE == MODE_GRAD);
@@ -281,7 +307,7 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& a, const SmemLayout& L,
       if (!wait_bounded(&L.tmem_empty[acc], acc_phase ^ 1u, abort_flag, a.dev_err)) return false;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-      const int nk = kblocks_of<MODE>(a, t);
+      const int nk = kblocks_of<MODE>(a, dm, t);
       bool any = false;
       for (int kb = 0; kb < nk; ++kb) {
         if (kblock_skipped<MODE>(a, t, kb)) continue;
@@ -560,9 +586,10 @@ __device__ __forceinline__ bool epi_bwd_g(const GemmArgs& a, const SmemLayout& L
 
 // GRAD, KIND_DC: bf16 output tile, rows = vocabulary (chunk_v0 + 128m ...),
 // cols = D tile of width bn, stored in 32-column boxes (64-byte swizzle).
-__device__ __forceinline__ void epi_dc(const GemmArgs& a, const SmemLayout& L, const Tile& t, int acc, EpiCtx& e) {
+__device__ __forceinline__ void epi_dc(const GemmArgs& a, const Dims& dm, const SmemLayout& L, const Tile& t,
+                                       int acc, EpiCtx& e) {
   const uint32_t lane = lane_id();
-  const bool empty = tile_empty(a, t);
+  const bool empty = tile_empty(a, dm, t);
   const uint32_t tbase = e.taddr + static_cast<uint32_t>(acc * BN);
   const int gy = a.chunk_v0 + t.m * BM + e.q * 32;
   const int x0 = t.n * a.bn;
@@ -602,9 +629,10 @@ __device__ __forceinline__ void epi_dc(const GemmArgs& a, const SmemLayout& L, c
 
 // GRAD, KIND_DE: fp32 output tile, rows = tokens, cols = D tile; store (first
 // chunk) or reduce-add, in 32-column boxes (128-byte swizzle).
-__device__ __forceinline__ void epi_de(const GemmArgs& a, const SmemLayout& L, const Tile& t, int acc, EpiCtx& e) {
+__device__ __forceinline__ void epi_de(const GemmArgs& a, const Dims& dm, const SmemLayout& L, const Tile& t,
+                                       int acc, EpiCtx& e) {
   const uint32_t lane = lane_id();
-  const bool empty = tile_empty(a, t);
+  const bool empty = tile_empty(a, dm, t);
   if (empty && !a.first_chunk) {  // adding zero: nothing to do
     release_tmem(L, acc);
     return;
@@ -657,12 +685,13 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& a, const SmemLayou
   FwdState st{NEG_BIG, 0.0f};
   int acc = 0;
   uint32_t acc_phase = 0;
+  const Dims dm = dims_of<MODE>(a);
   for (int k = 0;; ++k) {
     int item = 0;
     if (lane_id() == 0) item = ring_take(L, k, a);
     item = __shfl_sync(0xffffffffu, item, 0);
     if (item < 0) break;
-    const bool ok = for_each_tile_of_item<MODE>(a, item, [&](const Tile& t) -> bool {
+    const bool ok = for_each_tile_of_item<MODE>(a, dm, item, [&](const Tile& t) -> bool {
       if (!warp_wait_bounded(&L.tmem_full[acc], acc_phase, L.abort_flag, a.dev_err)) return false;
       tc_fence_after();
       bool r = true;
@@ -672,9 +701,9 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& a, const SmemLayou
         r = epi_bwd_g<CAP>(a, L, t, acc, e);
       } else {
         if (t.kind == KIND_DC) {
-          epi_dc(a, L, t, acc, e);
+          epi_dc(a, dm, L, t, acc, e);
         } else {
-          epi_de(a, L, t, acc, e);
+          epi_de(a, dm, L, t, acc, e);
         }
       }
       ++e.iter;

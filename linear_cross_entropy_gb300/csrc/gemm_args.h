@@ -60,7 +60,11 @@ struct GemmArgs {
   int first_chunk;  // dE: store (1) or reduce-add (0)
   // dynamic scheduling: work items are handed out by atomicAdd on *counter
   int* counter;     // zeroed before the launch
-  int items;
+  int items;        // FWD: work items (BWD_G / GRAD derive theirs from the row count)
+  // BWD_G / GRAD: device-side number of token rows taking part (the backward
+  // compacts away ignored rows on the device); N and n_blocks above are the
+  // allocated upper bounds.  Null: all N rows.
+  const int* n_dev;
   const int64_t* x;
   long long ignore_index;
   float* part_m;  // FWD: [splits][N] running max (log2 units)

@@ -249,12 +249,26 @@ def tile_keep(G, BN, BV, eps=FILTER_EPS):
 
 
 def backward_filtered(E, C, x, lse, w, BN, BV, eps=FILTER_EPS, ignore_index=IGNORE_INDEX,
-                      filter_dE=True, filter_dC=True, softcap=0.0):
+                      filter_dE=True, filter_dC=True, softcap=0.0, compact_ignored=False):
     """dE, dC with the contributions of skipped tiles removed from the
     outputs whose filter is on; also returns the survival map.  With eps = 0
     no tile is skipped.  filter_dE only ("Cut Your Losses ...", "Numerical
     Stability Variants": CCE-Kahan-FullC computes dC from every tile) and
-    filter_dC only (CCE-Kahan-FullE)."""
+    filter_dC only (CCE-Kahan-FullE).
+
+    compact_ignored: remove the ignored rows first ("Cut Your Losses ...",
+    Table A1: removing ignored tokens), so the BN-row tiles are made of
+    consecutive non-ignored rows; dE rows are returned in the original order
+    (ignored rows 0) and the survival map is over the compact rows."""
+    if compact_ignored:
+        x = np.asarray(x, np.int64)
+        keep_rows = np.nonzero(x != ignore_index)[0]
+        dEc, dC, keep = backward_filtered(np.asarray(E)[keep_rows], C, x[keep_rows], np.asarray(lse)[keep_rows],
+                                          np.asarray(w)[keep_rows], BN, BV, eps, ignore_index, filter_dE,
+                                          filter_dC, softcap, False)
+        dE = np.zeros((x.shape[0], dEc.shape[1]))
+        dE[keep_rows] = dEc
+        return dE, dC, keep
     E = np.asarray(E, np.float64)
     C = np.asarray(C, np.float64)
     A = logits(E, C)

@@ -61,7 +61,8 @@ def oracle_full(E_bits, C_bits, x, ignore_index=-100, reduction="mean", grad_out
     dE, dC = O.backward(E, C, x, f["lse"], w, ignore_index)
     out = {"loss": f["loss"], "lse": f["lse"], "loss_rows": f["loss_rows"], "dE": dE, "dC": dC}
     if filter_eps:
-        dEf, dCf, keep = O.backward_filtered(E, C, x, f["lse"], w, tile[0], tile[1], filter_eps, ignore_index)
+        dEf, dCf, keep = O.backward_filtered(E, C, x, f["lse"], w, tile[0], tile[1], filter_eps, ignore_index,
+                                             compact_ignored=True)
         out.update(dE_f=dEf, dC_f=dCf, keep=keep)
     return out
 

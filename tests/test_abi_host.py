@@ -70,7 +70,8 @@ def test_workspace_queries(lib, N, D, V):
     if V > 256:
         assert r["bwd_chunk_cols"] < V
     assert N * r["bwd_chunk_cols"] * 2 <= max(512 << 20, N * 256 * 2)
-    assert b <= N * D * 4 + N * r["bwd_chunk_cols"] * 2 + 2 * (N // 128 + 1) * (V // 128 + 1) + 4096
+    compaction = N * (4 + 4 + 8 + 4 + 4) + N * D * 2  # row map + compact x, LSE, grad_out and E
+    assert b <= N * D * 4 + N * r["bwd_chunk_cols"] * 2 + 2 * (N // 128 + 1) * (V // 128 + 1) + compaction + 8192
     assert f < N * V * 4 or V < 1024
 
 

@@ -202,7 +202,7 @@ def test_per_output_filter_flags(outputs, fde, fdc):
     f = O.forward(Ef, Cf, x, reduction="mean")
     w = O.row_weights(x, -100, "mean", 1.0, f["count"])
     rE, rC, keep = O.backward_filtered(Ef, Cf, x, f["lse"], w, 128, 128, O.FILTER_EPS, filter_dE=fde,
-                                       filter_dC=fdc)
+                                       filter_dC=fdc, compact_ignored=True)
     assert rel_fro(bf16_to_f64(dE), rE) <= TOL_GRAD
     assert rel_fro(bf16_to_f64(dC), rC) <= TOL_GRAD
     assert st["skipped"] == int((~keep).sum()) > 0
@@ -231,3 +231,20 @@ def test_softcap_against_oracle(filter_on):
     tol = TOL_GRAD_FILTERED if filter_on else TOL_GRAD
     assert rel_fro(bf16_to_f64(dE), rE) <= tol
     assert rel_fro(bf16_to_f64(dC), rC) <= tol
+
+
+def test_mostly_ignored_batch_is_compacted():
+    """70% of the rows ignored: the backward runs on the compacted rows and
+    matches the oracle (unfiltered and filtered); ignored rows stay exact zeros."""
+    import linear_cross_entropy_gb300 as cce
+    from tests.gpu_util import to_device, bf16_to_f64
+    w, (E, C, x) = make(W.small("k", 900, 128, 5000, ignore_frac=0.7, reduction="sum"))
+    assert (x == -100).mean() > 0.6
+    for eps in (0.0, O.FILTER_EPS):
+        got = run_cuda(E, C, x, reduction="sum", filter_eps=eps)
+        ref = oracle_full(E, C, x, reduction="sum", filter_eps=eps or None)
+        assert_forward_close(got, ref, "sum", x)
+        assert_grads_close(got, ref["dE"], ref["dC"], TOL_GRAD if eps == 0 else TOL_GRAD_FILTERED, x)
+        if eps:
+            assert rel_fro(got["dE"], ref["dE_f"]) <= TOL_GRAD
+            assert got["stats"]["tiles"] == ref["keep"].size

@@ -462,3 +462,20 @@ def test_softcap_bounds_the_logits(rng):
     f = O.forward(E, C, x, reduction="none", softcap=cap)
     assert np.all(f["lse"] < cap + math.log(50))
     assert np.all(np.abs(f["target_logit"]) < cap)
+
+
+def test_compacting_ignored_rows_changes_only_the_tiling(rng):
+    """Unfiltered, removing ignored rows first changes nothing; filtered, it
+    equals the filtered backward of the batch without those rows."""
+    E, C, x = _problem(rng, 200, 16, 700, scale=3.0, ignore=tuple(range(0, 200, 3)))
+    f = O.forward(E, C, x, reduction="mean")
+    w = O.row_weights(x, -100, "mean", 1.0, f["count"])
+    dE, dC = O.backward(E, C, x, f["lse"], w)
+    a_dE, a_dC, _ = O.backward_filtered(E, C, x, f["lse"], w, 16, 16, eps=0.0, compact_ignored=True)
+    assert np.allclose(a_dE, dE, rtol=1e-13, atol=1e-16) and np.allclose(a_dC, dC, rtol=1e-13, atol=1e-16)
+    keep_rows = np.nonzero(x != -100)[0]
+    b_dE, b_dC, keep = O.backward_filtered(E, C, x, f["lse"], w, 16, 16, eps=1e-3, compact_ignored=True)
+    c_dE, c_dC, keep_c = O.backward_filtered(E[keep_rows], C, x[keep_rows], f["lse"][keep_rows], w[keep_rows],
+                                             16, 16, eps=1e-3)
+    assert np.array_equal(keep, keep_c) and np.array_equal(b_dC, c_dC)
+    assert np.array_equal(b_dE[keep_rows], c_dE) and np.all(b_dE[x == -100] == 0.0)
