@@ -281,12 +281,24 @@ def small(name: str, N: int, D: int, V: int, **kw) -> Workload:
 
 
 def frequent_token_inputs(N: int, D: int, V: int, n_freq: int = 256, seed: int = 0,
-                          ignore_frac: float = 0.05):
+                          ignore_frac: float = 0.05, scatter: bool = False, unigram: float = 0.0):
     """A supplementary workload where the gradient filter bites: the n_freq
     lowest ids are "frequent tokens" with large classifier rows (as byte-pair
     merge order puts frequent tokens at low ids), every other row is small,
     and targets are drawn uniformly among the frequent ids.  Softmax mass then
     sits in the first n_freq columns, so most 128 x 128 tiles are skippable.
+
+    unigram > 0: every hidden state gets a common component 4 u along a fixed
+    random unit direction u and every frequent row gets (unigram / 4) u, so
+    the frequent tokens' logits are raised by about `unigram` on every row --
+    the shared "frequent token" bias of a trained head, which makes the
+    average logit a useful sort key.
+    scatter: token ids are relabelled by a seeded random permutation of
+    [0, V), so the frequent tokens are spread over the whole vocabulary (an
+    arbitrary vocabulary order; "Cut Cross-Entropy: Training Loss Without the
+    Logit Matrix ...", section "Gradient filtering: the part that makes it
+    fast", measures the filter under a random vocabulary permutation).
+    Defaults reproduce the original draw bit for bit.
     Returns (E_bits, C_bits, x)."""
     g = _gen(seed, 7)
     big = normal_bf16(seed, 8, n_freq * D, 6.0 / math.sqrt(D))
@@ -294,6 +306,29 @@ def frequent_token_inputs(N: int, D: int, V: int, n_freq: int = 256, seed: int =
     C_bits = np.concatenate([big, small]).reshape(V, D)
     E_bits = normal_bf16(seed, 10, N * D, 1.0).reshape(N, D)
     x = g.integers(0, n_freq, size=N, dtype=np.int64)
+    if unigram > 0.0:
+        u = normal_f64(seed, 12, D)
+        sq = 0.0
+        for d in range(D):
+            sq += u[d] * u[d]
+        u = u / math.sqrt(sq)
+        E = bf16_bits_to_f32(E_bits).astype(np.float64) + 4.0 * u[None, :]
+        E_bits = f32_to_bf16_bits(E.astype(np.float32))
+        Cf = bf16_bits_to_f32(C_bits[:n_freq]).astype(np.float64) + (unigram / 4.0) * u[None, :]
+        C_bits[:n_freq] = f32_to_bf16_bits(Cf.astype(np.float32))
+    if scatter:
+        perm = _gen(seed, 13).permutation(V)  # natural id j -> token id perm[j]
+        C_s = np.empty_like(C_bits)
+        C_s[perm] = C_bits
+        C_bits = C_s
+        x = perm[x].astype(np.int64)
     u = _uniform_open(_gen(seed, 11), N)
     x = np.where(u < ignore_frac, np.int64(IGNORE_INDEX), x)
     return E_bits, C_bits, x
+
+
+# A supplementary benchmark workload (not one of the five above): the
+# Qwen2.5-0.5B head shape with softmax mass on 256 frequent tokens that a
+# random vocabulary order scatters; the case vocabulary sorting is for.
+FREQ_SCATTERED = dict(N=4096, D=896, V=151936, n_freq=256, seed=0, ignore_frac=0.05, scatter=True,
+                      unigram=8.0)

@@ -37,6 +37,12 @@ Passages followed (page title, section):
   with cap > 0 the logits are a'_iv = cap tanh(a_iv / cap); LSE, loss and
   G = softmax(a') - onehot use a', and the gradient reaching E and C is
   G (1 - tanh^2(a / cap)).  The filter tests |G| before that factor.
+* Vocabulary sorting ("Cut Your Losses ...", section "Vocabulary Sorting"):
+  the vocabulary is reordered by each token's average logit over the batch
+  so that tokens with large softmax values share tiles; the filter then
+  works on tiles of consecutive sorted positions.  The order (ascending,
+  equal keys by token id) follows the argsort the first page names.  Sorting
+  changes which tiles exist, never the unfiltered result.
 * Reading where the pages are silent: mean divides by the number of
   non-ignored rows, clamped to at least 1 (the chunked-CE code on the
   "fused-linear-cross-entropy" page clamps the count the same way); the LSE of
@@ -50,7 +56,10 @@ Pins (tests/test_oracle_pins.py): closed forms (C = 0 gives loss = log V;
 N = 1, V = 2 gives a softplus), central finite differences of the loss for dE
 and dC, torch.nn.functional.cross_entropy on materialised fp64 logits,
 row sums of G equal to zero, vocabulary-permutation invariance, the
-pigeonhole bound on entries >= 2^-12 and the eps tie case.  Every function
+pigeonhole bound on entries >= 2^-12 and the eps tie case; for sorting, the
+logit sums by brute-force loops and by the linearity C (sum_i E_i), the order
+by brute-force rank counting and a hand-sorted example, and the sorted
+filtered backward by its independence of the input vocabulary order.  Every function
 below is pinned by at least one of them.
 """
 from __future__ import annotations
@@ -249,7 +258,7 @@ def tile_keep(G, BN, BV, eps=FILTER_EPS):
 
 
 def backward_filtered(E, C, x, lse, w, BN, BV, eps=FILTER_EPS, ignore_index=IGNORE_INDEX,
-                      filter_dE=True, filter_dC=True, softcap=0.0, compact_ignored=False):
+                      filter_dE=True, filter_dC=True, softcap=0.0, compact_ignored=False, vocab_perm=None):
     """dE, dC with the contributions of skipped tiles removed from the
     outputs whose filter is on; also returns the survival map.  With eps = 0
     no tile is skipped.  filter_dE only ("Cut Your Losses ...", "Numerical
@@ -259,7 +268,29 @@ def backward_filtered(E, C, x, lse, w, BN, BV, eps=FILTER_EPS, ignore_index=IGNO
     compact_ignored: remove the ignored rows first ("Cut Your Losses ...",
     Table A1: removing ignored tokens), so the BN-row tiles are made of
     consecutive non-ignored rows; dE rows are returned in the original order
-    (ignored rows 0) and the survival map is over the compact rows."""
+    (ignored rows 0) and the survival map is over the compact rows.
+
+    vocab_perm: the vocabulary in sorted order (vocab_perm[j] = the token at
+    position j; "Cut Your Losses ...", section "Vocabulary Sorting").  The
+    BV-column tiles are then made of consecutive sorted positions: the
+    problem is solved on C[vocab_perm] with each target replaced by its
+    sorted position, and the rows of dC are put back in token order.  The
+    survival map is over sorted positions."""
+    if vocab_perm is not None:
+        p = np.asarray(vocab_perm, np.int64)
+        V = p.shape[0]
+        inv = np.empty(V, np.int64)
+        inv[p] = np.arange(V)
+        x = np.asarray(x, np.int64)
+        take = (x != ignore_index) & (x >= 0) & (x < V)
+        # rows that take part get their target's sorted position; the rest get
+        # -1, outside [0, V), and -1 becomes the ignore index of the sub-call
+        xs = np.where(take, inv[np.where(take, x, 0)], -1)
+        dE, dCs, keep = backward_filtered(E, np.asarray(C)[p], xs, lse, w, BN, BV, eps, -1, filter_dE,
+                                          filter_dC, softcap, compact_ignored, None)
+        dC = np.empty_like(dCs)
+        dC[p] = dCs
+        return dE, dC, keep
     if compact_ignored:
         x = np.asarray(x, np.int64)
         keep_rows = np.nonzero(x != ignore_index)[0]
@@ -278,6 +309,33 @@ def backward_filtered(E, C, x, lse, w, BN, BV, eps=FILTER_EPS, ignore_index=IGNO
     Gw = np.asarray(w)[:, None] * G * softcap_slope(A, softcap)
     Gf = np.where(mask, Gw, 0.0)
     return (Gf if filter_dE else Gw) @ C, (Gf if filter_dC else Gw).T @ E, keep
+
+
+def vocab_logit_sums(E, C, x, ignore_index=IGNORE_INDEX):
+    """The statistic vocabulary sorting orders by ("Cut Your Losses ...",
+    section "Vocabulary Sorting"): for every token v, the sum over the rows
+    that take part of the logit a_iv = C_v . E_i, and the number of those rows
+    (the average logit is sum / count, so both order the vocabulary alike).
+    A row takes part when its target is in [0, V) and is not ignore_index.
+    Returns (sums [V] float64, count)."""
+    E = np.asarray(E, np.float64)
+    C = np.asarray(C, np.float64)
+    x = np.asarray(x, np.int64)
+    V = C.shape[0]
+    rows = np.nonzero((x != ignore_index) & (x >= 0) & (x < V))[0]
+    S = np.zeros(V)
+    for r0, r1 in _row_blocks(len(rows), V):
+        S += logits(E[rows[r0:r1]], C).sum(axis=0)
+    return S, int(len(rows))
+
+
+def vocab_order(keys):
+    """The sorted vocabulary: perm[j] is the token at position j, with the keys
+    in ascending order ("Cut Cross-Entropy: Training Loss Without the Logit
+    Matrix ...", section "Gradient filtering: the part that makes it fast",
+    sorts with an ascending argsort of the average logit) and equal keys in
+    increasing token id (a stable sort; -0.0 equals +0.0)."""
+    return np.argsort(np.asarray(keys, np.float64), kind="stable")
 
 
 def from_bits(E_bits, C_bits):
