@@ -1,7 +1,7 @@
 """Benchmark of the Cut Cross-Entropy hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                    [--config qwen] [--filter on|off]
+                    [--config qwen] [--filter on|off] [--vocab-sort]
 
 One step = cce_forward + cce_backward (every stage of the path: LSE GEMM with
 target capture, combine + reduction, target count, recompute + G + filter,
@@ -44,6 +44,7 @@ SOURCE_FILES = ("linear_cross_entropy_gb300/csrc/gemm.cuh", "linear_cross_entrop
 WORKLOAD_NAMES = {
     "tiny": "tiny CCE head", "qwen": "Qwen2.5-0.5B-shaped head", "gemma": "Gemma-2-2B-shaped head",
     "llama": "Llama-3-8B-shaped head", "long": "long-context filter stress",
+    "freq": "Qwen2.5-0.5B-shaped head, frequent tokens scattered",
 }
 
 
@@ -194,8 +195,9 @@ def run_gpu(args, rank, world, local_rank):
         import torch.distributed as dist
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    w = W.CONFIGS[args.config]
+    w = W.ALL_CONFIGS[args.config]
     eps = W_FILTER_EPS if args.filter == "on" else 0.0
+    sort = bool(args.vocab_sort)
     E_bits, C_bits, x = W.make_inputs(w)
     N, D, V = w.N, w.D, w.V
     E = torch.from_numpy(E_bits.view(np.int16)).to(dev).view(torch.bfloat16)
@@ -204,7 +206,7 @@ def run_gpu(args, rank, world, local_rank):
     red = w.reduction
     g = torch.ones(N if red == "none" else 1, dtype=torch.float32, device=dev)
     ws_f = torch.empty(cce.forward_workspace_bytes(N, D, V), dtype=torch.uint8, device=dev)
-    ws_b = torch.empty(cce.backward_workspace_bytes(N, D, V), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(cce.backward_workspace_bytes(N, D, V, vocab_sort=sort), dtype=torch.uint8, device=dev)
     dE = torch.empty_like(E)
     dC = torch.empty_like(C)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -213,7 +215,7 @@ def run_gpu(args, rank, world, local_rank):
     def step():
         loss, lse = cce.cce_forward(E, C, xt, -100, red, workspace=ws_f, dev_err=err, check_errors=False)
         cce.cce_backward(E, C, xt, lse, g, -100, red, eps, workspace=ws_b, dev_err=err, check_errors=False,
-                         dE=dE, dC=dC)
+                         dE=dE, dC=dC, vocab_sort=sort)
         return loss
 
     for _ in range(args.warmup):
@@ -223,7 +225,8 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.reset_peak_memory_stats(dev)
     base = torch.cuda.memory_allocated(dev)
     loss, lse = cce.cce_forward(E, C, xt, -100, red, dev_err=err, check_errors=False)
-    _, _, st = cce.cce_backward(E, C, xt, lse, g, -100, red, eps, dev_err=err, check_errors=False, stats=True)
+    _, _, st = cce.cce_backward(E, C, xt, lse, g, -100, red, eps, dev_err=err, check_errors=False, stats=True,
+                                vocab_sort=sort)
     torch.cuda.synchronize()
     outputs = dE.numel() * 2 + dC.numel() * 2 + N * 4 + (N * 4 if red == "none" else 4) + 16
     peak_extra = torch.cuda.max_memory_allocated(dev) - base - outputs
@@ -267,7 +270,7 @@ def run_gpu(args, rank, world, local_rank):
         xd.copy_(xh, non_blocking=True)
         Ed.requires_grad_(True)
         Cd.requires_grad_(True)
-        loss = cce.linear_cross_entropy(Ed, Cd, xd, -100, red, eps)
+        loss = cce.linear_cross_entropy(Ed, Cd, xd, -100, red, eps, vocab_sort=sort)
         loss.backward()
         loss_h.copy_(loss.detach().reshape(1), non_blocking=True)
         Ed.requires_grad_(False)
@@ -319,7 +322,7 @@ def run_gpu(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": round(agg["ms_per_step"], 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{WORKLOAD_NAMES[args.config]} N={N} D={D} V={V}", "N": N, "D": D, "V": V,
-                   "reduction": red, "filter_eps": eps, "ignore_frac": w.ignore_frac,
+                   "reduction": red, "filter_eps": eps, "vocab_sort": sort, "ignore_frac": w.ignore_frac,
                    "l2": f"inputs larger than L2 (C is {C.numel() * 2 / 1e6:.0f} MB)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         # the pages' metric: 8 N D V over all N tokens, whatever the filter or
@@ -342,7 +345,7 @@ W_FILTER_EPS = 2.0 ** -12
 def run_reference(args):
     """The fp64 oracle on the host cores: each step one bounded sample."""
     import oracle
-    w = W.CONFIGS[args.config]
+    w = W.ALL_CONFIGS[args.config]
     E_bits, C_bits, x = W.make_inputs(w)
     rate, sample, cores = oracle_sample_rate(w, E_bits, C_bits, x, target_s=6.0)
     k = max(1, int(round(rate * 3.0)))  # ~3 s per step
@@ -375,14 +378,16 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
-    ap.add_argument("--config", choices=tuple(W.CONFIGS), default=DEFAULT_CONFIG)
+    ap.add_argument("--config", choices=tuple(W.ALL_CONFIGS), default=DEFAULT_CONFIG)
     ap.add_argument("--filter", choices=("on", "off"), default=None)
+    ap.add_argument("--vocab-sort", action="store_true",
+                    help="filter over the vocabulary sorted by average logit")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.filter is None:
-        args.filter = W.CONFIGS[args.config].filter_modes[0]
+        args.filter = W.ALL_CONFIGS[args.config].filter_modes[0]
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

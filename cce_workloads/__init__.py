@@ -195,7 +195,7 @@ class Workload:
     D: int
     V: int
     c_scale: float          # C ~ N(0, (c_scale / sqrt(D))^2)
-    targets: str            # "uniform" or "zipf"
+    targets: str            # "uniform", "zipf" or "frequent_scattered"
     zipf_s: float = 1.1
     boost: float = 0.0      # E_i += boost * C[x_i] / ||C[x_i]||
     ignore_frac: float = 0.0
@@ -229,6 +229,16 @@ CONFIGS = {
 }
 CONFIG_ORDER = ("tiny", "qwen", "gemma", "llama", "long")
 
+# A supplementary workload (not one of the five above): the Qwen2.5-0.5B head
+# shape with the softmax mass on 256 frequent tokens that a random vocabulary
+# order scatters (frequent_token_inputs with scatter=True, unigram=8) -- the
+# case vocabulary sorting is for.
+SUPPLEMENTARY = {
+    "freq": Workload("freq", 4096, 896, 151936, 0.0, "frequent_scattered", ignore_frac=0.05,
+                     reduction="mean", filter_modes=("on",)),
+}
+ALL_CONFIGS = {**CONFIGS, **SUPPLEMENTARY}
+
 
 def make_inputs(w: Workload):
     """Draw (E_bits [N,D] uint16, C_bits [V,D] uint16, x [N] int64) for w.
@@ -241,6 +251,9 @@ def make_inputs(w: Workload):
     was applied to those rows too).
     """
     N, D, V = w.N, w.D, w.V
+    if w.targets == "frequent_scattered":
+        return frequent_token_inputs(N, D, V, n_freq=256, seed=w.seed, ignore_frac=w.ignore_frac, scatter=True,
+                                     unigram=8.0)
     C_bits = normal_bf16(w.seed, _S_C, V * D, w.c_sigma).reshape(V, D)
     if w.targets == "uniform":
         x = _gen(w.seed, _S_XUNIF).integers(0, V, size=N, dtype=np.int64)

@@ -186,16 +186,62 @@ cce_status cce_forward_ex(const void* E, const void* C, const int64_t* x, int64_
  *                    no Kahan compensation is needed);
  *   CCE_FILTER_DC    only dC skips them (CCE-Kahan-FullE);
  *   0                neither (same as filter_eps = 0).
- * The survival map and dev_stats always describe the filter decisions.  Any
- * other flag bit returns CCE_ERR_ARG.
+ * The survival map and dev_stats always describe the filter decisions.
+ *
+ * CCE_SORT_VOCAB (OR-ed into filter_flags) walks the vocabulary in sorted
+ * order ("Cut Your Losses ...", section "Vocabulary Sorting"): tokens are
+ * ordered by their logit sum over the rows that take part, ascending, equal
+ * sums by token id (the pages sort by the average logit; dividing by the row
+ * count does not change the order).  The sums are computed on the device as
+ * C_v . (sum of those rows of E) in fp32, in a fixed order, so the order is
+ * deterministic.  The filter tiles are then 128 consecutive sorted positions,
+ * which groups the tokens that carry softmax mass into few tiles; dE and dC
+ * are those of the same gradient (dC in token order: the dC tiles write their
+ * token rows directly).  Costs: a pass over C for the sums, a radix sort of V
+ * keys, and per vocabulary chunk a gather of its C rows into sorted order;
+ * the workspace grows to cce_backward_workspace_bytes_ex(N, D, V, flags).
+ * Any other flag bit returns CCE_ERR_ARG.
  */
 #define CCE_FILTER_DE 1
 #define CCE_FILTER_DC 2
 #define CCE_FILTER_BOTH 3
+#define CCE_SORT_VOCAB 4
 cce_status cce_backward_ex(const void* E, const void* C, const int64_t* x, const float* lse,
                            const float* grad_out, int64_t N, int64_t D, int64_t V, int64_t ignore_index,
                            int reduction, float softcap, float filter_eps, int filter_flags, void* dE, void* dC,
                            void* workspace, size_t ws_bytes, int32_t* dev_err, int64_t* dev_stats, void* stream);
+
+/* Workspace of cce_backward_ex for these sizes and flags (0 for invalid
+ * sizes or flags).  Equals cce_backward_workspace_bytes() without
+ * CCE_SORT_VOCAB; with it, adds the sort keys, the order and its inverse
+ * (12 bytes per token), the sort scratch, and one vocabulary chunk of C in
+ * sorted order (bf16). */
+size_t cce_backward_workspace_bytes_ex(int64_t N, int64_t D, int64_t V, int flags);
+
+/*
+ * The two steps of vocabulary sorting, exposed on their own (the backward
+ * with CCE_SORT_VOCAB runs the same kernels on its compacted rows).
+ *
+ * cce_vocab_logit_sums: sums[v] (fp32, [V], written) = sum over the rows i
+ *   that take part (x_i in [0, V) and != ignore_index) of the logit C_v . E_i,
+ *   computed as C_v . (sum_i E_i) -- the statistic "Cut Your Losses ...",
+ *   section "Vocabulary Sorting", accumulates (its average is sums / count).
+ *   Deterministic: fp32 column sums in a fixed order, then fp32 dot products
+ *   in a fixed order.
+ * cce_vocab_order: perm (int32 [V], written) = the stable ascending order of
+ *   keys (fp32 [V], device): perm[j] is the token at position j; equal keys
+ *   (-0.0 equals +0.0) keep increasing token id.  The order of NaN keys is
+ *   unspecified.  A least-significant-digit radix sort, 4 passes of 8 bits.
+ * workspace: >= cce_vocab_sort_workspace_bytes(N, D, V) bytes, scratch (for
+ *   cce_vocab_order any N >= 1, D >= 8 with D % 8 == 0 gives a large enough
+ *   figure).  Same argument checks and status codes as the other calls; E, C
+ *   and workspace 16-byte aligned, keys / sums / perm 4-byte aligned.
+ */
+size_t cce_vocab_sort_workspace_bytes(int64_t N, int64_t D, int64_t V);
+cce_status cce_vocab_logit_sums(const void* E, const void* C, const int64_t* x, int64_t N, int64_t D, int64_t V,
+                                int64_t ignore_index, float* sums, void* workspace, size_t ws_bytes, void* stream);
+cce_status cce_vocab_order(const float* keys, int64_t V, int32_t* perm, void* workspace, size_t ws_bytes,
+                           void* stream);
 
 /* Memory accounting (host arithmetic, no GPU).  Reproduces the page's memory
  * table ("Cut Cross-Entropy: Training Loss Without the Logit Matrix ...",
@@ -236,8 +282,10 @@ uint64_t cce_kernel_launch_count(void);
  * cce_profile_read synchronises on those events and returns, per phase, the
  * summed milliseconds and the number of launches since the last reset.
  * Phases: 0 fwd_lse_gemm, 1 fwd_combine, 2 bwd_prep, 3 bwd_recompute_g,
- * 4 bwd_grad_gemm (dC and dE of a vocabulary chunk, one launch), 5 bwd_finalize. */
-#define CCE_NUM_PHASES 6
+ * 4 bwd_grad_gemm (dC and dE of a vocabulary chunk, one launch), 5 bwd_finalize,
+ * 6 bwd_vocab_sort (with CCE_SORT_VOCAB: sums, order, target remap, and the
+ * per-chunk gather of C). */
+#define CCE_NUM_PHASES 7
 cce_status cce_profile_enable(int enable);
 cce_status cce_profile_reset(void);
 cce_status cce_profile_read(double* ms /* host [CCE_NUM_PHASES] */, int64_t* launches /* host [CCE_NUM_PHASES] */);

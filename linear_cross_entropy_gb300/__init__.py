@@ -30,7 +30,7 @@ FILTER_EPS = 2.0 ** -12  # finfo(bf16).eps / 32
 __all__ = [
     "linear_cross_entropy", "cce_forward", "cce_backward", "CCEError", "FILTER_EPS",
     "forward_workspace_bytes", "backward_workspace_bytes", "memory_report", "kernel_launch_count",
-    "Profiler",
+    "Profiler", "vocab_logit_sums", "vocab_order",
 ]
 
 _lib.load()
@@ -63,8 +63,9 @@ def forward_workspace_bytes(N, D, V) -> int:
     return int(_lib.load().cce_forward_workspace_bytes(N, D, V))
 
 
-def backward_workspace_bytes(N, D, V) -> int:
-    return int(_lib.load().cce_backward_workspace_bytes(N, D, V))
+def backward_workspace_bytes(N, D, V, *, filter_outputs="both", vocab_sort=False) -> int:
+    flags = FILTER_OUTPUTS[filter_outputs] | (_lib.SORT_VOCAB if vocab_sort else 0)
+    return int(_lib.load().cce_backward_workspace_bytes_ex(N, D, V, flags))
 
 
 def memory_report(N, D, V) -> dict:
@@ -116,12 +117,14 @@ FILTER_OUTPUTS = {"both": 3, "dE": 1, "dC": 2, "none": 0}
 
 
 def cce_backward(E, C, x, lse, grad_out, ignore_index=-100, reduction="mean", filter_eps=FILTER_EPS, *,
-                 filter_outputs="both", softcap=0.0, stream=None, check_errors=True, workspace=None,
-                 dev_err=None, stats=False, dE=None, dC=None):
+                 filter_outputs="both", softcap=0.0, vocab_sort=False, stream=None, check_errors=True,
+                 workspace=None, dev_err=None, stats=False, dE=None, dC=None):
     """Returns (dE, dC) or (dE, dC, {tiles, skipped}) with stats=True.
 
     filter_outputs: which gradients skip the filtered tiles -- "both" (plain
-    CCE), "dE" (dC from every tile: CCE-Kahan-FullC), "dC" (FullE) or "none"."""
+    CCE), "dE" (dC from every tile: CCE-Kahan-FullC), "dC" (FullE) or "none".
+    vocab_sort: filter over the vocabulary sorted by average logit (the
+    gradients are the same; the tiles, and so what the filter skips, differ)."""
     _check_inputs(E, C, x)
     N, D = E.shape
     V = C.shape[0]
@@ -136,7 +139,8 @@ def cce_backward(E, C, x, lse, grad_out, ignore_index=-100, reduction="mean", fi
         dE = torch.empty_like(E)
     if dC is None:
         dC = torch.empty_like(C)
-    need = int(lib.cce_backward_workspace_bytes(N, D, V))
+    flags = FILTER_OUTPUTS[filter_outputs] | (_lib.SORT_VOCAB if vocab_sort else 0)
+    need = int(lib.cce_backward_workspace_bytes_ex(N, D, V, flags))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     if dev_err is None:
@@ -144,7 +148,7 @@ def cce_backward(E, C, x, lse, grad_out, ignore_index=-100, reduction="mean", fi
     st_t = torch.zeros(2, dtype=torch.int64, device=dev) if stats else None
     with torch.cuda.device(dev):
         st = lib.cce_backward_ex(_ptr(E), _ptr(C), _ptr(x), _ptr(lse), _ptr(g), N, D, V, int(ignore_index), red,
-                                 float(softcap), float(filter_eps), FILTER_OUTPUTS[filter_outputs], _ptr(dE), _ptr(dC),
+                                 float(softcap), float(filter_eps), flags, _ptr(dE), _ptr(dC),
                                  _ptr(workspace), workspace.numel(), _ptr(dev_err), _ptr(st_t),
                                  _stream_handle(stream))
     _lib.check(st, "cce_backward")
@@ -158,31 +162,65 @@ def cce_backward(E, C, x, lse, grad_out, ignore_index=-100, reduction="mean", fi
 
 class LinearCrossEntropyFunction(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, E, C, x, ignore_index, reduction, filter_eps, filter_outputs, softcap):
+    def forward(ctx, E, C, x, ignore_index, reduction, filter_eps, filter_outputs, softcap, vocab_sort):
         loss, lse = cce_forward(E, C, x, ignore_index, reduction, softcap=softcap)
         ctx.save_for_backward(E, C, x, lse)
-        ctx.cfg = (ignore_index, reduction, filter_eps, filter_outputs, softcap)
+        ctx.cfg = (ignore_index, reduction, filter_eps, filter_outputs, softcap, vocab_sort)
         return loss
 
     @staticmethod
     def backward(ctx, grad_loss):
         E, C, x, lse = ctx.saved_tensors
-        ignore_index, reduction, filter_eps, filter_outputs, softcap = ctx.cfg
+        ignore_index, reduction, filter_eps, filter_outputs, softcap, vocab_sort = ctx.cfg
         dE, dC = cce_backward(E, C, x, lse, grad_loss, ignore_index, reduction, filter_eps,
-                              filter_outputs=filter_outputs, softcap=softcap)
-        return dE, dC, None, None, None, None, None, None
+                              filter_outputs=filter_outputs, softcap=softcap, vocab_sort=vocab_sort)
+        return dE, dC, None, None, None, None, None, None, None
 
 
 def linear_cross_entropy(E, C, x, ignore_index=-100, reduction="mean", filter_eps=FILTER_EPS,
-                         filter_outputs="both", softcap=0.0):
+                         filter_outputs="both", softcap=0.0, vocab_sort=False):
     """Cross-entropy of the logits E @ C^T against targets x, never materialised.
 
     E [N, D] bf16 (hidden states), C [V, D] bf16 (classifier weight), x [N]
     int64.  filter_eps is the backward's tile-skip threshold (0 disables);
     filter_outputs picks which gradients it applies to ("both", "dE", "dC",
-    "none"); softcap > 0 caps the logits as softcap * tanh(logit / softcap)."""
+    "none"); softcap > 0 caps the logits as softcap * tanh(logit / softcap);
+    vocab_sort filters over the vocabulary sorted by average logit."""
     return LinearCrossEntropyFunction.apply(E, C, x, ignore_index, reduction, filter_eps, filter_outputs,
-                                            softcap)
+                                            softcap, vocab_sort)
+
+
+def vocab_logit_sums(E, C, x, ignore_index=-100, *, stream=None):
+    """sums[v] = sum of the logits C_v . E_i over the rows that take part
+    (fp32 [V]); the statistic vocabulary sorting orders by."""
+    _check_inputs(E, C, x)
+    N, D = E.shape
+    V = C.shape[0]
+    lib = _lib.load()
+    ws = torch.empty(max(int(lib.cce_vocab_sort_workspace_bytes(N, D, V)), 16), dtype=torch.uint8,
+                     device=E.device)
+    sums = torch.empty(V, dtype=torch.float32, device=E.device)
+    with torch.cuda.device(E.device):
+        st = lib.cce_vocab_logit_sums(_ptr(E), _ptr(C), _ptr(x), N, D, V, int(ignore_index), _ptr(sums), _ptr(ws),
+                                      ws.numel(), _stream_handle(stream))
+    _lib.check(st, "cce_vocab_logit_sums")
+    return sums
+
+
+def vocab_order(keys, *, stream=None):
+    """perm (int32 [V]): the stable ascending order of the fp32 keys."""
+    if not keys.is_cuda or keys.dtype != torch.float32 or keys.dim() != 1:
+        raise ValueError("keys must be a 1-D float32 CUDA tensor")
+    keys = keys.contiguous()
+    V = keys.numel()
+    lib = _lib.load()
+    ws = torch.empty(max(int(lib.cce_vocab_sort_workspace_bytes(1, 8, V)), 16), dtype=torch.uint8,
+                     device=keys.device)
+    perm = torch.empty(V, dtype=torch.int32, device=keys.device)
+    with torch.cuda.device(keys.device):
+        st = lib.cce_vocab_order(_ptr(keys), V, _ptr(perm), _ptr(ws), ws.numel(), _stream_handle(stream))
+    _lib.check(st, "cce_vocab_order")
+    return perm
 
 
 @dataclass

@@ -21,7 +21,8 @@ STATUS_NAMES = {
 RED = {"none": 0, "sum": 1, "mean": 2}
 DEVERR_TARGET_RANGE = 1
 DEVERR_TIMEOUT = 2
-NUM_PHASES = 6
+NUM_PHASES = 7
+SORT_VOCAB = 4
 
 
 class CCEError(RuntimeError):
@@ -72,6 +73,14 @@ def load() -> ctypes.CDLL:
     lib.cce_backward_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_int, ctypes.c_float,
                                     ctypes.c_float, ctypes.c_int, vp, vp, vp, sz, vp, vp, vp]
     lib.cce_backward_ex.restype = ctypes.c_int
+    lib.cce_backward_workspace_bytes_ex.argtypes = [i64, i64, i64, ctypes.c_int]
+    lib.cce_backward_workspace_bytes_ex.restype = sz
+    lib.cce_vocab_sort_workspace_bytes.argtypes = [i64, i64, i64]
+    lib.cce_vocab_sort_workspace_bytes.restype = sz
+    lib.cce_vocab_logit_sums.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, vp, sz, vp]
+    lib.cce_vocab_logit_sums.restype = ctypes.c_int
+    lib.cce_vocab_order.argtypes = [vp, i64, vp, vp, sz, vp]
+    lib.cce_vocab_order.restype = ctypes.c_int
     lib.cce_forward_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, ctypes.c_int, vp, vp, vp, vp]
     lib.cce_forward_noalloc.restype = ctypes.c_int
     lib.cce_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint32, vp]

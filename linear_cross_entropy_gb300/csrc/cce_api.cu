@@ -294,10 +294,13 @@ FwdLayout fwd_layout(int64_t N, int64_t V) {
 
 struct BwdLayout {
   size_t count, counters, pos, ridx, xc, lsec, gc, ec, bitmap, bitmapT, gbuf, deacc, total;
+  // vocabulary sorting only: sort keys, order and its inverse, scratch, and
+  // the chunk of C in sorted order
+  size_t keys, perm, inv, sortscr, cs;
   int64_t vc, bm_ld, n128, nchunks;
 };
 
-BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V) {
+BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V, bool sort = false) {
   BwdLayout L{};
   L.vc = bwd_chunk_cols(N, V);
   L.bm_ld = cdiv(V, 128);
@@ -328,6 +331,18 @@ BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V) {
   o = align_up(o + static_cast<size_t>(N) * L.vc * 2, ALIGN);
   L.deacc = o;
   o = align_up(o + static_cast<size_t>(N) * D * 4, ALIGN);
+  if (sort) {
+    L.keys = o;
+    o = align_up(o + sizeof(float) * static_cast<size_t>(V), ALIGN);
+    L.perm = o;
+    o = align_up(o + sizeof(int) * static_cast<size_t>(V), ALIGN);
+    L.inv = o;
+    o = align_up(o + sizeof(int) * static_cast<size_t>(V), ALIGN);
+    L.sortscr = o;
+    o = align_up(o + std::max(vocab_keys_scratch_bytes(N, D), vocab_order_scratch_bytes(V)), ALIGN);
+    L.cs = o;
+    o = align_up(o + static_cast<size_t>(L.vc) * D * 2, ALIGN);
+  }
   L.total = o;
   return L;
 }
@@ -505,6 +520,50 @@ size_t cce_backward_workspace_bytes(int64_t N, int64_t D, int64_t V) {
   return bwd_layout(N, D, V).total;
 }
 
+size_t cce_backward_workspace_bytes_ex(int64_t N, int64_t D, int64_t V, int flags) {
+  if (!sizes_ok(N, D, V) || (flags & ~(CCE_FILTER_BOTH | CCE_SORT_VOCAB))) return 0;
+  return bwd_layout(N, D, V, (flags & CCE_SORT_VOCAB) != 0).total;
+}
+
+size_t cce_vocab_sort_workspace_bytes(int64_t N, int64_t D, int64_t V) {
+  if (!sizes_ok(N, D, V)) return 0;
+  return std::max(vocab_keys_scratch_bytes(N, D), vocab_order_scratch_bytes(V));
+}
+
+cce_status cce_vocab_logit_sums(const void* E, const void* C, const int64_t* x, int64_t N, int64_t D, int64_t V,
+                                int64_t ignore_index, float* sums, void* workspace, size_t ws_bytes, void* stream) {
+  if (!E || !C || !x || !sums || !workspace) return CCE_ERR_NULL;
+  if (!sizes_ok(N, D, V)) return CCE_ERR_SHAPE;
+  if (!aligned16(E) || !aligned16(C) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(x) & 7u) ||
+      (reinterpret_cast<uintptr_t>(sums) & 3u))
+    return CCE_ERR_ALIGN;
+  if (ws_bytes < cce_vocab_sort_workspace_bytes(N, D, V)) return CCE_ERR_WORKSPACE;
+  int sms = 0;
+  cce_status st = device_check(&sms);
+  if (st != CCE_OK) return st;
+  int launched = 0;
+  cudaError_t e = launch_vocab_keys(E, N, nullptr, x, static_cast<long long>(ignore_index), D, C, V, sums,
+                                    workspace, static_cast<cudaStream_t>(stream), sms, &launched);
+  g_launches += static_cast<uint64_t>(launched);
+  return cuda_status(e);
+}
+
+cce_status cce_vocab_order(const float* keys, int64_t V, int32_t* perm, void* workspace, size_t ws_bytes,
+                           void* stream) {
+  if (!keys || !perm || !workspace) return CCE_ERR_NULL;
+  if (!sizes_ok(1, 8, V)) return CCE_ERR_SHAPE;
+  if (!aligned16(workspace) || (reinterpret_cast<uintptr_t>(keys) & 3u) || (reinterpret_cast<uintptr_t>(perm) & 3u))
+    return CCE_ERR_ALIGN;
+  if (ws_bytes < vocab_order_scratch_bytes(V)) return CCE_ERR_WORKSPACE;
+  int sms = 0;
+  cce_status st = device_check(&sms);
+  if (st != CCE_OK) return st;
+  int launched = 0;
+  cudaError_t e = launch_vocab_order(keys, V, perm, workspace, static_cast<cudaStream_t>(stream), sms, &launched);
+  g_launches += static_cast<uint64_t>(launched);
+  return cuda_status(e);
+}
+
 cce_status cce_memory_accounting(int64_t N, int64_t D, int64_t V, cce_memory_report* out) {
   if (!out) return CCE_ERR_NULL;
   if (!sizes_ok(N, D, V)) return CCE_ERR_SHAPE;
@@ -617,9 +676,10 @@ cce_status cce_backward_ex(const void* E, const void* C, const int64_t* x, const
     return CCE_ERR_ALIGN;
   if (reduction != CCE_RED_NONE && reduction != CCE_RED_SUM && reduction != CCE_RED_MEAN) return CCE_ERR_ARG;
   if (!(filter_eps >= 0.0f) || !std::isfinite(filter_eps)) return CCE_ERR_ARG;
-  if (filter_flags & ~CCE_FILTER_BOTH) return CCE_ERR_ARG;
+  if (filter_flags & ~(CCE_FILTER_BOTH | CCE_SORT_VOCAB)) return CCE_ERR_ARG;
   if (!(softcap >= 0.0f) || !std::isfinite(softcap)) return CCE_ERR_ARG;
-  const BwdLayout W = bwd_layout(N, D, V);
+  const bool sort = (filter_flags & CCE_SORT_VOCAB) != 0;
+  const BwdLayout W = bwd_layout(N, D, V, sort);
   if (ws_bytes < W.total) return CCE_ERR_WORKSPACE;
   int sms = 0;
   cce_status st = device_check(&sms);
@@ -654,6 +714,24 @@ cce_status cce_backward_ex(const void* E, const void* C, const int64_t* x, const
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_status(e);
   }
+  // Vocabulary sorting ("Cut Your Losses ...", section "Vocabulary
+  // Sorting"): order the vocabulary by the logit sum over the compact rows,
+  // and move every compact target to its sorted position.  The chunks below
+  // then cover consecutive sorted positions.
+  int* perm = sort ? reinterpret_cast<int*>(ws + W.perm) : nullptr;
+  void* Cs = sort ? static_cast<void*>(ws + W.cs) : nullptr;
+  if (sort) {
+    PhaseScope ps(6, s);
+    int launched = 0;
+    float* keys = reinterpret_cast<float*>(ws + W.keys);
+    void* scr = ws + W.sortscr;
+    cudaError_t e = launch_vocab_keys(Ec, N, count, nullptr, 0, D, C, V, keys, scr, s, sms, &launched);
+    if (e == cudaSuccess) e = launch_vocab_order(keys, V, perm, scr, s, sms, &launched);
+    if (e == cudaSuccess)
+      e = launch_remap_targets(perm, V, reinterpret_cast<int*>(ws + W.inv), xc, count, N, s, sms, &launched);
+    g_launches += static_cast<uint64_t>(launched);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
 
   GemmArgs g;  // recompute + G
   std::memset(&g, 0, sizeof(g));
@@ -661,17 +739,22 @@ cce_status cce_backward_ex(const void* E, const void* C, const int64_t* x, const
   std::memset(&r, 0, sizeof(r));
   const uint64_t vc = static_cast<uint64_t>(W.vc);
   bool ok = true;
+  // C as the GEMMs see it: the whole tensor, or (sorted) one chunk's rows
+  // gathered into sorted order; sorted dC tiles write their token rows of dC
+  // directly (dc_rows), unsorted ones through the dC tensor map
+  const void* Cg = sort ? Cs : C;
+  const uint64_t c_rows = sort ? vc : static_cast<uint64_t>(V);
   ok &= make_tmap(&g.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Ec, D, N, D, BK, BM);
-  ok &= make_tmap(&g.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, D, V, D, BK, BN);
+  ok &= make_tmap(&g.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Cg, D, c_rows, D, BK, BN);
   ok &= make_tmap(&g.tmOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, gbuf, vc, N, vc, 64, 32);
   r.b3d = (D % 64 == 0) ? 1 : 0;
   ok &= make_tmap_mn3(&r.tmA, gbuf, vc, N, BM / 64);  // G chunk, MN-major A of dC (vc % 256 == 0)
   if (r.b3d) {
     ok &= make_tmap_mn3(&r.tmB, Ec, D, N);
-    ok &= make_tmap_mn3(&r.tmB2, C, D, V);
+    ok &= make_tmap_mn3(&r.tmB2, Cg, D, c_rows);
   } else {
     ok &= make_tmap(&r.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Ec, D, N, D, 64, 64);
-    ok &= make_tmap(&r.tmB2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, D, V, D, 64, 64);
+    ok &= make_tmap(&r.tmB2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Cg, D, c_rows, D, 64, 64);
   }
   ok &= make_tmap(&r.tmOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dC, D, V, D, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
   ok &= make_tmap(&r.tmA2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, gbuf, vc, N, vc, 64, BM);
@@ -684,7 +767,9 @@ cce_status cce_backward_ex(const void* E, const void* C, const int64_t* x, const
     p->V = static_cast<int>(V);
     p->n_blocks = static_cast<int>(cdiv(N, BM));
     p->x = xc;  // every per-row input in compact order
-    p->ignore_index = ignore_index;
+    // sorted: targets are sorted positions in [0, V) and the padding rows
+    // hold -1, so no compact target can collide with the ignore index
+    p->ignore_index = sort ? -1 : ignore_index;
     p->lse = lsec;
     p->grad_out = reduction == CCE_RED_NONE ? gc : grad_out;
     p->count = count;
@@ -718,7 +803,10 @@ cce_status cce_backward_ex(const void* E, const void* C, const int64_t* x, const
     for (GemmArgs* p : {&g, &r}) {
       p->chunk_v0 = v0;
       p->chunk_w = w;
+      p->c_row0 = sort ? 0 : v0;
     }
+    r.dc_rows = sort ? perm + v0 : nullptr;
+    r.dC_out = static_cast<uint16_t*>(dC);
     g.v_tiles = static_cast<int>(cdiv(w, BN));
     g.counter = counters + 2 * ch;
     r.dc_m_tiles = static_cast<int>(cdiv(w, BM));
@@ -727,6 +815,14 @@ cce_status cce_backward_ex(const void* E, const void* C, const int64_t* x, const
     r.first_chunk = (ch == 0) ? 1 : 0;
     r.counter = counters + 2 * ch + 1;
     cudaError_t e;
+    if (sort) {  // the chunk's C rows in sorted order, zero rows up to the last 256-row tile
+      PhaseScope ps(6, s);
+      int launched = 0;
+      e = launch_gather_vocab_rows(C, perm + v0, w, std::min<int64_t>(W.vc, cdiv(w, BN) * BN), D, Cs, s, sms,
+                                   &launched);
+      g_launches += static_cast<uint64_t>(launched);
+      if (e != cudaSuccess) return cuda_status(e);
+    }
     {
       PhaseScope ps(3, s);
       e = launch_gemm(MODE_BWD_G, g, std::min(sms, g.n_blocks * g.v_tiles), s);
@@ -811,8 +907,8 @@ cce_status cce_profile_read(double* ms, int64_t* launches) {
 }
 
 const char* cce_profile_phase_name(int phase) {
-  static const char* names[CCE_NUM_PHASES] = {"fwd_lse_gemm",    "fwd_combine",   "bwd_prep",
-                                               "bwd_recompute_g", "bwd_grad_gemm", "bwd_finalize"};
+  static const char* names[CCE_NUM_PHASES] = {"fwd_lse_gemm",  "fwd_combine",  "bwd_prep",       "bwd_recompute_g",
+                                               "bwd_grad_gemm", "bwd_finalize", "bwd_vocab_sort"};
   if (phase < 0 || phase >= CCE_NUM_PHASES) return "";
   return names[phase];
 }

@@ -118,19 +118,47 @@ __device__ __forceinline__ int kblocks_of(const GemmArgs& a, const Dims& dm, con
   return a.k_blocks;
 }
 
-// Is K-block kb of tile t skipped by the filter?  (dC: K = tokens, read from
-// the vocabulary-major map; dE: K = chunk columns.)  FWD and BWD_G never skip.
+// The first K-block >= kb of tile t that the filter keeps (nk when none).
+// dC: K = tokens, read from the vocabulary-major map; dE: K = chunk columns;
+// FWD and BWD_G never skip.  Filter tile j covers K-blocks 2j and 2j + 1;
+// the survival bytes are read 8
+// at a time with independent loads, so a long run of skipped tiles costs one
+// load latency per 16 K-blocks instead of one per K-block.
 template <int MODE>
-__device__ __forceinline__ bool kblock_skipped(const GemmArgs& a, const Tile& t, int kb) {
-  if constexpr (MODE == MODE_GRAD) {
+__device__ __forceinline__ int next_kblock(const GemmArgs& a, const Tile& t, int kb, int nk) {
+  if constexpr (MODE != MODE_GRAD) {
+    return kb;
+  } else {
+    const uint8_t* row;
     if (t.kind == KIND_DC) {
-      if (!a.filter_dc) return false;
-      return __ldg(a.bitmapT + static_cast<size_t>((a.chunk_v0 >> 7) + t.m) * a.n_blocks + (kb >> 1)) == 0;
+      if (!a.filter_dc) return kb;
+      row = a.bitmapT + static_cast<size_t>((a.chunk_v0 >> 7) + t.m) * a.n_blocks;
+    } else {
+      if (!a.filter_de) return kb;
+      row = a.bitmap + static_cast<size_t>(t.m) * a.bm_ld + (a.chunk_v0 >> 7);
     }
-    if (!a.filter_de) return false;
-    return __ldg(a.bitmap + static_cast<size_t>(t.m) * a.bm_ld + (a.chunk_v0 >> 7) + (kb >> 1)) == 0;
+    const int jn = (nk + 1) >> 1;
+    int j = kb >> 1;
+    if (j >= jn) return nk;
+    if (__ldg(row + j)) return kb;  // kept: the common case of a dense tile costs one load
+    ++j;
+    while (j < jn) {
+      if (j + 8 <= jn) {
+        uint8_t v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = __ldg(row + j + u);
+        int f = 8;
+#pragma unroll
+        for (int u = 7; u >= 0; --u) f = v[u] ? u : f;
+        if (f < 8) return max(kb, 2 * (j + f));
+        j += 8;
+      } else {
+        if (__ldg(row + j)) return max(kb, 2 * j);
+        ++j;
+      }
+    }
+    return nk;
   }
-  return false;
 }
 
 // Warp-wide: does the output tile have no surviving K-block at all?
@@ -176,9 +204,16 @@ struct SmemLayout {
   uint64_t* ring_empty;
   uint32_t* tmem_base;
   int* abort_flag;
-  int* flags;     // [2 parity][2 half][4 warps]
-  int* ring_ids;  // [RING]
+  int* flags;       // [2 parity][2 half][4 warps]
+  int* ring_ids;    // [RING]
+  int* stage_meta;  // [STAGES] what the producer put in the stage (META_*)
 };
+
+// Stage tags written by the producer before it arms the stage's full
+// barrier: the MMA thread learns where a tile's K loop ends (or that the
+// tile has no K-block left after filtering) without reading the filter map.
+constexpr int META_LAST = 1;   // the tile's last K-block
+constexpr int META_EMPTY = 2;  // no data: the tile has no K-block at all
 
 __device__ __forceinline__ SmemLayout carve_smem(uint8_t* raw) {
   SmemLayout L;
@@ -199,6 +234,7 @@ __device__ __forceinline__ SmemLayout carve_smem(uint8_t* raw) {
   L.abort_flag = reinterpret_cast<int*>(tail + 4);
   L.flags = reinterpret_cast<int*>(tail + 8);      // 16 ints
   L.ring_ids = reinterpret_cast<int*>(tail + 72);  // RING ints
+  L.stage_meta = reinterpret_cast<int*>(tail + 72 + 4 * RING);  // STAGES ints
   return L;
 }
 
@@ -233,9 +269,24 @@ __device__ __forceinline__ void producer_loop(const GemmArgs& a, const SmemLayou
     if (item < 0) break;
     const bool ok = for_each_tile_of_item<MODE>(a, dm, item, [&](const Tile& t) -> bool {
       const int nk = kblocks_of<MODE>(a, dm, t);
-      for (int kb = 0; kb < nk; ++kb) {
-        if (kblock_skipped<MODE>(a, t, kb)) continue;
+      int kb = next_kblock<MODE>(a, t, 0, nk);
+      if (MODE == MODE_GRAD && kb >= nk) {  // nothing survives the filter: an empty tagged stage
         if (!wait_bounded(&L.empty[stage], phase ^ 1u, abort_flag, a.dev_err)) return false;
+        L.stage_meta[stage] = META_EMPTY;
+        mbar_arrive(&L.full[stage]);
+        // tracked like a copy, so the abort drain below waits on this stage's latest phase
+        issued_mask |= 1u << stage;
+        issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        return true;
+      }
+      while (kb < nk) {
+        const int next = next_kblock<MODE>(a, t, kb + 1, nk);
+        if (!wait_bounded(&L.empty[stage], phase ^ 1u, abort_flag, a.dev_err)) return false;
+        if (MODE == MODE_GRAD) L.stage_meta[stage] = next >= nk ? META_LAST : 0;
         uint8_t* sA = L.stages + stage * STAGE_BYTES;
         uint8_t* sB = sA + A_STAGE_BYTES;
         uint64_t* fb = &L.full[stage];
@@ -243,7 +294,7 @@ __device__ __forceinline__ void producer_loop(const GemmArgs& a, const SmemLayou
         const int k0 = kb * BK;
         if (MODE != MODE_GRAD) {
           tma_load_2d(&a.tmA, fb, sA, k0, t.m * BM);
-          tma_load_2d(&a.tmB, fb, sB, k0, a.chunk_v0 + t.n * BN);
+          tma_load_2d(&a.tmB, fb, sB, k0, a.c_row0 + t.n * BN);
         } else if (t.kind == KIND_DC) {
           tma_load_3d(&a.tmA, fb, sA, 0, k0, (t.m * BM) >> 6);  // both 64-column groups of A
           if (a.b3d) {  // the four 64-column groups of B in one instruction
@@ -254,10 +305,10 @@ __device__ __forceinline__ void producer_loop(const GemmArgs& a, const SmemLayou
         } else {
           tma_load_2d(&a.tmA2, fb, sA, k0, t.m * BM);
           if (a.b3d) {
-            tma_load_3d(&a.tmB2, fb, sB, 0, a.chunk_v0 + k0, (t.n * a.bn) >> 6);
+            tma_load_3d(&a.tmB2, fb, sB, 0, a.c_row0 + k0, (t.n * a.bn) >> 6);
           } else {
             for (int j = 0; j < BN / 64; ++j)
-              tma_load_2d(&a.tmB2, fb, sB + j * 8192, t.n * a.bn + j * 64, a.chunk_v0 + k0);
+              tma_load_2d(&a.tmB2, fb, sB + j * 8192, t.n * a.bn + j * 64, a.c_row0 + k0);
           }
         }
         issued_mask |= 1u << stage;
@@ -266,6 +317,7 @@ __device__ __forceinline__ void producer_loop(const GemmArgs& a, const SmemLayou
           stage = 0;
           phase ^= 1u;
         }
+        kb = next;
       }
       return true;
     });
@@ -307,12 +359,25 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& a, const SmemLayout& L,
       if (!wait_bounded(&L.tmem_empty[acc], acc_phase ^ 1u, abort_flag, a.dev_err)) return false;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-      const int nk = kblocks_of<MODE>(a, dm, t);
       bool any = false;
-      for (int kb = 0; kb < nk; ++kb) {
-        if (kblock_skipped<MODE>(a, t, kb)) continue;
+      // FWD / BWD_G: every K-block; GRAD: the producer's stage tags end the loop
+      const int nk = MODE == MODE_GRAD ? 0 : kblocks_of<MODE>(a, dm, t);
+      for (int kb = 0;; ++kb) {
+        if (MODE != MODE_GRAD && kb >= nk) break;
         if (!wait_bounded(&L.full[stage], phase, abort_flag, a.dev_err)) return false;
         tc_fence_after();
+        int meta = 0;
+        if constexpr (MODE == MODE_GRAD) {
+          meta = *reinterpret_cast<volatile int*>(&L.stage_meta[stage]);
+          if (meta & META_EMPTY) {
+            mbar_arrive(&L.empty[stage]);  // hand the stage straight back
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            break;
+          }
+        }
         const uint32_t sA = smem_u32(L.stages + stage * STAGE_BYTES);
         const uint32_t sB = sA + A_STAGE_BYTES;
         const uint64_t adesc = smem_desc_sw128(sA, a_lbo, 1024u);
@@ -328,6 +393,7 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& a, const SmemLayout& L,
           stage = 0;
           phase ^= 1u;
         }
+        if (MODE == MODE_GRAD && (meta & META_LAST)) break;
       }
       if (any) {
         mma_commit(&L.tmem_full[acc]);
@@ -584,17 +650,50 @@ __device__ __forceinline__ bool epi_bwd_g(const GemmArgs& a, const SmemLayout& L
   return ok;
 }
 
-// GRAD, KIND_DC: bf16 output tile, rows = vocabulary (chunk_v0 + 128m ...),
+// GRAD, KIND_DC: bf16 output tile, rows = vocabulary (c_row0 + 128m ...),
 // cols = D tile of width bn, stored in 32-column boxes (64-byte swizzle).
 __device__ __forceinline__ void epi_dc(const GemmArgs& a, const Dims& dm, const SmemLayout& L, const Tile& t,
                                        int acc, EpiCtx& e) {
   const uint32_t lane = lane_id();
   const bool empty = tile_empty(a, dm, t);
   const uint32_t tbase = e.taddr + static_cast<uint32_t>(acc * BN);
-  const int gy = a.chunk_v0 + t.m * BM + e.q * 32;
+  const int ly = t.m * BM + e.q * 32;  // first row of the box within the chunk
+  const int gy = a.c_row0 + ly;        // ... in the dC tensor map
   const int x0 = t.n * a.bn;
-  // boxes that start inside dC (no store may start outside the tensor)
-  const int nbox = (gy < a.V) ? min(a.bn / 32, (a.D - x0 + 31) / 32) : 0;
+  if (a.dc_rows) {
+    // Sorted vocabulary: row ly + lane of the chunk is token dc_rows[ly + lane];
+    // each lane writes its own row of dC directly, 16 bytes at a time.
+    const int lr = ly + static_cast<int>(lane);
+    const bool row_ok = lr < a.chunk_w;
+    const size_t grow = row_ok ? static_cast<size_t>(__ldg(a.dc_rows + lr)) : 0;
+    uint4* dst = reinterpret_cast<uint4*>(a.dC_out + grow * a.D + x0);
+    const int nb = (ly < a.chunk_w) ? min(a.bn / 32, (a.D - x0 + 31) / 32) : 0;
+#pragma unroll 1
+    for (int j = 0; j < nb; ++j) {
+      uint32_t r[32];
+      if (!empty) {
+        tmem_ld32(tbase + 32 * j, r);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) r[u] = 0u;
+      }
+      if (row_ok) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (x0 + 32 * j + 8 * u < a.D)
+            dst[4 * j + u] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * u + 0]), __uint_as_float(r[8 * u + 1])),
+                                        pack_bf16x2(__uint_as_float(r[8 * u + 2]), __uint_as_float(r[8 * u + 3])),
+                                        pack_bf16x2(__uint_as_float(r[8 * u + 4]), __uint_as_float(r[8 * u + 5])),
+                                        pack_bf16x2(__uint_as_float(r[8 * u + 6]), __uint_as_float(r[8 * u + 7])));
+        }
+      }
+    }
+    release_tmem(L, acc);
+    return;
+  }
+  // boxes that start inside the chunk and dC (no store may start outside the tensor)
+  const int nbox = (ly < a.chunk_w) ? min(a.bn / 32, (a.D - x0 + 31) / 32) : 0;
 #pragma unroll 1
   for (int j = 0; j < nbox; ++j) {
     const int b = j & 1;

@@ -48,6 +48,12 @@ struct GemmArgs {
   int v_tiles;   // FWD: ceil(V / 256); BWD_G: 256-wide tiles in the chunk
   int chunk_v0;  // BWD: first vocabulary row of the chunk (multiple of 256)
   int chunk_w;   // BWD: vocabulary rows in the chunk
+  int c_row0;    // BWD: row of the chunk's first vocabulary entry in the C / dC tensor maps
+                 // (chunk_v0, or 0 when the chunk was gathered into sorted order)
+  // GRAD, sorted vocabulary: dc_rows[j] = the token of the chunk's row j; the
+  // dC tiles then write dC_out [V, D] bf16 rows directly (null: TMA stores)
+  const int* dc_rows;
+  uint16_t* dC_out;
   int group_n;   // BWD_G: token blocks per raster group
   // GRAD
   int bn;           // width of a D tile (multiple of 32, <= 256; of 64 when b3d)

@@ -1,6 +1,6 @@
 """Write the fp64 oracle's LSE for every row of the full-size workloads.
 
-Usage: python tests/golden/make_oracle_lse.py qwen gemma llama long
+Usage: python tests/golden/make_oracle_lse.py qwen gemma llama long freq
 
 For each workload this draws the seeded inputs (cce_workloads), runs
 oracle.forward over all rows and stores tests/golden/oracle_lse_<name>.npz
@@ -24,7 +24,7 @@ import oracle  # noqa: E402
 
 def main(names):
     for name in names:
-        w = W.CONFIGS[name]
+        w = W.ALL_CONFIGS[name]
         t0 = time.time()
         E_bits, C_bits, x = W.make_inputs(w)
         digest = W.inputs_digest(E_bits, C_bits, x)
@@ -39,4 +39,4 @@ def main(names):
 
 
 if __name__ == "__main__":
-    main(sys.argv[1:] or ["qwen", "gemma", "llama", "long"])
+    main(sys.argv[1:] or ["qwen", "gemma", "llama", "long", "freq"])

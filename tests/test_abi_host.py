@@ -75,6 +75,25 @@ def test_workspace_queries(lib, N, D, V):
     assert f < N * V * 4 or V < 1024
 
 
+@pytest.mark.parametrize("N,D,V", [(256, 128, 4096), (4096, 896, 151936), (65536, 2048, 128256), (1, 8, 1)])
+def test_sorted_workspace_adds_keys_order_and_two_chunks(lib, N, D, V):
+    """With vocabulary sorting the backward adds the keys, the order and its
+    inverse (4 bytes each per token), the sort scratch, and one chunk of C in
+    sorted order -- never a V x D copy when V spans several chunks."""
+    import linear_cross_entropy_gb300 as cce
+    b = lib.cce_backward_workspace_bytes(N, D, V)
+    for flags in (0, 1, 2, 3):
+        assert lib.cce_backward_workspace_bytes_ex(N, D, V, flags) == b
+    bs = lib.cce_backward_workspace_bytes_ex(N, D, V, 4 | 3)
+    vc = cce.memory_report(N, D, V)["bwd_chunk_cols"]
+    extra = bs - b
+    assert extra >= 12 * V + vc * D * 2
+    scratch = lib.cce_vocab_sort_workspace_bytes(N, D, V)
+    assert 12 * V <= scratch <= 12 * V + 4 * (256 * (V // 1024 + 1) + D * (N // 32 + 2)) + 4096
+    assert extra <= 12 * V + scratch + vc * D * 2 + 8 * 256
+    assert lib.cce_backward_workspace_bytes_ex(N, D, V, 8) == 0
+
+
 def test_workspace_rejects_bad_sizes(lib):
     for N, D, V in [(0, 64, 10), (10, 0, 10), (10, 64, 0), (10, 12, 10), (1 << 31, 64, 10)]:
         assert lib.cce_forward_workspace_bytes(N, D, V) == 0
@@ -146,5 +165,6 @@ def test_extended_entry_points_reject_bad_options(lib):
         assert lib.cce_forward_ex(*args, cap, vp(FAKE), vp(FAKE), vp(FAKE), 1 << 40, vp(0), vp(0)) == 4
     bargs = [vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), 256, 128, 4096, -100, 2]
     tail = [vp(FAKE), vp(FAKE), vp(FAKE), 1 << 40, vp(0), vp(0), vp(0)]
-    assert lib.cce_backward_ex(*bargs, 0.0, 2.0 ** -12, 4, *tail) == 4      # unknown flag bit
+    assert lib.cce_backward_ex(*bargs, 0.0, 2.0 ** -12, 8, *tail) == 4      # unknown flag bit
+    assert lib.cce_backward_ex(*bargs, 0.0, 2.0 ** -12, 4 | 16, *tail) == 4  # sort plus an unknown bit
     assert lib.cce_backward_ex(*bargs, -3.0, 2.0 ** -12, 3, *tail) == 4     # negative softcap

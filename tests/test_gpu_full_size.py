@@ -13,6 +13,11 @@ stored beside it proves the box drew the same bytes.  Checked here:
 * every ignored row of dE is bit-exact +0;
 * the identity <E, dE> = <C, dC> (both equal sum_i w_i sum_v G_iv a_iv),
   which ties all of dC to dE at any size.
+
+The same checks run with vocabulary sorting on, on the Qwen2.5-0.5B-shaped
+head and on the supplementary workload of that shape whose frequent tokens
+are scattered through the vocabulary (where sorting must let the filter
+skip nearly every tile).
 """
 import functools
 import os
@@ -39,7 +44,7 @@ def _built():
 
 @functools.lru_cache(maxsize=1)
 def _inputs(name):
-    w = W.CONFIGS[name]
+    w = W.ALL_CONFIGS[name]
     E, C, x = W.make_inputs(w)
     ref = np.load(os.path.join(GOLDEN, f"oracle_lse_{name}.npz"))
     assert str(ref["digest"]) == W.inputs_digest(E, C, x), "inputs differ from the ones the oracle saw"
@@ -47,11 +52,12 @@ def _inputs(name):
     return w, E, C, x, ref["lse"]
 
 
-CASES = [(n, f) for n in ("qwen", "gemma", "llama", "long") for f in W.CONFIGS[n].filter_modes]
+CASES = [(n, f, False) for n in ("qwen", "gemma", "llama", "long") for f in W.CONFIGS[n].filter_modes]
+CASES += [("qwen", "on", True), ("freq", "on", False), ("freq", "on", True)]
 
 
-@pytest.mark.parametrize("name,filter_mode", CASES)
-def test_full_size(name, filter_mode):
+@pytest.mark.parametrize("name,filter_mode,sort", CASES)
+def test_full_size(name, filter_mode, sort):
     import linear_cross_entropy_gb300 as cce
     w, E_bits, C_bits, x, lse_ref = _inputs(name)
     eps = O.FILTER_EPS if filter_mode == "on" else 0.0
@@ -59,7 +65,8 @@ def test_full_size(name, filter_mode):
     E, C, xt = to_device(E_bits, C_bits, x)
     loss, lse = cce.cce_forward(E, C, xt, reduction=w.reduction)
     g = torch.ones(1, dtype=torch.float32, device="cuda")
-    dE, dC, stats = cce.cce_backward(E, C, xt, lse, g, reduction=w.reduction, filter_eps=eps, stats=True)
+    dE, dC, stats = cce.cce_backward(E, C, xt, lse, g, reduction=w.reduction, filter_eps=eps, stats=True,
+                                     vocab_sort=sort)
     torch.cuda.synchronize()
 
     # forward: every row
@@ -99,7 +106,11 @@ def test_full_size(name, filter_mode):
     lhs = float((E.double() * dE.double()).sum())
     rhs = float((C.double() * dC.double()).sum())
     assert abs(lhs - rhs) <= 2e-2 * max(abs(lhs), abs(rhs)), (lhs, rhs)
-    print(f"{name} filter={filter_mode}: loss {loss.item():.6f} (oracle {loss_ref:.6f}) lse err {err.max():.2e} "
+    if name == "freq" and sort:
+        # 256 frequent tokens: sorted, they fill the last two or three 128-wide
+        # vocabulary tiles, so nearly every other tile is skipped
+        assert stats["skipped"] >= 0.97 * stats["tiles"], stats
+    print(f"{name} filter={filter_mode} sort={sort}: loss {loss.item():.6f} (oracle {loss_ref:.6f}) lse err {err.max():.2e} "
           f"dE err {e_dE:.2e} dC err {e_dC:.2e} tiles skipped {stats['skipped']}/{stats['tiles']} "
           f"<E,dE>={lhs:.6e} <C,dC>={rhs:.6e}")
     del E, C, dE, dC
