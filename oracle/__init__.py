@@ -43,6 +43,9 @@ Passages followed (page title, section):
   works on tiles of consecutive sorted positions.  The order (ascending,
   equal keys by token id) follows the argsort the first page names.  Sorting
   changes which tiles exist, never the unfiltered result.
+* The single call ("fused-linear-cross-entropy" page, section "2. Fused
+  Linear Cross-Entropy (FLCE)"): loss and both gradients computed together
+  for a unit upstream gradient, which the backward then multiplies in.
 * Reading where the pages are silent: mean divides by the number of
   non-ignored rows, clamped to at least 1 (the chunked-CE code on the
   "fused-linear-cross-entropy" page clamps the count the same way); the LSE of
@@ -309,6 +312,36 @@ def backward_filtered(E, C, x, lse, w, BN, BV, eps=FILTER_EPS, ignore_index=IGNO
     Gw = np.asarray(w)[:, None] * G * softcap_slope(A, softcap)
     Gf = np.where(mask, Gw, 0.0)
     return (Gf if filter_dE else Gw) @ C, (Gf if filter_dC else Gw).T @ E, keep
+
+
+def loss_and_grad(E, C, x, ignore_index=IGNORE_INDEX, reduction="mean", softcap=0.0, filter_eps=0.0, BN=128,
+                  BV=128, filter_dE=True, filter_dC=True):
+    """The single-call form of the loss ("fused-linear-cross-entropy" page,
+    section "2. Fused Linear Cross-Entropy (FLCE)"): the loss and both
+    gradients in one pass, for the reduced loss with a unit upstream gradient;
+    the autograd backward only multiplies them by the upstream gradient
+    (which is exact: both gradients are linear in it).  Only the sum and mean
+    reductions have a scalar upstream gradient, so only they are defined.
+
+    It is forward() followed by backward() with grad_out = 1.  With
+    filter_eps > 0 the skipped tiles' contributions are removed as in
+    backward_filtered over all rows in their order (the single call keeps
+    every row, so a filter tile is 128 consecutive rows, ignored ones
+    included, x 128 vocabulary entries).  Returns {loss, lse, count, dE, dC,
+    keep}."""
+    if reduction not in ("sum", "mean"):
+        raise ValueError("the single call is defined for the sum and mean reductions")
+    E = np.asarray(E, np.float64)
+    C = np.asarray(C, np.float64)
+    f = forward(E, C, x, ignore_index, reduction, softcap=softcap)
+    w = row_weights(x, ignore_index, reduction, 1.0, f["count"])
+    if filter_eps:
+        dE, dC, keep = backward_filtered(E, C, x, f["lse"], w, BN, BV, filter_eps, ignore_index, filter_dE,
+                                         filter_dC, softcap, compact_ignored=False)
+    else:
+        dE, dC = backward(E, C, x, f["lse"], w, ignore_index, softcap)
+        keep = None
+    return {"loss": f["loss"], "lse": f["lse"], "count": f["count"], "dE": dE, "dC": dC, "keep": keep}
 
 
 def vocab_logit_sums(E, C, x, ignore_index=IGNORE_INDEX):

@@ -479,3 +479,51 @@ def test_compacting_ignored_rows_changes_only_the_tiling(rng):
                                              16, 16, eps=1e-3)
     assert np.array_equal(keep, keep_c) and np.array_equal(b_dC, c_dC)
     assert np.array_equal(b_dE[keep_rows], c_dE) and np.all(b_dE[x == -100] == 0.0)
+
+
+# ------------------------------------------------------------- single call
+@pytest.mark.parametrize("reduction", ["sum", "mean"])
+def test_single_call_matches_torch_autograd(rng, reduction):
+    """Unfiltered, the single call's loss and gradients are those of torch's
+    cross_entropy on materialised fp64 logits (unit upstream gradient)."""
+    E, C, x = _problem(rng, 40, 12, 70, scale=0.7, ignore=(3, 17))
+    out = O.loss_and_grad(E, C, x, reduction=reduction)
+    Et, Ct = torch.tensor(E, requires_grad=True), torch.tensor(C, requires_grad=True)
+    ref = torch.nn.functional.cross_entropy(Et @ Ct.T, torch.tensor(x), ignore_index=-100, reduction=reduction)
+    ref.backward()
+    assert np.allclose(out["loss"], ref.item(), rtol=1e-12)
+    assert np.allclose(out["dE"], Et.grad.numpy(), rtol=1e-10, atol=1e-14)
+    assert np.allclose(out["dC"], Ct.grad.numpy(), rtol=1e-10, atol=1e-14)
+    assert out["count"] == 38
+
+
+def test_single_call_scales_linearly_with_the_upstream_gradient(rng):
+    """What the single call's backward does -- multiply by the upstream
+    gradient g -- is the gradient of g * loss (finite differences)."""
+    E, C, x = _problem(rng, 6, 4, 9, scale=0.8, ignore=(2,))
+    g = -1.7
+    out = O.loss_and_grad(E, C, x, reduction="mean")
+    h = 1e-6
+    for idx in [(0, 1), (3, 2), (5, 0)]:
+        E2 = E.copy()
+        E2[idx] += h
+        lp = O.loss_and_grad(E2, C, x, reduction="mean")["loss"]
+        E2[idx] -= 2 * h
+        lm = O.loss_and_grad(E2, C, x, reduction="mean")["loss"]
+        assert abs(g * (lp - lm) / (2 * h) - g * out["dE"][idx]) <= 1e-6
+
+
+def test_single_call_filter_tiles_keep_ignored_rows_in_place(rng):
+    """The single call keeps every row: with ignored rows between the others,
+    its filtered gradient is the uncompacted tiling's, not the compacted
+    one's."""
+    E, C, x = _problem(rng, 96, 12, 300, scale=3.0, ignore=tuple(range(0, 96, 3)))
+    out = O.loss_and_grad(E, C, x, reduction="sum", filter_eps=2e-2, BN=16, BV=16)
+    f = O.forward(E, C, x, reduction="sum")
+    w = O.row_weights(x, -100, "sum", 1.0, f["count"])
+    a = O.backward_filtered(E, C, x, f["lse"], w, 16, 16, 2e-2)
+    b = O.backward_filtered(E, C, x, f["lse"], w, 16, 16, 2e-2, compact_ignored=True)
+    assert np.array_equal(out["keep"], a[2]) and np.array_equal(out["dC"], a[1])
+    assert a[2].shape != b[2].shape
+    with pytest.raises(ValueError):
+        O.loss_and_grad(E, C, x, reduction="none")
