@@ -1,12 +1,14 @@
 """Benchmark of the Cut Cross-Entropy hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                    [--config qwen] [--filter on|off] [--vocab-sort]
+                    [--config qwen] [--filter on|off] [--vocab-sort] [--mode two-call|single]
 
 One step = cce_forward + cce_backward (every stage of the path: LSE GEMM with
 target capture, combine + reduction, target count, recompute + G + filter,
 dC GEMM, dE GEMM, dE finalise) over one batch of the seeded synthetic
-workload, inputs resident in HBM.  Prints one JSON line (rank 0).
+workload, inputs resident in HBM.  --mode single times the single call
+instead (cce_loss_and_grad: staged logits, no recompute).  Prints one JSON
+line (rank 0).
 
 Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
 and torch.cuda.synchronize() on both sides, CUDA events on the launching
@@ -206,13 +208,21 @@ def run_gpu(args, rank, world, local_rank):
     red = w.reduction
     g = torch.ones(N if red == "none" else 1, dtype=torch.float32, device=dev)
     ws_f = torch.empty(cce.forward_workspace_bytes(N, D, V), dtype=torch.uint8, device=dev)
-    ws_b = torch.empty(cce.backward_workspace_bytes(N, D, V, vocab_sort=sort), dtype=torch.uint8, device=dev)
+    single = args.mode == "single"
+    if single:
+        ws_b = torch.empty(cce.loss_and_grad_workspace_bytes(N, D, V), dtype=torch.uint8, device=dev)
+    else:
+        ws_b = torch.empty(cce.backward_workspace_bytes(N, D, V, vocab_sort=sort), dtype=torch.uint8, device=dev)
     dE = torch.empty_like(E)
     dC = torch.empty_like(C)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stats = torch.zeros(2, dtype=torch.int64, device=dev)
 
     def step():
+        if single:
+            loss, _, _, _ = cce.cce_loss_and_grad(E, C, xt, -100, red, eps, workspace=ws_b, dev_err=err,
+                                                  check_errors=False, lse=False, dE=dE, dC=dC)
+            return loss
         loss, lse = cce.cce_forward(E, C, xt, -100, red, workspace=ws_f, dev_err=err, check_errors=False)
         cce.cce_backward(E, C, xt, lse, g, -100, red, eps, workspace=ws_b, dev_err=err, check_errors=False,
                          dE=dE, dC=dC, vocab_sort=sort)
@@ -224,9 +234,13 @@ def run_gpu(args, rank, world, local_rank):
     # filter statistics and peak extra memory of one step (untimed)
     torch.cuda.reset_peak_memory_stats(dev)
     base = torch.cuda.memory_allocated(dev)
-    loss, lse = cce.cce_forward(E, C, xt, -100, red, dev_err=err, check_errors=False)
-    _, _, st = cce.cce_backward(E, C, xt, lse, g, -100, red, eps, dev_err=err, check_errors=False, stats=True,
-                                vocab_sort=sort)
+    if single:
+        loss, lse, _, _, st = cce.cce_loss_and_grad(E, C, xt, -100, red, eps, dev_err=err, check_errors=False,
+                                                    stats=True)
+    else:
+        loss, lse = cce.cce_forward(E, C, xt, -100, red, dev_err=err, check_errors=False)
+        _, _, st = cce.cce_backward(E, C, xt, lse, g, -100, red, eps, dev_err=err, check_errors=False,
+                                    stats=True, vocab_sort=sort)
     torch.cuda.synchronize()
     outputs = dE.numel() * 2 + dC.numel() * 2 + N * 4 + (N * 4 if red == "none" else 4) + 16
     peak_extra = torch.cuda.max_memory_allocated(dev) - base - outputs
@@ -270,7 +284,10 @@ def run_gpu(args, rank, world, local_rank):
         xd.copy_(xh, non_blocking=True)
         Ed.requires_grad_(True)
         Cd.requires_grad_(True)
-        loss = cce.linear_cross_entropy(Ed, Cd, xd, -100, red, eps, vocab_sort=sort)
+        if single:
+            loss = cce.fused_linear_cross_entropy(Ed, Cd, xd, -100, red, eps)
+        else:
+            loss = cce.linear_cross_entropy(Ed, Cd, xd, -100, red, eps, vocab_sort=sort)
         loss.backward()
         loss_h.copy_(loss.detach().reshape(1), non_blocking=True)
         Ed.requires_grad_(False)
@@ -296,8 +313,10 @@ def run_gpu(args, rank, world, local_rank):
     # take part (ignored rows are compacted away) and, for dC / dE, over the
     # filter tiles kept.
     n_part = int((x != W.IGNORE_INDEX).sum())
+    # the single call keeps every row (no compaction) and has no recompute
+    n_grad = N if single else n_part
     flops = {"fwd_lse_gemm": 2.0 * N * D * V, "bwd_recompute_g": 2.0 * n_part * D * V,
-             "bwd_grad_gemm": 4.0 * n_part * D * V * kept}
+             "bwd_grad_gemm": 4.0 * n_grad * D * V * kept}
     phase_rep = {}
     for name, ms in phases.ms.items():
         n_l = phases.launches[name]
@@ -314,7 +333,7 @@ def run_gpu(args, rank, world, local_rank):
     roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "peak_kind": f"sustained bf16 ({peak_src})",
                 "frac_of_burst_peak": round(achieved / peaks["bf16_tflops"], 4),
-                "traffic": recorded_traffic(dom, args.config),
+                "traffic": recorded_traffic(dom, args.config + ("-single" if single else "")),
                 "algorithmic_flops_per_launch": flops[dom] / launches_dom}
     total_flops = 8.0 * N * D * V
     out = {
@@ -323,6 +342,7 @@ def run_gpu(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{WORKLOAD_NAMES[args.config]} N={N} D={D} V={V}", "N": N, "D": D, "V": V,
                    "reduction": red, "filter_eps": eps, "vocab_sort": sort, "ignore_frac": w.ignore_frac,
+                   "mode": "single call (cce_loss_and_grad)" if single else "two calls (cce_forward + cce_backward)",
                    "l2": f"inputs larger than L2 (C is {C.numel() * 2 / 1e6:.0f} MB)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         # the pages' metric: 8 N D V over all N tokens, whatever the filter or
@@ -382,12 +402,16 @@ def main(argv=None):
     ap.add_argument("--filter", choices=("on", "off"), default=None)
     ap.add_argument("--vocab-sort", action="store_true",
                     help="filter over the vocabulary sorted by average logit")
+    ap.add_argument("--mode", choices=("two-call", "single"), default="two-call",
+                    help="two-call: cce_forward + cce_backward; single: cce_loss_and_grad")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.filter is None:
         args.filter = W.ALL_CONFIGS[args.config].filter_modes[0]
+    if args.mode == "single" and (args.vocab_sort or W.ALL_CONFIGS[args.config].reduction == "none"):
+        ap.error("--mode single takes neither --vocab-sort nor a workload with reduction 'none'")
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

@@ -243,6 +243,44 @@ cce_status cce_vocab_logit_sums(const void* E, const void* C, const int64_t* x, 
 cce_status cce_vocab_order(const float* keys, int64_t V, int32_t* perm, void* workspace, size_t ws_bytes,
                            void* stream);
 
+/*
+ * Single call: the loss and both gradients in one pass ("fused-linear-cross-
+ * entropy" page, section "2. Fused Linear Cross-Entropy (FLCE)": per token
+ * chunk, the logits, then loss and dlogits = softmax - onehot, then
+ * dx = dlogits C and dw += dlogits^T x; the autograd backward only scales).
+ * dE and dC are the gradients of the reduced loss for a unit upstream
+ * gradient; multiply them by the real one with cce_scale_grads (both are
+ * linear in it).  Only CCE_RED_SUM and CCE_RED_MEAN (a scalar upstream
+ * gradient); CCE_RED_NONE returns CCE_ERR_ARG.
+ *
+ * Rows are processed in chunks of Nc tokens (a multiple of 256) whose logits,
+ * staged as fp16 [Nc][V rounded up to 256] (each logit minus its row's max
+ * over a 256-column tile), fit in max_staging_bytes (0: 2 GiB; at least one
+ * 256-row chunk).  Nothing is recomputed: the chunk's logits are computed
+ * once (6 N D V flops in all, against 8 N D V for cce_forward +
+ * cce_backward), at the cost of the staging traffic.  The filter (filter_eps,
+ * filter_flags as in cce_backward_ex; CCE_SORT_VOCAB is not accepted) works on
+ * tiles of 128 consecutive rows, ignored rows included (every row is kept),
+ * x 128 vocabulary entries.  With more than one chunk dC is accumulated in an
+ * fp32 buffer in the workspace; dE always goes through fp32 slabs.
+ *
+ *   loss   [1] fp32 (written).   lse  [N] fp32 (written) or NULL.
+ *   dE     [N, D] bf16, dC [V, D] bf16 (written; ignored rows of dE are +0).
+ *   workspace >= cce_loss_and_grad_workspace_bytes(N, D, V, max_staging_bytes).
+ *   dev_stats  optional device int64[2]: {tiles, skipped tiles} over all chunks.
+ * Checks and status codes as for the other calls.  Deterministic.
+ */
+size_t cce_loss_and_grad_workspace_bytes(int64_t N, int64_t D, int64_t V, size_t max_staging_bytes);
+cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int64_t N, int64_t D, int64_t V,
+                             int64_t ignore_index, int reduction, float softcap, float filter_eps, int filter_flags,
+                             size_t max_staging_bytes, float* loss, float* lse, void* dE, void* dC, void* workspace,
+                             size_t ws_bytes, int32_t* dev_err, int64_t* dev_stats, void* stream);
+
+/* dE *= g and dC *= g for bf16 arrays of nE and nC elements (multiples of 8,
+ * 16-byte aligned), g = *grad_out (device fp32); nothing is written when
+ * g == 1.  The backward of the single call. */
+cce_status cce_scale_grads(void* dE, int64_t nE, void* dC, int64_t nC, const float* grad_out, void* stream);
+
 /* Memory accounting (host arithmetic, no GPU).  Reproduces the page's memory
  * table ("Cut Cross-Entropy: Training Loss Without the Logit Matrix ...",
  * section "The memory numbers hold up"): the fp32 N x V logit buffer that the
@@ -284,8 +322,10 @@ uint64_t cce_kernel_launch_count(void);
  * Phases: 0 fwd_lse_gemm, 1 fwd_combine, 2 bwd_prep, 3 bwd_recompute_g,
  * 4 bwd_grad_gemm (dC and dE of a vocabulary chunk, one launch), 5 bwd_finalize,
  * 6 bwd_vocab_sort (with CCE_SORT_VOCAB: sums, order, target remap, and the
- * per-chunk gather of C). */
-#define CCE_NUM_PHASES 7
+ * per-chunk gather of C), 7 single_g_pass (cce_loss_and_grad: staged logits to
+ * G; its logit GEMMs count as phase 0, combines as 1, row count as 2,
+ * gradient GEMMs as 4, finalisation as 5). */
+#define CCE_NUM_PHASES 8
 cce_status cce_profile_enable(int enable);
 cce_status cce_profile_reset(void);
 cce_status cce_profile_read(double* ms /* host [CCE_NUM_PHASES] */, int64_t* launches /* host [CCE_NUM_PHASES] */);

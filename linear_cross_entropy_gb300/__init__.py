@@ -30,7 +30,8 @@ FILTER_EPS = 2.0 ** -12  # finfo(bf16).eps / 32
 __all__ = [
     "linear_cross_entropy", "cce_forward", "cce_backward", "CCEError", "FILTER_EPS",
     "forward_workspace_bytes", "backward_workspace_bytes", "memory_report", "kernel_launch_count",
-    "Profiler", "vocab_logit_sums", "vocab_order",
+    "Profiler", "vocab_logit_sums", "vocab_order", "cce_loss_and_grad", "fused_linear_cross_entropy",
+    "loss_and_grad_workspace_bytes",
 ]
 
 _lib.load()
@@ -188,6 +189,84 @@ def linear_cross_entropy(E, C, x, ignore_index=-100, reduction="mean", filter_ep
     vocab_sort filters over the vocabulary sorted by average logit."""
     return LinearCrossEntropyFunction.apply(E, C, x, ignore_index, reduction, filter_eps, filter_outputs,
                                             softcap, vocab_sort)
+
+
+def loss_and_grad_workspace_bytes(N, D, V, max_staging_bytes=0) -> int:
+    return int(_lib.load().cce_loss_and_grad_workspace_bytes(N, D, V, int(max_staging_bytes)))
+
+
+def cce_loss_and_grad(E, C, x, ignore_index=-100, reduction="mean", filter_eps=FILTER_EPS, *,
+                      filter_outputs="both", softcap=0.0, max_staging_bytes=0, stream=None, check_errors=True,
+                      workspace=None, dev_err=None, stats=False, lse=True, dE=None, dC=None):
+    """The single call: (loss, lse, dE, dC) or, with stats=True, also
+    {tiles, skipped}.  dE and dC are the gradients of the reduced loss for a
+    unit upstream gradient.  reduction: "sum" or "mean".  lse=False skips
+    writing the per-row LSE (returns None for it)."""
+    _check_inputs(E, C, x)
+    if reduction not in ("sum", "mean"):
+        raise ValueError("the single call supports reduction 'sum' and 'mean'")
+    N, D = E.shape
+    V = C.shape[0]
+    lib = _lib.load()
+    dev = E.device
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    lse_t = torch.empty(N, dtype=torch.float32, device=dev) if lse else None
+    if dE is None:
+        dE = torch.empty_like(E)
+    if dC is None:
+        dC = torch.empty_like(C)
+    need = int(lib.cce_loss_and_grad_workspace_bytes(N, D, V, int(max_staging_bytes)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    if dev_err is None:
+        dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
+    st_t = torch.zeros(2, dtype=torch.int64, device=dev) if stats else None
+    with torch.cuda.device(dev):
+        st = lib.cce_loss_and_grad(_ptr(E), _ptr(C), _ptr(x), N, D, V, int(ignore_index), RED[reduction],
+                                   float(softcap), float(filter_eps), FILTER_OUTPUTS[filter_outputs],
+                                   int(max_staging_bytes), _ptr(loss), _ptr(lse_t), _ptr(dE), _ptr(dC),
+                                   _ptr(workspace), workspace.numel(), _ptr(dev_err), _ptr(st_t),
+                                   _stream_handle(stream))
+    _lib.check(st, "cce_loss_and_grad")
+    if check_errors:
+        _raise_dev_err(dev_err)
+    out = (loss.reshape(()), lse_t, dE, dC)
+    if stats:
+        s = st_t.tolist()
+        return out + ({"tiles": s[0], "skipped": s[1]},)
+    return out
+
+
+class FusedLinearCrossEntropyFunction(torch.autograd.Function):
+    """The loss and both gradients come from one library call in the forward;
+    the backward only multiplies them by the upstream gradient."""
+
+    @staticmethod
+    def forward(ctx, E, C, x, ignore_index, reduction, filter_eps, filter_outputs, softcap, max_staging_bytes):
+        loss, _, dE, dC = cce_loss_and_grad(E, C, x, ignore_index, reduction, filter_eps,
+                                            filter_outputs=filter_outputs, softcap=softcap,
+                                            max_staging_bytes=max_staging_bytes, lse=False)
+        ctx.save_for_backward(dE, dC)
+        return loss
+
+    @staticmethod
+    def backward(ctx, grad_loss):
+        dE, dC = ctx.saved_tensors
+        g = grad_loss.to(device=dE.device, dtype=torch.float32).contiguous().reshape(1)
+        with torch.cuda.device(dE.device):
+            st = _lib.load().cce_scale_grads(_ptr(dE), dE.numel(), _ptr(dC), dC.numel(), _ptr(g),
+                                             _stream_handle(None))
+        _lib.check(st, "cce_scale_grads")
+        return dE, dC, None, None, None, None, None, None, None
+
+
+def fused_linear_cross_entropy(E, C, x, ignore_index=-100, reduction="mean", filter_eps=FILTER_EPS,
+                               filter_outputs="both", softcap=0.0, max_staging_bytes=0):
+    """linear_cross_entropy computed by the single call: loss and gradients in
+    the forward (token chunks of staged logits, no recompute), the backward
+    only scales.  reduction "sum" or "mean"."""
+    return FusedLinearCrossEntropyFunction.apply(E, C, x, ignore_index, reduction, filter_eps, filter_outputs,
+                                                 softcap, max_staging_bytes)
 
 
 def vocab_logit_sums(E, C, x, ignore_index=-100, *, stream=None):

@@ -21,7 +21,7 @@ STATUS_NAMES = {
 RED = {"none": 0, "sum": 1, "mean": 2}
 DEVERR_TARGET_RANGE = 1
 DEVERR_TIMEOUT = 2
-NUM_PHASES = 7
+NUM_PHASES = 8
 SORT_VOCAB = 4
 
 
@@ -81,6 +81,13 @@ def load() -> ctypes.CDLL:
     lib.cce_vocab_logit_sums.restype = ctypes.c_int
     lib.cce_vocab_order.argtypes = [vp, i64, vp, vp, sz, vp]
     lib.cce_vocab_order.restype = ctypes.c_int
+    lib.cce_loss_and_grad_workspace_bytes.argtypes = [i64, i64, i64, sz]
+    lib.cce_loss_and_grad_workspace_bytes.restype = sz
+    lib.cce_loss_and_grad.argtypes = [vp, vp, vp, i64, i64, i64, i64, ctypes.c_int, ctypes.c_float, ctypes.c_float,
+                                      ctypes.c_int, sz, vp, vp, vp, vp, vp, sz, vp, vp, vp]
+    lib.cce_loss_and_grad.restype = ctypes.c_int
+    lib.cce_scale_grads.argtypes = [vp, i64, vp, i64, vp, vp]
+    lib.cce_scale_grads.restype = ctypes.c_int
     lib.cce_forward_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, ctypes.c_int, vp, vp, vp, vp]
     lib.cce_forward_noalloc.restype = ctypes.c_int
     lib.cce_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint32, vp]

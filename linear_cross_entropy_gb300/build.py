@@ -22,7 +22,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcce.so")
-SOURCES = ("cce_api.cu", "gemm_kernels.cu", "cce_noalloc.cu", "cce_sort.cu")
+SOURCES = ("cce_api.cu", "gemm_kernels.cu", "cce_noalloc.cu", "cce_sort.cu", "cce_flce.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

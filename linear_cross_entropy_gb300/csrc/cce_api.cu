@@ -347,6 +347,65 @@ BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V, bool sort = false) {
   return L;
 }
 
+// Single call: token chunks of Nc rows (a multiple of 256) whose staged
+// logits, fp16 [Nc][Vp] with Vp = V rounded up to 256, fit in max_staging
+// bytes (at least one 256-row chunk); per chunk the forward partials, the
+// 32-column chunk maxima and the survival maps; dE in de_splits fp32 slabs of
+// roundup(N, 128) rows; with more than one chunk an fp32 dC accumulator.
+constexpr size_t FLCE_STAGING_DEFAULT = size_t(2) << 30;
+
+struct FlceLayout {
+  size_t counters, count, part_m, part_s, tgt, lse, blk_sum, blk_cnt, stage, mtile, bitmap, bitmapT, deacc, dcacc,
+      total;
+  int64_t Nc, nchunks, Vp, bm_ld, slab, n_tiles, bn, kps;
+  int S, Sde, nblk;
+};
+
+FlceLayout flce_layout(int64_t N, int64_t D, int64_t V, size_t max_staging) {
+  FlceLayout L{};
+  if (max_staging == 0) max_staging = FLCE_STAGING_DEFAULT;
+  L.Vp = cdiv(V, 256) * 256;
+  const int64_t fit = static_cast<int64_t>(max_staging / (static_cast<size_t>(L.Vp) * 2)) / 256 * 256;
+  L.Nc = std::min(std::max<int64_t>(256, fit), cdiv(N, 256) * 256);
+  L.nchunks = cdiv(N, L.Nc);
+  L.bm_ld = cdiv(V, 128);
+  L.slab = cdiv(N, 128) * 128;
+  L.S = fwd_splits(L.Nc, V);
+  L.nblk = static_cast<int>(cdiv(N, COMBINE_THREADS));
+  // dE: split the vocabulary (K) so that no dE tile is much longer than the
+  // average work per SM of a chunk's gradient launch
+  L.bn = grad_tile_width(D, D % 64 == 0 ? 64 : 32);
+  L.n_tiles = cdiv(D, L.bn);
+  const int64_t nb = L.Nc / BM, kde = cdiv(V, BK);
+  const double units = static_cast<double>(nb * L.n_tiles) * kde + static_cast<double>(cdiv(V, BM) * L.n_tiles) * 2 * nb;
+  const double avg = std::max(1.0, units / REF_SMS);
+  L.Sde = static_cast<int>(std::min<double>(8.0, std::max(1.0, std::ceil(kde / avg))));
+  L.kps = cdiv(cdiv(kde, L.Sde), 2) * 2;
+  L.Sde = static_cast<int>(cdiv(kde, L.kps));
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes, ALIGN);
+    return at;
+  };
+  L.counters = take(sizeof(int) * 2 * static_cast<size_t>(L.nchunks));
+  L.count = take(sizeof(int));
+  L.part_m = take(sizeof(float) * L.S * static_cast<size_t>(L.Nc));
+  L.part_s = take(sizeof(float) * L.S * static_cast<size_t>(L.Nc));
+  L.tgt = take(sizeof(float) * static_cast<size_t>(L.Nc));
+  L.lse = take(sizeof(float) * static_cast<size_t>(N));
+  L.blk_sum = take(sizeof(double) * L.nblk);
+  L.blk_cnt = take(sizeof(int) * L.nblk);
+  L.stage = take(static_cast<size_t>(L.Nc) * L.Vp * 2);
+  L.mtile = take(sizeof(float) * static_cast<size_t>(L.Vp / 32) * L.Nc);
+  L.bitmap = take(static_cast<size_t>(L.Nc / BM) * L.bm_ld);
+  L.bitmapT = take(static_cast<size_t>(L.Nc / BM) * L.bm_ld);
+  L.deacc = take(sizeof(float) * static_cast<size_t>(L.Sde) * L.slab * D);
+  L.dcacc = take(L.nchunks > 1 ? sizeof(float) * static_cast<size_t>(V) * D : 0);
+  L.total = o;
+  return L;
+}
+
 bool sizes_ok(int64_t N, int64_t D, int64_t V) {
   const int64_t lim = int64_t(1) << 31;
   return N >= 1 && N < lim && V >= 1 && V < lim && D >= 8 && D < lim && D % 8 == 0;
@@ -854,6 +913,200 @@ cce_status cce_backward_ex(const void* E, const void* C, const int64_t* x, const
   return CCE_OK;
 }
 
+size_t cce_loss_and_grad_workspace_bytes(int64_t N, int64_t D, int64_t V, size_t max_staging_bytes) {
+  if (!sizes_ok(N, D, V)) return 0;
+  return flce_layout(N, D, V, max_staging_bytes).total;
+}
+
+cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int64_t N, int64_t D, int64_t V,
+                             int64_t ignore_index, int reduction, float softcap, float filter_eps, int filter_flags,
+                             size_t max_staging_bytes, float* loss, float* lse, void* dE, void* dC, void* workspace,
+                             size_t ws_bytes, int32_t* dev_err, int64_t* dev_stats, void* stream) {
+  if (!E || !C || !x || !loss || !dE || !dC || !workspace) return CCE_ERR_NULL;
+  if (!sizes_ok(N, D, V)) return CCE_ERR_SHAPE;
+  if (!aligned16(E) || !aligned16(C) || !aligned16(dE) || !aligned16(dC) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(x) & 7u) || (reinterpret_cast<uintptr_t>(loss) & 3u) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(dev_stats) & 7u))
+    return CCE_ERR_ALIGN;
+  if (reduction != CCE_RED_SUM && reduction != CCE_RED_MEAN) return CCE_ERR_ARG;
+  if (!(filter_eps >= 0.0f) || !std::isfinite(filter_eps)) return CCE_ERR_ARG;
+  if (filter_flags & ~CCE_FILTER_BOTH) return CCE_ERR_ARG;
+  if (!(softcap >= 0.0f) || !std::isfinite(softcap)) return CCE_ERR_ARG;
+  const FlceLayout W = flce_layout(N, D, V, max_staging_bytes);
+  if (ws_bytes < W.total) return CCE_ERR_WORKSPACE;
+  int sms = 0;
+  cce_status st = device_check(&sms);
+  if (st != CCE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* counters = reinterpret_cast<int*>(ws + W.counters);
+  int* count = reinterpret_cast<int*>(ws + W.count);
+  float* lse_all = lse ? lse : reinterpret_cast<float*>(ws + W.lse);
+  double* blk_sum = reinterpret_cast<double*>(ws + W.blk_sum);
+  int* blk_cnt = reinterpret_cast<int*>(ws + W.blk_cnt);
+  uint16_t* stage = reinterpret_cast<uint16_t*>(ws + W.stage);
+  float* mtile = reinterpret_cast<float*>(ws + W.mtile);
+  uint8_t* bitmap = ws + W.bitmap;
+  uint8_t* bitmapT = ws + W.bitmapT;
+  float* deacc = reinterpret_cast<float*>(ws + W.deacc);
+  float* dcacc = reinterpret_cast<float*>(ws + W.dcacc);
+  const bool filter_de = (filter_flags & CCE_FILTER_DE) != 0, filter_dc = (filter_flags & CCE_FILTER_DC) != 0;
+  const bool multi = W.nchunks > 1;
+  {
+    PhaseScope ps(2, s);
+    int launched = 0;
+    cudaError_t e = cudaMemsetAsync(counters, 0, sizeof(int) * 2 * static_cast<size_t>(W.nchunks), s);
+    if (e == cudaSuccess && dev_stats) e = cudaMemsetAsync(dev_stats, 0, 2 * sizeof(int64_t), s);
+    if (e == cudaSuccess) e = launch_count_rows(x, N, V, static_cast<long long>(ignore_index), count, s, &launched);
+    g_launches += static_cast<uint64_t>(launched);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  const bool b3d = D % 64 == 0;
+  for (int64_t c = 0; c < W.nchunks; ++c) {
+    const int64_t r0 = c * W.Nc, rows = std::min(W.Nc, N - r0);
+    const int64_t nb = cdiv(rows, BM);
+    const uint16_t* Ec = static_cast<const uint16_t*>(E) + r0 * D;
+    // (1) logits of the chunk: fold + target capture + staging
+    GemmArgs f;
+    std::memset(&f, 0, sizeof(f));
+    bool ok = make_tmap(&f.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Ec, D, rows, D, BK, BM) &&
+              make_tmap(&f.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, D, V, D, BK, BN) &&
+              make_tmap(&f.tmOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, stage, W.Vp, rows, W.Vp, 64, 32);
+    if (!ok) return CCE_ERR_CUDA;
+    f.N = static_cast<int>(rows);
+    f.D = static_cast<int>(D);
+    f.V = static_cast<int>(V);
+    f.n_blocks = static_cast<int>(nb);
+    f.k_blocks = static_cast<int>(cdiv(D, BK));
+    f.splits = W.S;
+    f.v_tiles = static_cast<int>(cdiv(V, BN));
+    f.items = f.n_blocks * f.splits;
+    f.x = x + r0;
+    f.ignore_index = ignore_index;
+    f.part_m = reinterpret_cast<float*>(ws + W.part_m);
+    f.part_s = reinterpret_cast<float*>(ws + W.part_s);
+    f.tgt = reinterpret_cast<float*>(ws + W.tgt);
+    f.mtile = mtile;
+    f.softcap = softcap;
+    f.inv_softcap = softcap > 0.0f ? 1.0f / softcap : 0.0f;
+    f.dev_err = dev_err;
+    f.counter = counters + 2 * c;
+    cudaError_t e;
+    {
+      PhaseScope ps(0, s);
+      e = launch_gemm(MODE_FWD_STAGE, f, std::min(f.items, sms), s);
+      g_launches++;
+      if (e != cudaSuccess) return cuda_status(e);
+    }
+    {  // (2) LSE of the chunk's rows and their block sums of the loss
+      PhaseScope ps(1, s);
+      combine_kernel<<<static_cast<unsigned>(cdiv(rows, COMBINE_THREADS)), COMBINE_THREADS, 0, s>>>(
+          f.part_m, f.part_s, f.tgt, x + r0, f.N, W.S, f.V, static_cast<long long>(ignore_index), reduction,
+          lse_all + r0, nullptr, blk_sum + r0 / COMBINE_THREADS, blk_cnt + r0 / COMBINE_THREADS, dev_err);
+      g_launches++;
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return cuda_status(e);
+    }
+    {  // (3) staged logits -> G-hat (bf16, in place) and the filter votes
+      PhaseScope ps(7, s);
+      int launched = 0;
+      e = launch_gpass(stage, W.Vp, mtile, rows, V, x + r0, static_cast<long long>(ignore_index), lse_all + r0, count,
+                       reduction, softcap, filter_eps, !(filter_de && filter_dc), bitmap, bitmapT, W.bm_ld, s,
+                       &launched);
+      g_launches += static_cast<uint64_t>(launched);
+      if (e != cudaSuccess) return cuda_status(e);
+    }
+    // (4) dE rows of the chunk (K = the whole vocabulary, in W.Sde ranges)
+    //     and its contribution to dC (K = the chunk's rows)
+    GemmArgs r;
+    std::memset(&r, 0, sizeof(r));
+    ok = make_tmap_mn3(&r.tmA, stage, W.Vp, rows, BM / 64) &&
+         make_tmap(&r.tmA2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, stage, W.Vp, rows, W.Vp, 64, BM);
+    if (b3d) {
+      ok = ok && make_tmap_mn3(&r.tmB, Ec, D, rows) && make_tmap_mn3(&r.tmB2, C, D, V);
+    } else {
+      ok = ok && make_tmap(&r.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Ec, D, rows, D, 64, 64) &&
+           make_tmap(&r.tmB2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, D, V, D, 64, 64);
+    }
+    if (multi) {
+      ok = ok && make_tmap(&r.tmOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dcacc, D, V, D, 32, 32);
+    } else {
+      ok = ok && make_tmap(&r.tmOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dC, D, V, D, 32, 32,
+                           CU_TENSOR_MAP_SWIZZLE_64B);
+    }
+    ok = ok && make_tmap(&r.tmOut2, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, deacc, D,
+                         static_cast<uint64_t>(W.Sde) * W.slab, D, 32, 32);
+    if (!ok) return CCE_ERR_CUDA;
+    r.N = static_cast<int>(rows);
+    r.D = static_cast<int>(D);
+    r.V = static_cast<int>(V);
+    r.n_blocks = static_cast<int>(nb);
+    r.x = x + r0;
+    r.ignore_index = ignore_index;
+    r.filter_de = filter_de ? 1 : 0;
+    r.filter_dc = filter_dc ? 1 : 0;
+    r.bitmap = bitmap;
+    r.bitmapT = bitmapT;
+    r.bm_ld = static_cast<int>(W.bm_ld);
+    r.dev_err = dev_err;
+    r.chunk_v0 = 0;
+    r.chunk_w = static_cast<int>(V);
+    r.c_row0 = 0;
+    r.b3d = b3d ? 1 : 0;
+    r.bn = static_cast<int>(W.bn);
+    r.n_tiles = static_cast<int>(W.n_tiles);
+    r.dc_m_tiles = static_cast<int>(cdiv(V, BM));
+    r.de_k_blocks = static_cast<int>(cdiv(V, BK));
+    r.de_splits = W.Sde;
+    r.de_kps = static_cast<int>(W.kps);
+    r.de_slab = static_cast<int>(W.slab);
+    r.de_row0 = static_cast<int>(r0);
+    r.first_chunk = 1;  // every dE slab row is written once
+    r.dc_f32 = multi ? 1 : 0;
+    r.dc_reduce = (multi && c > 0) ? 1 : 0;
+    r.dc_first = 2 * nb >= W.kps ? 1 : 0;  // longest tiles first
+    r.counter = counters + 2 * c + 1;
+    {
+      PhaseScope ps(4, s);
+      const int64_t items = (r.dc_m_tiles + nb * W.Sde) * r.n_tiles;
+      e = launch_gemm(MODE_GRAD, r, static_cast<int>(std::min<int64_t>(sms, items)), s);
+      g_launches++;
+      if (e != cudaSuccess) return cuda_status(e);
+    }
+    if (dev_stats) {
+      int launched = 0;
+      e = launch_stats_add(bitmap, nb, cdiv(V, 128), W.bm_ld, dev_stats, s, &launched);
+      g_launches += static_cast<uint64_t>(launched);
+      if (e != cudaSuccess) return cuda_status(e);
+    }
+  }
+  {
+    PhaseScope ps(5, s);
+    finish_loss_kernel<<<1, COMBINE_THREADS, 0, s>>>(blk_sum, blk_cnt, W.nblk, reduction, loss);
+    g_launches++;
+    int launched = 0;
+    cudaError_t e = launch_finalize_de_slabs(deacc, W.Sde, W.slab, N, D, dE, s, sms, &launched);
+    if (e == cudaSuccess && multi) e = launch_to_bf16(dcacc, V * D, dC, s, sms, &launched);
+    g_launches += static_cast<uint64_t>(launched);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return CCE_OK;
+}
+
+cce_status cce_scale_grads(void* dE, int64_t nE, void* dC, int64_t nC, const float* grad_out, void* stream) {
+  if (!dE || !dC || !grad_out) return CCE_ERR_NULL;
+  if (nE < 0 || nC < 0 || nE % 8 || nC % 8) return CCE_ERR_SHAPE;
+  if (!aligned16(dE) || !aligned16(dC) || (reinterpret_cast<uintptr_t>(grad_out) & 3u)) return CCE_ERR_ALIGN;
+  int sms = 0;
+  cce_status st = device_check(&sms);
+  if (st != CCE_OK) return st;
+  int launched = 0;
+  cudaError_t e = launch_scale_bf16(dE, nE, dC, nC, grad_out, static_cast<cudaStream_t>(stream), sms, &launched);
+  g_launches += static_cast<uint64_t>(launched);
+  return cuda_status(e);
+}
+
 cce_status cce_selftest_wait_timeout(int32_t* dev_err, uint32_t timeout_us, void* stream) {
   if (!dev_err) return CCE_ERR_NULL;
   if (timeout_us == 0 || timeout_us > 10000000u) return CCE_ERR_ARG;
@@ -908,7 +1161,7 @@ cce_status cce_profile_read(double* ms, int64_t* launches) {
 
 const char* cce_profile_phase_name(int phase) {
   static const char* names[CCE_NUM_PHASES] = {"fwd_lse_gemm",  "fwd_combine",  "bwd_prep",       "bwd_recompute_g",
-                                               "bwd_grad_gemm", "bwd_finalize", "bwd_vocab_sort"};
+                                               "bwd_grad_gemm", "bwd_finalize", "bwd_vocab_sort", "single_g_pass"};
   if (phase < 0 || phase >= CCE_NUM_PHASES) return "";
   return names[phase];
 }

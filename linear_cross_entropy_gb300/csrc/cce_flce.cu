@@ -1,0 +1,288 @@
+// Bandwidth-bound kernels of the single call (loss and both gradients in one
+// pass, "fused-linear-cross-entropy" page, section "2. Fused Linear
+// Cross-Entropy (FLCE)"): the forward GEMM of a token chunk has staged its
+// logits (fp16, minus each row's max over each 32-column chunk); here they
+// become the weighted logit gradient G-hat in bf16, in place, with the
+// 128 x 128 filter votes ("Cut Your Losses in Large-Vocabulary Language
+// Models", "Gradient Filtering").  Also: the count of rows that take part,
+// the dE / dC finalisation, the filter statistics and the scaling by the
+// upstream gradient.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/cce.h"
+#include "internal.h"
+
+namespace cce {
+namespace {
+
+constexpr float LOG2E_F = 1.4426950408889634f;
+
+__device__ __forceinline__ float ex2f(float v) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// Rows that take part: target in [0, V) and not ignore_index.  One block.
+__global__ void count_rows_kernel(const int64_t* __restrict__ x, int N, int V, long long ignore_index,
+                                  int* __restrict__ count) {
+  __shared__ int part[1024];
+  int c = 0;
+  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    const long long t = static_cast<long long>(x[i]);
+    c += (t != ignore_index && t >= 0 && t < V) ? 1 : 0;
+  }
+  part[threadIdx.x] = c;
+  __syncthreads();
+  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+    if (static_cast<int>(threadIdx.x) < w) part[threadIdx.x] += part[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *count = part[0];
+}
+
+// One 128-row x 128-column tile per block (256 threads: 16 threads of eight
+// columns per row, 16 rows per pass, 8 passes).  G = exp(a - LSE) - onehot
+// with a = staged value + the row's max over its 32-column chunk, computed as
+// exp2(h * log2e + c_row), c_row = (max - LSE) * log2e; rows that take no
+// part get c_row = -inf, so their G is 0.  The vote is any |G| >= eps
+// (unscaled G, before the softcap slope); the stored value is w * G * slope
+// in bf16.  A tile that both outputs skip is not written back (nothing reads
+// it).
+template <bool CAP>
+__global__ void __launch_bounds__(256, CAP ? 3 : 4) gpass_kernel(uint16_t* __restrict__ stage, int pitch,
+                                                    const float* __restrict__ mtile, int rows, int V,
+                                                    const int64_t* __restrict__ x, long long ignore_index,
+                                                    const float* __restrict__ lse, const int* __restrict__ count,
+                                                    int reduction, float softcap, float eps, int store_skipped,
+                                                    uint8_t* __restrict__ bitmap, uint8_t* __restrict__ bitmapT,
+                                                    int bm_ld, int n_blocks) {
+  const int vt = blockIdx.x, tb = blockIdx.y;
+  const int c8 = threadIdx.x & 15;
+  const int r_in = threadIdx.x >> 4;
+  const int col0 = vt * 128 + c8 * 8;
+  const bool ragged = col0 + 8 > V;  // only in the last column tile
+  const float w = reduction == CCE_RED_SUM ? 1.0f : 1.0f / static_cast<float>(max(*count, 1));
+  const float inv_cap = CAP ? 1.0f / softcap : 0.0f;
+  float amax = 0.0f;  // largest unscaled |G| this thread saw
+  uint32_t pk[8][4];  // the eight rows' results, bf16 pairs
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int row = tb * 128 + r_in + 16 * k;
+    const bool ok = row < rows;
+    const uint4 h = ok ? *reinterpret_cast<const uint4*>(stage + static_cast<size_t>(row) * pitch + col0)
+                       : make_uint4(0u, 0u, 0u, 0u);
+    const long long xr = ok ? static_cast<long long>(x[row]) : ignore_index;
+    const bool part = xr != ignore_index && xr >= 0 && xr < V;
+    const float m = ok ? mtile[static_cast<size_t>(col0 >> 5) * rows + row] : 0.0f;
+    const float cr = part ? (m - lse[row]) * LOG2E_F : -INFINITY;
+    const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
+    float g[8];
+    float sl[8];  // softcap slope 1 - tanh^2 (the staged value + m is the capped logit)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hw[j]));
+      g[2 * j] = ex2f(fmaf(f.x, LOG2E_F, cr));
+      g[2 * j + 1] = ex2f(fmaf(f.y, LOG2E_F, cr));
+      if constexpr (CAP) {
+        const float t0 = (f.x + m) * inv_cap, t1 = (f.y + m) * inv_cap;
+        sl[2 * j] = 1.0f - t0 * t0;
+        sl[2 * j + 1] = 1.0f - t1 * t1;
+      }
+    }
+    const long long rel = part ? xr - col0 : -1;
+    if (rel >= 0 && rel < 8) {  // the target column is one of these eight (one thread per row)
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j == rel) g[j] -= 1.0f;
+    }
+    if (ragged) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (col0 + j >= V) g[j] = 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      amax = fmaxf(amax, fmaxf(fabsf(g[2 * j]), fabsf(g[2 * j + 1])));
+      float a0 = w * g[2 * j], a1 = w * g[2 * j + 1];
+      if constexpr (CAP) {  // only where G != 0: columns past V stage +inf, whose slope is not a number
+        a0 = g[2 * j] != 0.0f ? a0 * sl[2 * j] : 0.0f;
+        a1 = g[2 * j + 1] != 0.0f ? a1 * sl[2 * j + 1] : 0.0f;
+      }
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(a0, a1);
+      std::memcpy(&pk[k][j], &b2, 4);
+    }
+  }
+  const bool keep = __syncthreads_or(!(eps > 0.0f) || amax >= eps) != 0;  // eps = 0: nothing is skipped
+  if (keep || store_skipped) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int row = tb * 128 + r_in + 16 * k;
+      if (row < rows)
+        *reinterpret_cast<uint4*>(stage + static_cast<size_t>(row) * pitch + col0) =
+            make_uint4(pk[k][0], pk[k][1], pk[k][2], pk[k][3]);
+    }
+  }
+  if (threadIdx.x == 0) {
+    bitmap[static_cast<size_t>(tb) * bm_ld + vt] = keep ? 1 : 0;
+    bitmapT[static_cast<size_t>(vt) * n_blocks + tb] = keep ? 1 : 0;
+  }
+}
+
+// dE[r] = bf16(sum over the S slabs of acc[s * slab + r]), slabs in order.
+__global__ void finalize_de_slabs_kernel(const float4* __restrict__ acc, int S, int slab, int N, int D,
+                                         uint2* __restrict__ dE) {
+  const size_t per_row = static_cast<size_t>(D) / 4;
+  const size_t total = static_cast<size_t>(N) * per_row;
+  const size_t slab4 = static_cast<size_t>(slab) * per_row;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    float4 v = acc[i];
+    for (int s = 1; s < S; ++s) {
+      const float4 u = acc[s * slab4 + i];
+      v.x += u.x;
+      v.y += u.y;
+      v.z += u.z;
+      v.w += u.w;
+    }
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 out;
+    std::memcpy(&out.x, &lo, 4);
+    std::memcpy(&out.y, &hi, 4);
+    dE[i] = out;
+  }
+}
+
+// fp32 -> bf16 (round to nearest even), four values per thread.
+__global__ void to_bf16_kernel(const float4* __restrict__ src, size_t n4, uint2* __restrict__ dst) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const float4 v = src[i];
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 out;
+    std::memcpy(&out.x, &lo, 4);
+    std::memcpy(&out.y, &hi, 4);
+    dst[i] = out;
+  }
+}
+
+// stats[0] += tiles, stats[1] += skipped tiles of one chunk's survival map
+// (nb rows of ncols bytes, pitch bm_ld).  One block; launches run in stream
+// order, so the sums are deterministic.
+__global__ void stats_add_kernel(const uint8_t* __restrict__ bitmap, int nb, int ncols, int bm_ld,
+                                 int64_t* __restrict__ stats) {
+  __shared__ long long sz[1024];
+  const long long n = static_cast<long long>(nb) * ncols;
+  long long z = 0;
+  for (long long i = threadIdx.x; i < n; i += blockDim.x) z += bitmap[(i / ncols) * bm_ld + (i % ncols)] == 0 ? 1 : 0;
+  sz[threadIdx.x] = z;
+  __syncthreads();
+  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+    if (static_cast<int>(threadIdx.x) < w) sz[threadIdx.x] += sz[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    stats[0] += n;
+    stats[1] += sz[0];
+  }
+}
+
+// x *= *g for bf16 arrays (eight values per thread); nothing when *g == 1.
+__global__ void scale_bf16_kernel(uint4* __restrict__ a, size_t n8a, uint4* __restrict__ b, size_t n8b,
+                                  const float* __restrict__ g) {
+  const float s = *g;
+  if (s == 1.0f) return;
+  const size_t total = n8a + n8b;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    uint4* p = i < n8a ? a + i : b + (i - n8a);
+    uint4 v = *p;
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      __nv_bfloat162 h;
+      std::memcpy(&h, &w[j], 4);
+      const float2 f = __bfloat1622float2(h);
+      h = __floats2bfloat162_rn(f.x * s, f.y * s);
+      std::memcpy(&w[j], &h, 4);
+    }
+    *p = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+int grid_cap(size_t work, int per_block, int cap) {
+  return static_cast<int>(std::max<size_t>(1, std::min<size_t>(static_cast<size_t>(cap), (work + per_block - 1) / per_block)));
+}
+
+}  // namespace
+
+cudaError_t launch_count_rows(const int64_t* x, int64_t N, int64_t V, long long ignore_index, int* count,
+                              cudaStream_t s, int* launches) {
+  count_rows_kernel<<<1, 1024, 0, s>>>(x, static_cast<int>(N), static_cast<int>(V), ignore_index, count);
+  ++*launches;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gpass(uint16_t* stage, int64_t pitch, const float* mtile, int64_t rows, int64_t V,
+                         const int64_t* x, long long ignore_index, const float* lse, const int* count, int reduction,
+                         float softcap, float eps, bool store_skipped, uint8_t* bitmap, uint8_t* bitmapT,
+                         int64_t bm_ld, cudaStream_t s, int* launches) {
+  const int nb = static_cast<int>((rows + 127) / 128);
+  const dim3 grid(static_cast<unsigned>((V + 127) / 128), static_cast<unsigned>(nb));
+  if (softcap > 0.0f) {
+    gpass_kernel<true><<<grid, 256, 0, s>>>(stage, static_cast<int>(pitch), mtile, static_cast<int>(rows),
+                                            static_cast<int>(V), x, ignore_index, lse, count, reduction, softcap, eps,
+                                            store_skipped ? 1 : 0, bitmap, bitmapT, static_cast<int>(bm_ld), nb);
+  } else {
+    gpass_kernel<false><<<grid, 256, 0, s>>>(stage, static_cast<int>(pitch), mtile, static_cast<int>(rows),
+                                             static_cast<int>(V), x, ignore_index, lse, count, reduction, softcap,
+                                             eps, store_skipped ? 1 : 0, bitmap, bitmapT, static_cast<int>(bm_ld), nb);
+  }
+  ++*launches;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize_de_slabs(const float* acc, int S, int64_t slab, int64_t N, int64_t D, void* dE,
+                                     cudaStream_t s, int sms, int* launches) {
+  const size_t n4 = static_cast<size_t>(N) * D / 4;
+  finalize_de_slabs_kernel<<<grid_cap(n4, 256, sms * 8), 256, 0, s>>>(
+      reinterpret_cast<const float4*>(acc), S, static_cast<int>(slab), static_cast<int>(N), static_cast<int>(D),
+      static_cast<uint2*>(dE));
+  ++*launches;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_to_bf16(const float* src, int64_t n, void* dst, cudaStream_t s, int sms, int* launches) {
+  const size_t n4 = static_cast<size_t>(n) / 4;
+  to_bf16_kernel<<<grid_cap(n4, 256, sms * 8), 256, 0, s>>>(reinterpret_cast<const float4*>(src), n4,
+                                                            static_cast<uint2*>(dst));
+  ++*launches;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_stats_add(const uint8_t* bitmap, int64_t nb, int64_t ncols, int64_t bm_ld, int64_t* stats,
+                             cudaStream_t s, int* launches) {
+  stats_add_kernel<<<1, 1024, 0, s>>>(bitmap, static_cast<int>(nb), static_cast<int>(ncols), static_cast<int>(bm_ld),
+                                      stats);
+  ++*launches;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale_bf16(void* a, int64_t na, void* b, int64_t nb, const float* g, cudaStream_t s, int sms,
+                              int* launches) {
+  const size_t n8a = static_cast<size_t>(na) / 8, n8b = static_cast<size_t>(nb) / 8;
+  scale_bf16_kernel<<<grid_cap(n8a + n8b, 256, sms * 8), 256, 0, s>>>(static_cast<uint4*>(a), n8a,
+                                                                      static_cast<uint4*>(b), n8b, g);
+  ++*launches;
+  return cudaGetLastError();
+}
+
+}  // namespace cce

@@ -28,6 +28,15 @@
 //              stream order, so the result is deterministic.  K-blocks of
 //              skipped filter tiles are not loaded and issue no MMA.
 //
+//   MODE_FWD_STAGE  MODE_FWD whose epilogue also writes each 32-column logit
+//              chunk, minus its per-row max, as fp16 to a staging buffer (and
+//              the max to mtile) for the single call ("fused-linear-cross-
+//              entropy" page, "2. Fused Linear Cross-Entropy (FLCE)": the
+//              chunk's logits are kept for the gradient instead of being
+//              recomputed).  There MODE_GRAD also covers a token chunk over
+//              the whole vocabulary: dE tiles split K into ranges written to
+//              separate fp32 slabs, dC tiles may write fp32 (store or add).
+//
 // Roles (192 threads): warp 0 lane 0 is the scheduler and TMA producer (a
 // 4-stage ring of 48 KiB stages); warp 1 owns TMEM (512 columns = two 128x256
 // fp32 accumulators) and lane 0 issues tcgen05.mma; warps 2..5 are the
@@ -38,6 +47,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 
 #include "gemm_args.h"
@@ -49,7 +59,7 @@ struct Tile {
   int kind;   // KIND_MAIN (FWD, BWD_G), KIND_DC or KIND_DE (GRAD)
   int m;      // A-row block (128)
   int n;      // B-row block (256) or output column block
-  int split;  // FWD
+  int split;  // FWD: vocabulary split; GRAD dE: K range
   bool first, last;  // FWD: first / last tile of a (row block, split) unit
 };
 
@@ -67,12 +77,12 @@ __device__ __forceinline__ Dims dims_of(const GemmArgs& a) {
   Dims d;
   d.nb = (n + BM - 1) / BM;
   d.dc_kb = (n + BK - 1) / BK;
-  if constexpr (MODE == MODE_FWD) {
+  if constexpr (MODE == MODE_FWD || MODE == MODE_FWD_STAGE) {
     d.items = a.items;
   } else if constexpr (MODE == MODE_BWD_G) {
     d.items = d.nb * a.v_tiles;
   } else {
-    d.items = (a.dc_m_tiles + d.nb) * a.n_tiles;
+    d.items = (a.dc_m_tiles + d.nb * max(a.de_splits, 1)) * a.n_tiles;
   }
   return d;
 }
@@ -80,7 +90,7 @@ __device__ __forceinline__ Dims dims_of(const GemmArgs& a) {
 // Calls f(tile) for every tile of work item `item`; false if f asked to stop.
 template <int MODE, typename F>
 __device__ __forceinline__ bool for_each_tile_of_item(const GemmArgs& a, const Dims& dm, int item, F&& f) {
-  if constexpr (MODE == MODE_FWD) {
+  if constexpr (MODE == MODE_FWD || MODE == MODE_FWD_STAGE) {
     const int m = item % a.n_blocks, s = item / a.n_blocks;
     const int t0 = static_cast<int>(static_cast<long long>(s) * a.v_tiles / a.splits);
     const int t1 = static_cast<int>(static_cast<long long>(s + 1) * a.v_tiles / a.splits);
@@ -98,7 +108,8 @@ __device__ __forceinline__ bool for_each_tile_of_item(const GemmArgs& a, const D
     return f(Tile{KIND_MAIN, g * a.group_n + j % gn, j / gn, 0, true, true});
   } else {
     const int dc_tiles = a.dc_m_tiles * a.n_tiles;
-    const int de_tiles = dm.nb * a.n_tiles;
+    const int nsplit = max(a.de_splits, 1);
+    const int de_tiles = dm.nb * nsplit * a.n_tiles;
     int i = item, kind;
     if (a.dc_first) {
       kind = i < dc_tiles ? KIND_DC : KIND_DE;
@@ -108,14 +119,28 @@ __device__ __forceinline__ bool for_each_tile_of_item(const GemmArgs& a, const D
       if (kind == KIND_DC) i -= de_tiles;
     }
     // the column (D) tile varies fastest: neighbouring CTAs share the A operand
-    return f(Tile{kind, i / a.n_tiles, i % a.n_tiles, 0, true, true});
+    if (kind == KIND_DC) return f(Tile{kind, i / a.n_tiles, i % a.n_tiles, 0, true, true});
+    const int ms = i / a.n_tiles;  // (token block, K range)
+    return f(Tile{kind, ms / nsplit, i % a.n_tiles, ms % nsplit, true, true});
   }
 }
 
+// K-blocks [kblock_begin, kblocks_of) of tile t.
 template <int MODE>
 __device__ __forceinline__ int kblocks_of(const GemmArgs& a, const Dims& dm, const Tile& t) {
-  if constexpr (MODE == MODE_GRAD) return t.kind == KIND_DC ? dm.dc_kb : a.de_k_blocks;
+  if constexpr (MODE == MODE_GRAD) {
+    if (t.kind == KIND_DC) return dm.dc_kb;
+    return a.de_splits > 1 ? min(a.de_k_blocks, (t.split + 1) * a.de_kps) : a.de_k_blocks;
+  }
   return a.k_blocks;
+}
+
+template <int MODE>
+__device__ __forceinline__ int kblock_begin(const GemmArgs& a, const Tile& t) {
+  if constexpr (MODE == MODE_GRAD) {
+    if (t.kind == KIND_DE && a.de_splits > 1) return t.split * a.de_kps;
+  }
+  return 0;
 }
 
 // The first K-block >= kb of tile t that the filter keeps (nk when none).
@@ -169,9 +194,11 @@ __device__ __forceinline__ bool tile_empty(const GemmArgs& a, const Dims& dm, co
     const uint8_t* row = a.bitmapT + static_cast<size_t>((a.chunk_v0 >> 7) + t.m) * a.n_blocks;
     for (int r = lane_id(); r < dm.nb; r += 32) any |= __ldg(row + r);
   } else {
-    const int ncols = (a.chunk_w + FILTER_TILE - 1) / FILTER_TILE;
+    // the filter columns of the tile's K range (two K-blocks per column)
+    const int j0 = kblock_begin<MODE_GRAD>(a, t) >> 1;
+    const int j1 = (kblocks_of<MODE_GRAD>(a, dm, t) + 1) >> 1;
     const uint8_t* row = a.bitmap + static_cast<size_t>(t.m) * a.bm_ld + (a.chunk_v0 >> 7);
-    for (int j = lane_id(); j < ncols; j += 32) any |= __ldg(row + j);
+    for (int j = j0 + lane_id(); j < j1; j += 32) any |= __ldg(row + j);
   }
   return __any_sync(0xffffffffu, any) == 0;
 }
@@ -269,7 +296,7 @@ __device__ __forceinline__ void producer_loop(const GemmArgs& a, const SmemLayou
     if (item < 0) break;
     const bool ok = for_each_tile_of_item<MODE>(a, dm, item, [&](const Tile& t) -> bool {
       const int nk = kblocks_of<MODE>(a, dm, t);
-      int kb = next_kblock<MODE>(a, t, 0, nk);
+      int kb = next_kblock<MODE>(a, t, kblock_begin<MODE>(a, t), nk);
       if (MODE == MODE_GRAD && kb >= nk) {  // nothing survives the filter: an empty tagged stage
         if (!wait_bounded(&L.empty[stage], phase ^ 1u, abort_flag, a.dev_err)) return false;
         L.stage_meta[stage] = META_EMPTY;
@@ -455,7 +482,7 @@ __device__ __forceinline__ void softcap_chunk(uint32_t (&r)[32], float cap, floa
 }
 
 __device__ __forceinline__ void fold_chunk(const uint32_t (&r)[32], int col0, int V, long long xr, float& run_m,
-                                           float& run_s, float& tval, bool& tfound) {
+                                           float& run_s, float& tval, bool& tfound, float& chunk_max) {
   const int nvalid = min(32, V - col0);  // < 32 only in the last tile of a ragged vocabulary
   const long long rel = xr - col0;
   if (rel >= 0 && rel < nvalid) {  // the target column passes: capture its logit (rare)
@@ -478,6 +505,7 @@ __device__ __forceinline__ void fold_chunk(const uint32_t (&r)[32], int col0, in
     for (int j = 0; j < 32; ++j)
       if (j < nvalid) cmax = fmaxf(cmax, __uint_as_float(r[j]));
   }
+  chunk_max = fmaxf(chunk_max, cmax);
   const float nm = fmaxf(run_m, cmax * LOG2E);
   float s = run_s * ex2(run_m - nm);
   if (nvalid == 32) {
@@ -504,6 +532,7 @@ __device__ __forceinline__ void epi_fwd(const GemmArgs& a, const SmemLayout& L, 
   }
   float tval = 0.0f;
   bool tfound = false;
+  float tmax = NEG_BIG;  // unused here (the staging epilogue needs it)
   const int vt0 = t.n * BN;
   const uint32_t tbase = e.taddr + static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
@@ -518,14 +547,99 @@ __device__ __forceinline__ void epi_fwd(const GemmArgs& a, const SmemLayout& L, 
       softcap_chunk(r0, a.softcap, a.inv_softcap);
       softcap_chunk(r1, a.softcap, a.inv_softcap);
     }
-    fold_chunk(r0, col0, a.V, xr, st.run_m, st.run_s, tval, tfound);
-    if (col0 + 32 < a.V) fold_chunk(r1, col0 + 32, a.V, xr, st.run_m, st.run_s, tval, tfound);
+    fold_chunk(r0, col0, a.V, xr, st.run_m, st.run_s, tval, tfound, tmax);
+    if (col0 + 32 < a.V) fold_chunk(r1, col0 + 32, a.V, xr, st.run_m, st.run_s, tval, tfound, tmax);
   }
   release_tmem(L, acc);
   if (in_range && tfound) a.tgt[row] = tval;
   if (t.last && in_range) {
     a.part_m[static_cast<size_t>(t.split) * a.N + row] = st.run_m;
     a.part_s[static_cast<size_t>(t.split) * a.N + row] = st.run_s;
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// FWD_STAGE: the fold of epi_fwd; each 32-column chunk is also staged as
+// fp16 (logit minus the row's max over the chunk: <= 0, and fp16 keeps about
+// 11 bits of it, so the entries within a few units of the max -- the ones
+// that carry softmax mass -- keep an absolute error near 2^-12 per unit) in
+// 64-column boxes (128-byte swizzle), and the chunk max goes to mtile.  One
+// pass over TMEM.
+template <bool CAP>
+__device__ __forceinline__ void epi_fwd_stage(const GemmArgs& a, const SmemLayout& L, const Tile& t, int acc,
+                                              EpiCtx& e, FwdState& st) {
+  const uint32_t lane = lane_id();
+  const int row0 = t.m * BM + e.q * 32;  // first row of this warp's quadrant
+  const int row = row0 + static_cast<int>(lane);
+  const bool in_range = row < a.N;
+  const bool store = row0 < a.N;  // uniform: the box starts inside the staging rows
+  const long long xr = in_range ? static_cast<long long>(__ldg(a.x + row)) : -1ll;
+  if (t.first) {
+    st.run_m = NEG_BIG;
+    st.run_s = 0.0f;
+  }
+  float tval = 0.0f;
+  bool tfound = false;
+  const int vt0 = t.n * BN;
+  const uint32_t tbase = e.taddr + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; c += 2) {
+    const int col0 = vt0 + 32 * c;
+    if (col0 >= a.V) break;  // uniform across the warp
+    uint32_t r0[32], r1[32];
+    tmem_ld32(tbase + 32 * c, r0);
+    tmem_ld32(tbase + 32 * (c + 1), r1);
+    tmem_ld_wait();
+    if constexpr (CAP) {
+      softcap_chunk(r0, a.softcap, a.inv_softcap);
+      softcap_chunk(r1, a.softcap, a.inv_softcap);
+    }
+    float m0 = NEG_BIG, m1 = NEG_BIG;
+    fold_chunk(r0, col0, a.V, xr, st.run_m, st.run_s, tval, tfound, m0);
+    const bool has1 = col0 + 32 < a.V;
+    if (has1) fold_chunk(r1, col0 + 32, a.V, xr, st.run_m, st.run_s, tval, tfound, m1);
+    if (store) {
+      const int b = (c >> 1) & 1;
+      uint8_t* buf = e.buf + b * 4096;
+      staging_acquire(e, b);
+      const uint32_t sb = smem_u32(buf);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        st_shared_v4(sb + swz(lane, u),
+                     pack_f16x2(__uint_as_float(r0[8 * u + 0]) - m0, __uint_as_float(r0[8 * u + 1]) - m0),
+                     pack_f16x2(__uint_as_float(r0[8 * u + 2]) - m0, __uint_as_float(r0[8 * u + 3]) - m0),
+                     pack_f16x2(__uint_as_float(r0[8 * u + 4]) - m0, __uint_as_float(r0[8 * u + 5]) - m0),
+                     pack_f16x2(__uint_as_float(r0[8 * u + 6]) - m0, __uint_as_float(r0[8 * u + 7]) - m0));
+        st_shared_v4(sb + swz(lane, 4 + u),
+                     pack_f16x2(__uint_as_float(r1[8 * u + 0]) - m1, __uint_as_float(r1[8 * u + 1]) - m1),
+                     pack_f16x2(__uint_as_float(r1[8 * u + 2]) - m1, __uint_as_float(r1[8 * u + 3]) - m1),
+                     pack_f16x2(__uint_as_float(r1[8 * u + 4]) - m1, __uint_as_float(r1[8 * u + 5]) - m1),
+                     pack_f16x2(__uint_as_float(r1[8 * u + 6]) - m1, __uint_as_float(r1[8 * u + 7]) - m1));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&a.tmOut, buf, col0, row0);
+        bulk_commit();
+      }
+      e.last_buf = b;
+    }
+    if (in_range) {
+      a.mtile[static_cast<size_t>(col0 >> 5) * a.N + row] = m0;
+      if (has1) a.mtile[static_cast<size_t>((col0 >> 5) + 1) * a.N + row] = m1;
+    }
+  }
+  release_tmem(L, acc);
+  if (in_range) {
+    if (tfound) a.tgt[row] = tval;
+    if (t.last) {
+      a.part_m[static_cast<size_t>(t.split) * a.N + row] = st.run_m;
+      a.part_s[static_cast<size_t>(t.split) * a.N + row] = st.run_s;
+    }
   }
 }
 
@@ -650,6 +764,42 @@ __device__ __forceinline__ bool epi_bwd_g(const GemmArgs& a, const SmemLayout& L
   return ok;
 }
 
+// fp32 output rows gy .. gy + 31 of tensor map tm, columns x0 .. x0 + 32 * nbox - 1:
+// 32-column boxes (128-byte swizzle) from TMEM, or zeros when the tile is
+// empty; stored, or reduce-added by TMA.
+__device__ __forceinline__ void store_f32_boxes(const CUtensorMap* tm, EpiCtx& e, uint32_t tbase, int x0, int gy,
+                                                int nbox, bool empty, bool reduce) {
+  const uint32_t lane = lane_id();
+#pragma unroll 1
+  for (int j = 0; j < nbox; ++j) {
+    const int b = j & 1;
+    uint8_t* buf = e.buf + b * 4096;
+    staging_acquire(e, b);
+    const uint32_t sb = smem_u32(buf);
+    if (!empty) {
+      uint32_t r[32];
+      tmem_ld32(tbase + 32 * j, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int u = 0; u < 8; ++u) st_shared_v4(sb + swz(lane, u), r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
+    } else {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) st_shared_v4(sb + swz(lane, u), 0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (reduce) {
+        tma_reduce_add_2d(tm, buf, x0 + 32 * j, gy);
+      } else {
+        tma_store_2d(tm, buf, x0 + 32 * j, gy);
+      }
+      bulk_commit();
+    }
+    e.last_buf = b;
+  }
+}
+
 // GRAD, KIND_DC: bf16 output tile, rows = vocabulary (c_row0 + 128m ...),
 // cols = D tile of width bn, stored in 32-column boxes (64-byte swizzle).
 __device__ __forceinline__ void epi_dc(const GemmArgs& a, const Dims& dm, const SmemLayout& L, const Tile& t,
@@ -660,6 +810,16 @@ __device__ __forceinline__ void epi_dc(const GemmArgs& a, const Dims& dm, const 
   const int ly = t.m * BM + e.q * 32;  // first row of the box within the chunk
   const int gy = a.c_row0 + ly;        // ... in the dC tensor map
   const int x0 = t.n * a.bn;
+  if (a.dc_f32) {  // fp32 rows through tmOut (the single call accumulates dC over token chunks)
+    if (empty && a.dc_reduce) {
+      release_tmem(L, acc);
+      return;
+    }
+    const int nb = (ly < a.chunk_w) ? min(a.bn / 32, (a.D - x0 + 31) / 32) : 0;
+    store_f32_boxes(&a.tmOut, e, tbase, x0, gy, nb, empty, a.dc_reduce != 0);
+    release_tmem(L, acc);
+    return;
+  }
   if (a.dc_rows) {
     // Sorted vocabulary: row ly + lane of the chunk is token dc_rows[ly + lane];
     // each lane writes its own row of dC directly, 16 bytes at a time.
@@ -727,48 +887,22 @@ __device__ __forceinline__ void epi_dc(const GemmArgs& a, const Dims& dm, const 
 }
 
 // GRAD, KIND_DE: fp32 output tile, rows = tokens, cols = D tile; store (first
-// chunk) or reduce-add, in 32-column boxes (128-byte swizzle).
+// chunk) or reduce-add, in 32-column boxes (128-byte swizzle).  With K ranges
+// (single call) range s stores to its own slab of rows.
 __device__ __forceinline__ void epi_de(const GemmArgs& a, const Dims& dm, const SmemLayout& L, const Tile& t,
                                        int acc, EpiCtx& e) {
-  const uint32_t lane = lane_id();
   const bool empty = tile_empty(a, dm, t);
   if (empty && !a.first_chunk) {  // adding zero: nothing to do
     release_tmem(L, acc);
     return;
   }
   const uint32_t tbase = e.taddr + static_cast<uint32_t>(acc * BN);
-  const int gy = t.m * BM + e.q * 32;
+  const int ly = t.m * BM + e.q * 32;  // row within the launch's rows
+  const int gy = (a.de_splits > 1 ? t.split * a.de_slab : 0) + a.de_row0 + ly;
   const int x0 = t.n * a.bn;
   // boxes that start inside dE (no store or reduce may start outside the tensor)
-  const int nbox = (gy < a.N) ? min(a.bn / 32, (a.D - x0 + 31) / 32) : 0;
-#pragma unroll 1
-  for (int j = 0; j < nbox; ++j) {
-    const int b = j & 1;
-    uint8_t* buf = e.buf + b * 4096;
-    staging_acquire(e, b);
-    const uint32_t sb = smem_u32(buf);
-    if (!empty) {
-      uint32_t r[32];
-      tmem_ld32(tbase + 32 * j, r);
-      tmem_ld_wait();
-#pragma unroll
-      for (int u = 0; u < 8; ++u) st_shared_v4(sb + swz(lane, u), r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
-    } else {
-#pragma unroll
-      for (int u = 0; u < 8; ++u) st_shared_v4(sb + swz(lane, u), 0u, 0u, 0u, 0u);
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      if (a.first_chunk) {
-        tma_store_2d(&a.tmOut2, buf, x0 + 32 * j, gy);
-      } else {
-        tma_reduce_add_2d(&a.tmOut2, buf, x0 + 32 * j, gy);
-      }
-      bulk_commit();
-    }
-    e.last_buf = b;
-  }
+  const int nbox = (ly < a.N) ? min(a.bn / 32, (a.D - x0 + 31) / 32) : 0;
+  store_f32_boxes(&a.tmOut2, e, tbase, x0, gy, nbox, empty, !a.first_chunk);
   release_tmem(L, acc);
 }
 
@@ -796,6 +930,8 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& a, const SmemLayou
       bool r = true;
       if constexpr (MODE == MODE_FWD) {
         epi_fwd<CAP>(a, L, t, acc, e, st);
+      } else if constexpr (MODE == MODE_FWD_STAGE) {
+        epi_fwd_stage<CAP>(a, L, t, acc, e, st);
       } else if constexpr (MODE == MODE_BWD_G) {
         r = epi_bwd_g<CAP>(a, L, t, acc, e);
       } else {

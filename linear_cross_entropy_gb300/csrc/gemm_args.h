@@ -26,8 +26,9 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr float NEG_BIG = -3.0e38f;  // finite "minus infinity" for the running max
 
 // MODE_GRAD runs the two gradient contractions of one vocabulary chunk in
-// one launch; each of its tiles is of kind KIND_DC or KIND_DE.
-enum Mode { MODE_FWD = 0, MODE_BWD_G = 1, MODE_GRAD = 2 };
+// one launch; each of its tiles is of kind KIND_DC or KIND_DE.  MODE_FWD_STAGE
+// is MODE_FWD that also stages its logits for the single call (see mtile).
+enum Mode { MODE_FWD = 0, MODE_BWD_G = 1, MODE_GRAD = 2, MODE_FWD_STAGE = 3 };
 enum Kind { KIND_MAIN = 0, KIND_DC = 1, KIND_DE = 2 };
 
 struct GemmArgs {
@@ -88,6 +89,21 @@ struct GemmArgs {
   uint8_t* bitmap;   // [ceil(N/128)][bm_ld] tile survival, token-block major
   uint8_t* bitmapT;  // [bm_ld][ceil(N/128)] the same, vocabulary-block major (read along K by dC)
   int bm_ld;         // ceil(V / 128)
+  // FWD_STAGE: each row's max over each 32-column chunk, [v_tiles * 8][N]
+  // fp32; the logits minus that max go to tmOut as fp16 [N][v_tiles * 256]
+  float* mtile;
+  // GRAD, single call: the dE tiles split the vocabulary (K) into de_splits
+  // ranges of de_kps K-blocks (even); split s stores its fp32 tile to rows
+  // s * de_slab + de_row0 + ... of the tmOut2 tensor (de_splits = 0 or 1:
+  // one range, rows de_row0 + ...)
+  int de_splits;
+  int de_kps;
+  int de_slab;
+  int de_row0;
+  // GRAD: the dC tiles write fp32 through tmOut (SW128 32-column boxes),
+  // stored (dc_reduce = 0) or reduce-added (1), instead of bf16
+  int dc_f32;
+  int dc_reduce;
   int32_t* dev_err;
 };
 

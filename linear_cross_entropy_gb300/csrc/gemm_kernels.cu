@@ -1,4 +1,4 @@
-// Instantiations and launcher of the three tcgen05 GEMM kernels.
+// Instantiations and launcher of the tcgen05 GEMM kernels.
 #include "gemm.cuh"
 #include "internal.h"
 
@@ -15,6 +15,8 @@ cudaError_t prepare_gemm_kernels() {
   if ((e = set_smem<MODE_FWD, true>()) != cudaSuccess) return e;
   if ((e = set_smem<MODE_BWD_G, false>()) != cudaSuccess) return e;
   if ((e = set_smem<MODE_BWD_G, true>()) != cudaSuccess) return e;
+  if ((e = set_smem<MODE_FWD_STAGE, false>()) != cudaSuccess) return e;
+  if ((e = set_smem<MODE_FWD_STAGE, true>()) != cudaSuccess) return e;
   return set_smem<MODE_GRAD, false>();
 }
 
@@ -51,6 +53,13 @@ cudaError_t launch_gemm(int mode, const GemmArgs& args, int grid, cudaStream_t s
         cce_gemm_kernel<MODE_BWD_G, true><<<g, b, SMEM_BYTES, stream>>>(args);
       } else {
         cce_gemm_kernel<MODE_BWD_G, false><<<g, b, SMEM_BYTES, stream>>>(args);
+      }
+      break;
+    case MODE_FWD_STAGE:
+      if (cap) {
+        cce_gemm_kernel<MODE_FWD_STAGE, true><<<g, b, SMEM_BYTES, stream>>>(args);
+      } else {
+        cce_gemm_kernel<MODE_FWD_STAGE, false><<<g, b, SMEM_BYTES, stream>>>(args);
       }
       break;
     case MODE_GRAD: cce_gemm_kernel<MODE_GRAD, false><<<g, b, SMEM_BYTES, stream>>>(args); break;

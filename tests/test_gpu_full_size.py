@@ -115,3 +115,45 @@ def test_full_size(name, filter_mode, sort):
           f"<E,dE>={lhs:.6e} <C,dC>={rhs:.6e}")
     del E, C, dE, dC
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", ["qwen", "llama"])
+def test_full_size_single_call(name):
+    """The single call at full size (the Llama-shaped head takes two token
+    chunks at the default staging budget, so dC goes through the fp32
+    accumulator): LSE of every row, the loss, sampled dE and dC rows against
+    the oracle, ignored rows +0, and <E, dE> = <C, dC>."""
+    import linear_cross_entropy_gb300 as cce
+    w, E_bits, C_bits, x, lse_ref = _inputs(name)
+    E, C, xt = to_device(E_bits, C_bits, x)
+    loss, lse, dE, dC, stats = cce.cce_loss_and_grad(E, C, xt, reduction=w.reduction, stats=True)
+    torch.cuda.synchronize()
+    err = np.abs(lse.double().cpu().numpy() - lse_ref) / np.abs(lse_ref)
+    assert err.max() <= TOL_LSE, f"LSE rel err {err.max():.3e}"
+    Ef, Cf = O.from_bits(E_bits, C_bits)
+    valid = x != O.IGNORE_INDEX
+    count = int(valid.sum())
+    tgt = O.indexed_logits(Ef, Cf, x)
+    loss_ref = O.reduce_loss(np.where(valid, lse_ref - np.where(valid, tgt, 0.0), 0.0), count, w.reduction)
+    assert abs(loss.item() - loss_ref) <= TOL_LSE * abs(loss_ref), (loss.item(), loss_ref)
+    rng = np.random.default_rng(12)
+    wts = O.row_weights(x, O.IGNORE_INDEX, w.reduction, 1.0, count)
+    rows = np.unique(np.concatenate([[0, w.N - 1], rng.choice(w.N, 30, replace=False)]))
+    dE_ref = O.backward_dE(Ef, Cf, x, lse_ref[rows], wts[rows], rows)
+    e_dE = rel_fro(dE[torch.from_numpy(rows).cuda()].double().cpu().numpy(), dE_ref)
+    assert e_dE <= TOL_GRAD_FILTERED, f"dE sample rel err {e_dE:.3e}"
+    freq = np.bincount(x[valid], minlength=w.V).argsort()[::-1][:12]
+    vrows = np.unique(np.concatenate([freq, [0, w.V - 1], rng.choice(w.V, 20, replace=False)]))
+    dC_ref = O.backward_dC(Ef, Cf, x, lse_ref, wts, vrows)
+    e_dC = rel_fro(dC[torch.from_numpy(vrows).cuda()].double().cpu().numpy(), dC_ref)
+    assert e_dC <= TOL_GRAD_FILTERED, f"dC sample rel err {e_dC:.3e}"
+    ign = np.nonzero(~valid)[0]
+    if len(ign):
+        assert int(torch.count_nonzero(dE[torch.from_numpy(ign).cuda()].view(torch.int16))) == 0
+    lhs = float((E.double() * dE.double()).sum())
+    rhs = float((C.double() * dC.double()).sum())
+    assert abs(lhs - rhs) <= 2e-2 * max(abs(lhs), abs(rhs)), (lhs, rhs)
+    print(f"{name} single call: loss {loss.item():.6f} (oracle {loss_ref:.6f}) lse err {err.max():.2e} "
+          f"dE err {e_dE:.2e} dC err {e_dC:.2e} tiles skipped {stats['skipped']}/{stats['tiles']}")
+    del E, C, dE, dC
+    torch.cuda.empty_cache()
