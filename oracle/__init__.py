@@ -325,10 +325,10 @@ def loss_and_grad(E, C, x, ignore_index=IGNORE_INDEX, reduction="mean", softcap=
 
     It is forward() followed by backward() with grad_out = 1.  With
     filter_eps > 0 the skipped tiles' contributions are removed as in
-    backward_filtered over all rows in their order (the single call keeps
-    every row, so a filter tile is 128 consecutive rows, ignored ones
-    included, x 128 vocabulary entries).  Returns {loss, lse, count, dE, dC,
-    keep}."""
+    backward_filtered with the ignored rows removed first ("Cut Your Losses
+    ...", Table A1: removing ignored tokens), so a filter tile is 128
+    consecutive rows that take part x 128 vocabulary entries, as in the
+    two-call backward.  Returns {loss, lse, count, dE, dC, keep}."""
     if reduction not in ("sum", "mean"):
         raise ValueError("the single call is defined for the sum and mean reductions")
     E = np.asarray(E, np.float64)
@@ -337,7 +337,7 @@ def loss_and_grad(E, C, x, ignore_index=IGNORE_INDEX, reduction="mean", softcap=
     w = row_weights(x, ignore_index, reduction, 1.0, f["count"])
     if filter_eps:
         dE, dC, keep = backward_filtered(E, C, x, f["lse"], w, BN, BV, filter_eps, ignore_index, filter_dE,
-                                         filter_dC, softcap, compact_ignored=False)
+                                         filter_dC, softcap, compact_ignored=True)
     else:
         dE, dC = backward(E, C, x, f["lse"], w, ignore_index, softcap)
         keep = None

@@ -513,17 +513,19 @@ def test_single_call_scales_linearly_with_the_upstream_gradient(rng):
         assert abs(g * (lp - lm) / (2 * h) - g * out["dE"][idx]) <= 1e-6
 
 
-def test_single_call_filter_tiles_keep_ignored_rows_in_place(rng):
-    """The single call keeps every row: with ignored rows between the others,
-    its filtered gradient is the uncompacted tiling's, not the compacted
-    one's."""
+def test_single_call_filter_tiles_are_over_the_rows_that_take_part(rng):
+    """The single call removes the ignored rows first: with ignored rows
+    between the others, its filtered gradient is the compacted tiling's, and
+    equals the filtered backward of the batch without those rows."""
     E, C, x = _problem(rng, 96, 12, 300, scale=3.0, ignore=tuple(range(0, 96, 3)))
     out = O.loss_and_grad(E, C, x, reduction="sum", filter_eps=2e-2, BN=16, BV=16)
     f = O.forward(E, C, x, reduction="sum")
     w = O.row_weights(x, -100, "sum", 1.0, f["count"])
     a = O.backward_filtered(E, C, x, f["lse"], w, 16, 16, 2e-2)
-    b = O.backward_filtered(E, C, x, f["lse"], w, 16, 16, 2e-2, compact_ignored=True)
-    assert np.array_equal(out["keep"], a[2]) and np.array_equal(out["dC"], a[1])
+    keep_rows = np.nonzero(x != -100)[0]
+    b = O.backward_filtered(E[keep_rows], C, x[keep_rows], f["lse"][keep_rows], w[keep_rows], 16, 16, 2e-2)
+    assert np.array_equal(out["keep"], b[2]) and np.array_equal(out["dC"], b[1])
+    assert np.array_equal(out["dE"][keep_rows], b[0]) and np.all(out["dE"][x == -100] == 0.0)
     assert a[2].shape != b[2].shape
     with pytest.raises(ValueError):
         O.loss_and_grad(E, C, x, reduction="none")
