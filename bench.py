@@ -207,7 +207,8 @@ def run_gpu(args, rank, world, local_rank):
     xt = torch.from_numpy(x).to(dev)
     red = w.reduction
     g = torch.ones(N if red == "none" else 1, dtype=torch.float32, device=dev)
-    ws_f = torch.empty(cce.forward_workspace_bytes(N, D, V), dtype=torch.uint8, device=dev)
+    skip = bool(args.skip_ignored)
+    ws_f = torch.empty(cce.forward_workspace_bytes(N, D, V, skip_ignored=skip), dtype=torch.uint8, device=dev)
     single = args.mode == "single"
     if single:
         ws_b = torch.empty(cce.loss_and_grad_workspace_bytes(N, D, V), dtype=torch.uint8, device=dev)
@@ -223,7 +224,8 @@ def run_gpu(args, rank, world, local_rank):
             loss, _, _, _ = cce.cce_loss_and_grad(E, C, xt, -100, red, eps, workspace=ws_b, dev_err=err,
                                                   check_errors=False, lse=False, dE=dE, dC=dC)
             return loss
-        loss, lse = cce.cce_forward(E, C, xt, -100, red, workspace=ws_f, dev_err=err, check_errors=False)
+        loss, lse = cce.cce_forward(E, C, xt, -100, red, workspace=ws_f, dev_err=err, check_errors=False,
+                                    skip_ignored=skip)
         cce.cce_backward(E, C, xt, lse, g, -100, red, eps, workspace=ws_b, dev_err=err, check_errors=False,
                          dE=dE, dC=dC, vocab_sort=sort)
         return loss
@@ -238,7 +240,7 @@ def run_gpu(args, rank, world, local_rank):
         loss, lse, _, _, st = cce.cce_loss_and_grad(E, C, xt, -100, red, eps, dev_err=err, check_errors=False,
                                                     stats=True)
     else:
-        loss, lse = cce.cce_forward(E, C, xt, -100, red, dev_err=err, check_errors=False)
+        loss, lse = cce.cce_forward(E, C, xt, -100, red, dev_err=err, check_errors=False, skip_ignored=skip)
         _, _, st = cce.cce_backward(E, C, xt, lse, g, -100, red, eps, dev_err=err, check_errors=False,
                                     stats=True, vocab_sort=sort)
     torch.cuda.synchronize()
@@ -313,10 +315,11 @@ def run_gpu(args, rank, world, local_rank):
     # take part (ignored rows are compacted away) and, for dC / dE, over the
     # filter tiles kept.
     n_part = int((x != W.IGNORE_INDEX).sum())
-    # the single call keeps every row (no compaction) and has no recompute
-    n_grad = N if single else n_part
-    flops = {"fwd_lse_gemm": 2.0 * N * D * V, "bwd_recompute_g": 2.0 * n_part * D * V,
-             "bwd_grad_gemm": 4.0 * n_grad * D * V * kept}
+    # the forward runs over the rows that take part when it skips the others
+    # (always in the single call, which also has no recompute)
+    n_fwd = n_part if (skip or single) else N
+    flops = {"fwd_lse_gemm": 2.0 * n_fwd * D * V, "bwd_recompute_g": 2.0 * n_part * D * V,
+             "bwd_grad_gemm": 4.0 * n_part * D * V * kept}
     phase_rep = {}
     for name, ms in phases.ms.items():
         n_l = phases.launches[name]
@@ -343,6 +346,7 @@ def run_gpu(args, rank, world, local_rank):
         "config": {"workload": f"{WORKLOAD_NAMES[args.config]} N={N} D={D} V={V}", "N": N, "D": D, "V": V,
                    "reduction": red, "filter_eps": eps, "vocab_sort": sort, "ignore_frac": w.ignore_frac,
                    "mode": "single call (cce_loss_and_grad)" if single else "two calls (cce_forward + cce_backward)",
+                   "forward_skips_ignored_rows": skip or single,
                    "l2": f"inputs larger than L2 (C is {C.numel() * 2 / 1e6:.0f} MB)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         # the pages' metric: 8 N D V over all N tokens, whatever the filter or
@@ -402,6 +406,8 @@ def main(argv=None):
     ap.add_argument("--filter", choices=("on", "off"), default=None)
     ap.add_argument("--vocab-sort", action="store_true",
                     help="filter over the vocabulary sorted by average logit")
+    ap.add_argument("--skip-ignored", action="store_true",
+                    help="two-call mode: the forward skips the rows that take part in no loss")
     ap.add_argument("--mode", choices=("two-call", "single"), default="two-call",
                     help="two-call: cce_forward + cce_backward; single: cce_loss_and_grad")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -173,6 +173,24 @@ cce_status cce_forward_ex(const void* E, const void* C, const int64_t* x, int64_
                           void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream);
 
 /*
+ * Forward with options.  cce_forward_ex is cce_forward_ex2 with flags = 0.
+ * CCE_FWD_SKIP_IGNORED: the rows that take part (target in [0, V) and not
+ * ignore_index) are compacted on the device before the GEMM, which then runs
+ * over them only ("Cut Your Losses ...", Table A1: removing ignored tokens
+ * before the loss); the loss is unchanged, and lse (and loss for
+ * CCE_RED_NONE) is 0 on the other rows instead of their LSE.  cce_backward
+ * needs only the LSE of rows that take part, so it accepts this lse.  The
+ * workspace grows to cce_forward_workspace_bytes_ex(N, D, V, flags) (a compact
+ * copy of E: N * D * 2 bytes, plus 24 bytes per row).  Any other flag bit
+ * returns CCE_ERR_ARG.
+ */
+#define CCE_FWD_SKIP_IGNORED 1
+size_t cce_forward_workspace_bytes_ex(int64_t N, int64_t D, int64_t V, int flags);
+cce_status cce_forward_ex2(const void* E, const void* C, const int64_t* x, int64_t N, int64_t D, int64_t V,
+                           int64_t ignore_index, int reduction, float softcap, int flags, float* loss, float* lse,
+                           void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream);
+
+/*
  * Backward with softcapping and per-output filtering.  cce_backward is
  * cce_backward_ex with softcap = 0 and CCE_FILTER_BOTH.  softcap must match
  * the forward's; the gradient then carries the slope 1 - tanh^2(a / softcap),
@@ -253,18 +271,23 @@ cce_status cce_vocab_order(const float* keys, int64_t V, int32_t* perm, void* wo
  * linear in it).  Only CCE_RED_SUM and CCE_RED_MEAN (a scalar upstream
  * gradient); CCE_RED_NONE returns CCE_ERR_ARG.
  *
- * Rows are processed in chunks of Nc tokens (a multiple of 256) whose logits,
- * staged as fp16 [Nc][V rounded up to 256] (each logit minus its row's max
- * over a 256-column tile), fit in max_staging_bytes (0: 2 GiB; at least one
- * 256-row chunk).  Nothing is recomputed: the chunk's logits are computed
- * once (6 N D V flops in all, against 8 N D V for cce_forward +
- * cce_backward), at the cost of the staging traffic.  The filter (filter_eps,
- * filter_flags as in cce_backward_ex; CCE_SORT_VOCAB is not accepted) works on
- * tiles of 128 consecutive rows, ignored rows included (every row is kept),
- * x 128 vocabulary entries.  With more than one chunk dC is accumulated in an
- * fp32 buffer in the workspace; dE always goes through fp32 slabs.
+ * The rows that take part (target in [0, V) and not ignore_index) are
+ * compacted on the device first ("Cut Your Losses ...", Table A1: removing
+ * ignored tokens), and only they go through the GEMMs.  They are processed in
+ * chunks of Nc rows (a multiple of 256) whose logits, staged as fp16
+ * [Nc][V rounded up to 256] (each logit minus its row's max over a 32-column
+ * chunk), fit in max_staging_bytes (0: 2 GiB; at least one 256-row chunk).
+ * Nothing is recomputed: the chunk's logits are computed once (6 n D V flops
+ * for n rows taking part, against 8 N D V for cce_forward + cce_backward), at
+ * the cost of the staging traffic.  The filter (filter_eps, filter_flags as
+ * in cce_backward_ex; CCE_SORT_VOCAB is not accepted) works on tiles of 128
+ * consecutive compact rows x 128 vocabulary entries, as in cce_backward.
+ * With more than one chunk dC is accumulated in an fp32 buffer in the
+ * workspace; dE always goes through fp32 slabs.
  *
- *   loss   [1] fp32 (written).   lse  [N] fp32 (written) or NULL.
+ *   loss   [1] fp32 (written).
+ *   lse    [N] fp32 (written) or NULL: the LSE of rows that take part, 0 on
+ *          the others.
  *   dE     [N, D] bf16, dC [V, D] bf16 (written; ignored rows of dE are +0).
  *   workspace >= cce_loss_and_grad_workspace_bytes(N, D, V, max_staging_bytes).
  *   dev_stats  optional device int64[2]: {tiles, skipped tiles} over all chunks.

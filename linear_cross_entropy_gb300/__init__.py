@@ -60,8 +60,8 @@ def _check_inputs(E, C, x):
         raise ValueError(f"shape mismatch: E {tuple(E.shape)}, C {tuple(C.shape)}, x {tuple(x.shape)}")
 
 
-def forward_workspace_bytes(N, D, V) -> int:
-    return int(_lib.load().cce_forward_workspace_bytes(N, D, V))
+def forward_workspace_bytes(N, D, V, *, skip_ignored=False) -> int:
+    return int(_lib.load().cce_forward_workspace_bytes_ex(N, D, V, _lib.FWD_SKIP_IGNORED if skip_ignored else 0))
 
 
 def backward_workspace_bytes(N, D, V, *, filter_outputs="both", vocab_sort=False) -> int:
@@ -87,10 +87,12 @@ def _raise_dev_err(dev_err):
         raise CCEError(8, "target index outside [0, V) and not ignore_index")
 
 
-def cce_forward(E, C, x, ignore_index=-100, reduction="mean", *, softcap=0.0, stream=None, check_errors=True,
-                workspace=None, dev_err=None):
+def cce_forward(E, C, x, ignore_index=-100, reduction="mean", *, softcap=0.0, skip_ignored=False, stream=None,
+                check_errors=True, workspace=None, dev_err=None):
     """Returns (loss, lse).  loss is [N] for reduction='none', else a 0-d tensor.
-    softcap > 0 caps the logits as softcap * tanh(logit / softcap)."""
+    softcap > 0 caps the logits as softcap * tanh(logit / softcap).
+    skip_ignored: compact away the rows that take part in no loss before the
+    GEMM (their lse, and loss for 'none', are then 0; the loss is unchanged)."""
     _check_inputs(E, C, x)
     N, D = E.shape
     V = C.shape[0]
@@ -99,15 +101,16 @@ def cce_forward(E, C, x, ignore_index=-100, reduction="mean", *, softcap=0.0, st
     dev = E.device
     loss = torch.empty(N if red == 0 else 1, dtype=torch.float32, device=dev)
     lse = torch.empty(N, dtype=torch.float32, device=dev)
-    need = int(lib.cce_forward_workspace_bytes(N, D, V))
+    flags = _lib.FWD_SKIP_IGNORED if skip_ignored else 0
+    need = int(lib.cce_forward_workspace_bytes_ex(N, D, V, flags))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     if dev_err is None:
         dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
     with torch.cuda.device(dev):
-        st = lib.cce_forward_ex(_ptr(E), _ptr(C), _ptr(x), N, D, V, int(ignore_index), red, float(softcap),
-                                _ptr(loss), _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(dev_err),
-                                _stream_handle(stream))
+        st = lib.cce_forward_ex2(_ptr(E), _ptr(C), _ptr(x), N, D, V, int(ignore_index), red, float(softcap), flags,
+                                 _ptr(loss), _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(dev_err),
+                                 _stream_handle(stream))
     _lib.check(st, "cce_forward")
     if check_errors:
         _raise_dev_err(dev_err)

@@ -23,6 +23,7 @@ DEVERR_TARGET_RANGE = 1
 DEVERR_TIMEOUT = 2
 NUM_PHASES = 8
 SORT_VOCAB = 4
+FWD_SKIP_IGNORED = 1
 
 
 class CCEError(RuntimeError):
@@ -81,6 +82,11 @@ def load() -> ctypes.CDLL:
     lib.cce_vocab_logit_sums.restype = ctypes.c_int
     lib.cce_vocab_order.argtypes = [vp, i64, vp, vp, sz, vp]
     lib.cce_vocab_order.restype = ctypes.c_int
+    lib.cce_forward_workspace_bytes_ex.argtypes = [i64, i64, i64, ctypes.c_int]
+    lib.cce_forward_workspace_bytes_ex.restype = sz
+    lib.cce_forward_ex2.argtypes = [vp, vp, vp, i64, i64, i64, i64, ctypes.c_int, ctypes.c_float, ctypes.c_int, vp,
+                                    vp, vp, sz, vp, vp]
+    lib.cce_forward_ex2.restype = ctypes.c_int
     lib.cce_loss_and_grad_workspace_bytes.argtypes = [i64, i64, i64, sz]
     lib.cce_loss_and_grad_workspace_bytes.restype = sz
     lib.cce_loss_and_grad.argtypes = [vp, vp, vp, i64, i64, i64, i64, ctypes.c_int, ctypes.c_float, ctypes.c_float,

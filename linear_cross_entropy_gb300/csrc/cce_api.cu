@@ -35,18 +35,21 @@ std::atomic<uint64_t> g_launches{0};
 
 // ------------------------------------------------------------ small kernels
 // Per row: LSE from the per-split partials (fixed split order), loss, and a
-// deterministic per-block partial sum for the reduction.
+// deterministic per-block partial sum for the reduction.  With n_dev the rows
+// are compact and only the first clamp(*n_dev - n_row0, 0, N) exist.
 __global__ void combine_kernel(const float* __restrict__ part_m, const float* __restrict__ part_s,
                                const float* __restrict__ tgt, const int64_t* __restrict__ x, int N, int S, int V,
                                long long ignore_index, int reduction, float* __restrict__ lse,
                                float* __restrict__ loss_rows, double* __restrict__ blk_sum,
-                               int* __restrict__ blk_cnt, int32_t* dev_err) {
+                               int* __restrict__ blk_cnt, int32_t* dev_err, const int* __restrict__ n_dev,
+                               int n_row0) {
   __shared__ double ssum[COMBINE_THREADS];
   __shared__ int scnt[COMBINE_THREADS];
   const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  const int nrow = n_dev ? max(0, min(N, *n_dev - n_row0)) : N;
   double my = 0.0;
   int mycnt = 0;
-  if (row < N) {
+  if (row < nrow) {
     float M = -INFINITY;
     for (int s = 0; s < S; ++s) M = fmaxf(M, part_m[static_cast<size_t>(s) * N + row]);
     float sum = 0.0f;
@@ -174,17 +177,29 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ E, const int64_t* _
       for (int j = lane; j < per_row; j += 32) dst[j] = src[j];
       if (lane == 0) {
         xc[k] = x[r];
-        lsec[k] = lse[r];
+        if (lsec) lsec[k] = lse[r];
         if (gc) gc[k] = g[r];
       }
     } else {
       for (int j = lane; j < per_row; j += 32) dst[j] = make_uint4(0u, 0u, 0u, 0u);
       if (lane == 0) {
         xc[k] = ignore_index;
-        lsec[k] = 0.0f;
+        if (lsec) lsec[k] = 0.0f;
         if (gc) gc[k] = 0.0f;
       }
     }
+  }
+}
+
+// Compact per-row results back to the original rows: lse[r] (and, when
+// given, loss_rows[r]) from compact row pos[r], 0 for rows that took no part.
+__global__ void scatter_rows_kernel(const float* __restrict__ lsec, const float* __restrict__ lossc,
+                                    const int* __restrict__ pos, int N, float* __restrict__ lse,
+                                    float* __restrict__ loss_rows) {
+  for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < N; r += gridDim.x * blockDim.x) {
+    const int p = pos[r];
+    if (lse) lse[r] = p >= 0 ? lsec[p] : 0.0f;
+    if (loss_rows) loss_rows[r] = p >= 0 ? lossc[p] : 0.0f;
   }
 }
 
@@ -268,10 +283,12 @@ int grad_tile_width(int64_t D, int step) {
 
 struct FwdLayout {
   size_t counter, part_m, part_s, tgt, blk_sum, blk_cnt, total;
+  // CCE_FWD_SKIP_IGNORED only: compaction map, compact rows and results
+  size_t pos, ridx, count, xc, ec, lsec, lossc;
   int S, nblk;
 };
 
-FwdLayout fwd_layout(int64_t N, int64_t V) {
+FwdLayout fwd_layout(int64_t N, int64_t V, int64_t D = 0, bool compact = false) {
   FwdLayout L{};
   L.S = fwd_splits(N, V);
   L.nblk = static_cast<int>(cdiv(N, COMBINE_THREADS));
@@ -288,6 +305,22 @@ FwdLayout fwd_layout(int64_t N, int64_t V) {
   o = align_up(o + sizeof(double) * L.nblk, ALIGN);
   L.blk_cnt = o;
   o = align_up(o + sizeof(int) * L.nblk, ALIGN);
+  if (compact) {
+    L.pos = o;
+    o = align_up(o + sizeof(int) * static_cast<size_t>(N), ALIGN);
+    L.ridx = o;
+    o = align_up(o + sizeof(int) * static_cast<size_t>(N), ALIGN);
+    L.count = o;
+    o = align_up(o + sizeof(int), ALIGN);
+    L.xc = o;
+    o = align_up(o + sizeof(int64_t) * static_cast<size_t>(N), ALIGN);
+    L.ec = o;
+    o = align_up(o + static_cast<size_t>(N) * D * 2, ALIGN);
+    L.lsec = o;
+    o = align_up(o + sizeof(float) * static_cast<size_t>(N), ALIGN);
+    L.lossc = o;
+    o = align_up(o + sizeof(float) * static_cast<size_t>(N), ALIGN);
+  }
   L.total = o;
   return L;
 }
@@ -347,7 +380,8 @@ BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V, bool sort = false) {
   return L;
 }
 
-// Single call: token chunks of Nc rows (a multiple of 256) whose staged
+// Single call: the rows that take part are compacted first (pos, ridx, the
+// compact E and x), then token chunks of Nc compact rows (a multiple of 256) whose staged
 // logits, fp16 [Nc][Vp] with Vp = V rounded up to 256, fit in max_staging
 // bytes (at least one 256-row chunk); per chunk the forward partials, the
 // 32-column chunk maxima and the survival maps; dE in de_splits fp32 slabs of
@@ -355,8 +389,8 @@ BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V, bool sort = false) {
 constexpr size_t FLCE_STAGING_DEFAULT = size_t(2) << 30;
 
 struct FlceLayout {
-  size_t counters, count, part_m, part_s, tgt, lse, blk_sum, blk_cnt, stage, mtile, bitmap, bitmapT, deacc, dcacc,
-      total;
+  size_t counters, count, pos, ridx, xc, ec, part_m, part_s, tgt, lse, blk_sum, blk_cnt, stage, mtile, bitmap,
+      bitmapT, deacc, dcacc, total;
   int64_t Nc, nchunks, Vp, bm_ld, slab, n_tiles, bn, kps;
   int S, Sde, nblk;
 };
@@ -390,6 +424,10 @@ FlceLayout flce_layout(int64_t N, int64_t D, int64_t V, size_t max_staging) {
   };
   L.counters = take(sizeof(int) * 2 * static_cast<size_t>(L.nchunks));
   L.count = take(sizeof(int));
+  L.pos = take(sizeof(int) * static_cast<size_t>(N));
+  L.ridx = take(sizeof(int) * static_cast<size_t>(N));
+  L.xc = take(sizeof(int64_t) * static_cast<size_t>(N));
+  L.ec = take(static_cast<size_t>(N) * D * 2);
   L.part_m = take(sizeof(float) * L.S * static_cast<size_t>(L.Nc));
   L.part_s = take(sizeof(float) * L.S * static_cast<size_t>(L.Nc));
   L.tgt = take(sizeof(float) * static_cast<size_t>(L.Nc));
@@ -645,9 +683,9 @@ cce_status cce_forward(const void* E, const void* C, const int64_t* x, int64_t N
                         stream);
 }
 
-cce_status cce_forward_ex(const void* E, const void* C, const int64_t* x, int64_t N, int64_t D, int64_t V,
-                          int64_t ignore_index, int reduction, float softcap, float* loss, float* lse,
-                          void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream) {
+static cce_status forward_impl(const void* E, const void* C, const int64_t* x, int64_t N, int64_t D, int64_t V,
+                               int64_t ignore_index, int reduction, float softcap, int flags, float* loss, float* lse,
+                               void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream) {
   if (!E || !C || !x || !loss || !lse || !workspace) return CCE_ERR_NULL;
   if (!sizes_ok(N, D, V)) return CCE_ERR_SHAPE;
   if (!aligned16(E) || !aligned16(C) || !aligned16(loss) || !aligned16(lse) || !aligned16(workspace) ||
@@ -655,7 +693,9 @@ cce_status cce_forward_ex(const void* E, const void* C, const int64_t* x, int64_
     return CCE_ERR_ALIGN;
   if (reduction != CCE_RED_NONE && reduction != CCE_RED_SUM && reduction != CCE_RED_MEAN) return CCE_ERR_ARG;
   if (!(softcap >= 0.0f) || !std::isfinite(softcap)) return CCE_ERR_ARG;
-  const FwdLayout W = fwd_layout(N, V);
+  if (flags & ~CCE_FWD_SKIP_IGNORED) return CCE_ERR_ARG;
+  const bool compact = (flags & CCE_FWD_SKIP_IGNORED) != 0;
+  const FwdLayout W = fwd_layout(N, V, D, compact);
   if (ws_bytes < W.total) return CCE_ERR_WORKSPACE;
   int sms = 0;
   cce_status st = device_check(&sms);
@@ -663,10 +703,39 @@ cce_status cce_forward_ex(const void* E, const void* C, const int64_t* x, int64_
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
 
+  // Skipping ignored rows ("Cut Your Losses ...", Table A1: removing ignored
+  // tokens): the rows that take part are compacted first and the GEMM runs
+  // over them only, with their count read from device memory.
+  const void* Eg = E;
+  const int64_t* xg = x;
+  int* count = nullptr;
+  int* pos = nullptr;
+  if (compact) {
+    PhaseScope ps(2, s);
+    count = reinterpret_cast<int*>(ws + W.count);
+    pos = reinterpret_cast<int*>(ws + W.pos);
+    int* ridx = reinterpret_cast<int*>(ws + W.ridx);
+    int64_t* xc = reinterpret_cast<int64_t*>(ws + W.xc);
+    void* Ec = ws + W.ec;
+    compact_kernel<<<1, COMPACT_THREADS, 0, s>>>(x, static_cast<int>(N), static_cast<int>(V),
+                                                 static_cast<long long>(ignore_index), pos, ridx, count, dev_err);
+    g_launches++;
+    const int rows_per_block = 8;
+    const int blocks = static_cast<int>(std::min<int64_t>(int64_t(sms) * 16, cdiv(N, rows_per_block)));
+    gather_rows_kernel<<<std::max(blocks, 1), 32 * rows_per_block, 0, s>>>(
+        static_cast<const uint4*>(E), x, nullptr, nullptr, ridx, count, static_cast<int>(N), static_cast<int>(D),
+        static_cast<long long>(ignore_index), static_cast<uint4*>(Ec), xc, nullptr, nullptr);
+    g_launches++;
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_status(e);
+    Eg = Ec;
+    xg = xc;
+  }
+
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
   // A = E [N, D]: box 64 (D) x 128 rows.  B = C [V, D]: box 64 (D) x 256 rows.
-  if (!make_tmap(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, E, D, N, D, BK, BM) ||
+  if (!make_tmap(&a.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Eg, D, N, D, BK, BM) ||
       !make_tmap(&a.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, D, V, D, BK, BN))
     return CCE_ERR_CUDA;
   a.tmOut = a.tmA;  // unused
@@ -677,7 +746,7 @@ cce_status cce_forward_ex(const void* E, const void* C, const int64_t* x, int64_
   a.k_blocks = static_cast<int>(cdiv(D, BK));
   a.splits = W.S;
   a.v_tiles = static_cast<int>(cdiv(V, BN));
-  a.x = x;
+  a.x = xg;
   a.ignore_index = ignore_index;
   a.part_m = reinterpret_cast<float*>(ws + W.part_m);
   a.part_s = reinterpret_cast<float*>(ws + W.part_s);
@@ -686,6 +755,7 @@ cce_status cce_forward_ex(const void* E, const void* C, const int64_t* x, int64_
   a.inv_softcap = softcap > 0.0f ? 1.0f / softcap : 0.0f;
   a.dev_err = dev_err;
   a.counter = reinterpret_cast<int*>(ws + W.counter);
+  a.n_dev = count;  // null without compaction: all N rows
   const int units = a.n_blocks * a.splits;
   a.items = units;
   {
@@ -698,10 +768,13 @@ cce_status cce_forward_ex(const void* E, const void* C, const int64_t* x, int64_
   }
   {
     PhaseScope ps(1, s);
-    float* loss_rows = (reduction == CCE_RED_NONE) ? loss : nullptr;
+    float* lse_out = compact ? reinterpret_cast<float*>(ws + W.lsec) : lse;
+    float* loss_rows = (reduction == CCE_RED_NONE) ? (compact ? reinterpret_cast<float*>(ws + W.lossc) : loss)
+                                                   : nullptr;
     combine_kernel<<<W.nblk, COMBINE_THREADS, 0, s>>>(
-        a.part_m, a.part_s, a.tgt, x, a.N, W.S, a.V, static_cast<long long>(ignore_index), reduction, lse,
-        loss_rows, reinterpret_cast<double*>(ws + W.blk_sum), reinterpret_cast<int*>(ws + W.blk_cnt), dev_err);
+        a.part_m, a.part_s, a.tgt, xg, a.N, W.S, a.V, static_cast<long long>(ignore_index), reduction, lse_out,
+        loss_rows, reinterpret_cast<double*>(ws + W.blk_sum), reinterpret_cast<int*>(ws + W.blk_cnt), dev_err,
+        count, 0);
     g_launches++;
     if (reduction != CCE_RED_NONE) {
       finish_loss_kernel<<<1, COMBINE_THREADS, 0, s>>>(reinterpret_cast<double*>(ws + W.blk_sum),
@@ -709,10 +782,34 @@ cce_status cce_forward_ex(const void* E, const void* C, const int64_t* x, int64_
                                                        loss);
       g_launches++;
     }
+    if (compact) {  // back to the original rows; rows that took no part get 0
+      scatter_rows_kernel<<<static_cast<unsigned>(std::min<int64_t>(int64_t(sms) * 8, cdiv(N, 256))), 256, 0, s>>>(
+          lse_out, loss_rows, pos, static_cast<int>(N), lse, reduction == CCE_RED_NONE ? loss : nullptr);
+      g_launches++;
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_status(e);
   }
   return CCE_OK;
+}
+
+cce_status cce_forward_ex(const void* E, const void* C, const int64_t* x, int64_t N, int64_t D, int64_t V,
+                          int64_t ignore_index, int reduction, float softcap, float* loss, float* lse,
+                          void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream) {
+  return forward_impl(E, C, x, N, D, V, ignore_index, reduction, softcap, 0, loss, lse, workspace, ws_bytes, dev_err,
+                      stream);
+}
+
+cce_status cce_forward_ex2(const void* E, const void* C, const int64_t* x, int64_t N, int64_t D, int64_t V,
+                           int64_t ignore_index, int reduction, float softcap, int flags, float* loss, float* lse,
+                           void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream) {
+  return forward_impl(E, C, x, N, D, V, ignore_index, reduction, softcap, flags, loss, lse, workspace, ws_bytes,
+                      dev_err, stream);
+}
+
+size_t cce_forward_workspace_bytes_ex(int64_t N, int64_t D, int64_t V, int flags) {
+  if (!sizes_ok(N, D, V) || (flags & ~CCE_FWD_SKIP_IGNORED)) return 0;
+  return fwd_layout(N, V, D, (flags & CCE_FWD_SKIP_IGNORED) != 0).total;
 }
 
 cce_status cce_backward(const void* E, const void* C, const int64_t* x, const float* lse, const float* grad_out,
@@ -941,7 +1038,11 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int* counters = reinterpret_cast<int*>(ws + W.counters);
   int* count = reinterpret_cast<int*>(ws + W.count);
-  float* lse_all = lse ? lse : reinterpret_cast<float*>(ws + W.lse);
+  int* pos = reinterpret_cast<int*>(ws + W.pos);
+  int* ridx = reinterpret_cast<int*>(ws + W.ridx);
+  int64_t* xc = reinterpret_cast<int64_t*>(ws + W.xc);
+  uint16_t* Ecmp = reinterpret_cast<uint16_t*>(ws + W.ec);
+  float* lsec = reinterpret_cast<float*>(ws + W.lse);  // LSE of the compact rows
   double* blk_sum = reinterpret_cast<double*>(ws + W.blk_sum);
   int* blk_cnt = reinterpret_cast<int*>(ws + W.blk_cnt);
   uint16_t* stage = reinterpret_cast<uint16_t*>(ws + W.stage);
@@ -952,20 +1053,31 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
   float* dcacc = reinterpret_cast<float*>(ws + W.dcacc);
   const bool filter_de = (filter_flags & CCE_FILTER_DE) != 0, filter_dc = (filter_flags & CCE_FILTER_DC) != 0;
   const bool multi = W.nchunks > 1;
-  {
+  {  // the rows that take part, compacted ("Cut Your Losses ...", Table A1: removing ignored tokens)
     PhaseScope ps(2, s);
-    int launched = 0;
     cudaError_t e = cudaMemsetAsync(counters, 0, sizeof(int) * 2 * static_cast<size_t>(W.nchunks), s);
     if (e == cudaSuccess && dev_stats) e = cudaMemsetAsync(dev_stats, 0, 2 * sizeof(int64_t), s);
-    if (e == cudaSuccess) e = launch_count_rows(x, N, V, static_cast<long long>(ignore_index), count, s, &launched);
-    g_launches += static_cast<uint64_t>(launched);
+    if (e != cudaSuccess) return cuda_status(e);
+    compact_kernel<<<1, COMPACT_THREADS, 0, s>>>(x, static_cast<int>(N), static_cast<int>(V),
+                                                 static_cast<long long>(ignore_index), pos, ridx, count, dev_err);
+    g_launches++;
+    const int rows_per_block = 8;
+    const int blocks = static_cast<int>(std::min<int64_t>(int64_t(sms) * 16, cdiv(N, rows_per_block)));
+    gather_rows_kernel<<<std::max(blocks, 1), 32 * rows_per_block, 0, s>>>(
+        static_cast<const uint4*>(E), x, nullptr, nullptr, ridx, count, static_cast<int>(N), static_cast<int>(D),
+        static_cast<long long>(ignore_index), reinterpret_cast<uint4*>(Ecmp), xc, nullptr, nullptr);
+    g_launches++;
+    e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_status(e);
   }
   const bool b3d = D % 64 == 0;
+  // Chunks cover compact rows r0 .. r0 + Nc - 1; how many compact rows exist
+  // is only known on the device, so every launch reads the count and a chunk
+  // past it does nothing (its dC contribution is zero).
   for (int64_t c = 0; c < W.nchunks; ++c) {
     const int64_t r0 = c * W.Nc, rows = std::min(W.Nc, N - r0);
     const int64_t nb = cdiv(rows, BM);
-    const uint16_t* Ec = static_cast<const uint16_t*>(E) + r0 * D;
+    const uint16_t* Ec = Ecmp + r0 * D;
     // (1) logits of the chunk: fold + target capture + staging
     GemmArgs f;
     std::memset(&f, 0, sizeof(f));
@@ -980,8 +1092,10 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
     f.k_blocks = static_cast<int>(cdiv(D, BK));
     f.splits = W.S;
     f.v_tiles = static_cast<int>(cdiv(V, BN));
-    f.items = f.n_blocks * f.splits;
-    f.x = x + r0;
+    f.items = f.n_blocks * f.splits;  // upper bound; the kernel uses the device count
+    f.n_dev = count;
+    f.n_row0 = static_cast<int>(r0);
+    f.x = xc + r0;
     f.ignore_index = ignore_index;
     f.part_m = reinterpret_cast<float*>(ws + W.part_m);
     f.part_s = reinterpret_cast<float*>(ws + W.part_s);
@@ -1001,8 +1115,9 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
     {  // (2) LSE of the chunk's rows and their block sums of the loss
       PhaseScope ps(1, s);
       combine_kernel<<<static_cast<unsigned>(cdiv(rows, COMBINE_THREADS)), COMBINE_THREADS, 0, s>>>(
-          f.part_m, f.part_s, f.tgt, x + r0, f.N, W.S, f.V, static_cast<long long>(ignore_index), reduction,
-          lse_all + r0, nullptr, blk_sum + r0 / COMBINE_THREADS, blk_cnt + r0 / COMBINE_THREADS, dev_err);
+          f.part_m, f.part_s, f.tgt, xc + r0, f.N, W.S, f.V, static_cast<long long>(ignore_index), reduction,
+          lsec + r0, nullptr, blk_sum + r0 / COMBINE_THREADS, blk_cnt + r0 / COMBINE_THREADS, dev_err, count,
+          static_cast<int>(r0));
       g_launches++;
       e = cudaGetLastError();
       if (e != cudaSuccess) return cuda_status(e);
@@ -1010,9 +1125,9 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
     {  // (3) staged logits -> G-hat (bf16, in place) and the filter votes
       PhaseScope ps(7, s);
       int launched = 0;
-      e = launch_gpass(stage, W.Vp, mtile, rows, V, x + r0, static_cast<long long>(ignore_index), lse_all + r0, count,
-                       reduction, softcap, filter_eps, !(filter_de && filter_dc), bitmap, bitmapT, W.bm_ld, s,
-                       &launched);
+      e = launch_gpass(stage, W.Vp, mtile, rows, V, xc + r0, static_cast<long long>(ignore_index), lsec + r0, count,
+                       reduction, softcap, filter_eps, !(filter_de && filter_dc), bitmap, bitmapT, W.bm_ld, count, r0,
+                       s, &launched);
       g_launches += static_cast<uint64_t>(launched);
       if (e != cudaSuccess) return cuda_status(e);
     }
@@ -1041,7 +1156,9 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
     r.D = static_cast<int>(D);
     r.V = static_cast<int>(V);
     r.n_blocks = static_cast<int>(nb);
-    r.x = x + r0;
+    r.n_dev = count;
+    r.n_row0 = static_cast<int>(r0);
+    r.x = xc + r0;
     r.ignore_index = ignore_index;
     r.filter_de = filter_de ? 1 : 0;
     r.filter_dc = filter_dc ? 1 : 0;
@@ -1075,7 +1192,7 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
     }
     if (dev_stats) {
       int launched = 0;
-      e = launch_stats_add(bitmap, nb, cdiv(V, 128), W.bm_ld, dev_stats, s, &launched);
+      e = launch_stats_add(bitmap, count, r0, rows, cdiv(V, 128), W.bm_ld, dev_stats, s, &launched);
       g_launches += static_cast<uint64_t>(launched);
       if (e != cudaSuccess) return cuda_status(e);
     }
@@ -1084,8 +1201,13 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
     PhaseScope ps(5, s);
     finish_loss_kernel<<<1, COMBINE_THREADS, 0, s>>>(blk_sum, blk_cnt, W.nblk, reduction, loss);
     g_launches++;
+    if (lse) {  // back to the original rows; rows that took no part get 0
+      scatter_rows_kernel<<<static_cast<unsigned>(std::min<int64_t>(int64_t(sms) * 8, cdiv(N, 256))), 256, 0, s>>>(
+          lsec, nullptr, pos, static_cast<int>(N), lse, nullptr);
+      g_launches++;
+    }
     int launched = 0;
-    cudaError_t e = launch_finalize_de_slabs(deacc, W.Sde, W.slab, N, D, dE, s, sms, &launched);
+    cudaError_t e = launch_finalize_de_slabs(deacc, W.Sde, W.slab, N, D, pos, dE, s, sms, &launched);
     if (e == cudaSuccess && multi) e = launch_to_bf16(dcacc, V * D, dC, s, sms, &launched);
     g_launches += static_cast<uint64_t>(launched);
     if (e == cudaSuccess) e = cudaGetLastError();

@@ -4,9 +4,8 @@
 // logits (fp16, minus each row's max over each 32-column chunk); here they
 // become the weighted logit gradient G-hat in bf16, in place, with the
 // 128 x 128 filter votes ("Cut Your Losses in Large-Vocabulary Language
-// Models", "Gradient Filtering").  Also: the count of rows that take part,
-// the dE / dC finalisation, the filter statistics and the scaling by the
-// upstream gradient.
+// Models", "Gradient Filtering").  Also: the dE / dC finalisation, the filter
+// statistics and the scaling by the upstream gradient.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -29,24 +28,6 @@ __device__ __forceinline__ float ex2f(float v) {
   return r;
 }
 
-// Rows that take part: target in [0, V) and not ignore_index.  One block.
-__global__ void count_rows_kernel(const int64_t* __restrict__ x, int N, int V, long long ignore_index,
-                                  int* __restrict__ count) {
-  __shared__ int part[1024];
-  int c = 0;
-  for (int i = threadIdx.x; i < N; i += blockDim.x) {
-    const long long t = static_cast<long long>(x[i]);
-    c += (t != ignore_index && t >= 0 && t < V) ? 1 : 0;
-  }
-  part[threadIdx.x] = c;
-  __syncthreads();
-  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
-    if (static_cast<int>(threadIdx.x) < w) part[threadIdx.x] += part[threadIdx.x + w];
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) *count = part[0];
-}
-
 // One 128-row x 128-column tile per block (256 threads: 16 threads of eight
 // columns per row, 16 rows per pass, 8 passes).  G = exp(a - LSE) - onehot
 // with a = staged value + the row's max over its 32-column chunk, computed as
@@ -62,8 +43,15 @@ __global__ void __launch_bounds__(256, CAP ? 3 : 4) gpass_kernel(uint16_t* __res
                                                     const float* __restrict__ lse, const int* __restrict__ count,
                                                     int reduction, float softcap, float eps, int store_skipped,
                                                     uint8_t* __restrict__ bitmap, uint8_t* __restrict__ bitmapT,
-                                                    int bm_ld, int n_blocks) {
+                                                    int bm_ld, int n_blocks, const int* __restrict__ n_dev,
+                                                    int n_row0) {
   const int vt = blockIdx.x, tb = blockIdx.y;
+  // Compact rows that exist (their count is in device memory): row blocks
+  // past them are never read and get no survival byte.  Inside the last
+  // block the rows past the count are zero rows with an ignored target, so
+  // they get G = 0 below (the gradient GEMM reads them as part of its K).
+  const int nrows = n_dev ? max(0, min(rows, *n_dev - n_row0)) : rows;
+  if (tb * 128 >= nrows) return;
   const int c8 = threadIdx.x & 15;
   const int r_in = threadIdx.x >> 4;
   const int col0 = vt * 128 + c8 * 8;
@@ -135,17 +123,25 @@ __global__ void __launch_bounds__(256, CAP ? 3 : 4) gpass_kernel(uint16_t* __res
   }
 }
 
-// dE[r] = bf16(sum over the S slabs of acc[s * slab + r]), slabs in order.
+// dE[r] = bf16(sum over the S slabs of acc[s * slab + p]), slabs in order,
+// where p = pos[r] is row r's compact row (rows with p < 0 took no part: +0).
 __global__ void finalize_de_slabs_kernel(const float4* __restrict__ acc, int S, int slab, int N, int D,
-                                         uint2* __restrict__ dE) {
+                                         const int* __restrict__ pos, uint2* __restrict__ dE) {
   const size_t per_row = static_cast<size_t>(D) / 4;
   const size_t total = static_cast<size_t>(N) * per_row;
   const size_t slab4 = static_cast<size_t>(slab) * per_row;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    float4 v = acc[i];
+    const size_t row = i / per_row;
+    const int p = pos[row];
+    if (p < 0) {
+      dE[i] = make_uint2(0u, 0u);
+      continue;
+    }
+    const size_t at = static_cast<size_t>(p) * per_row + (i - row * per_row);
+    float4 v = acc[at];
     for (int s = 1; s < S; ++s) {
-      const float4 u = acc[s * slab4 + i];
+      const float4 u = acc[s * slab4 + at];
       v.x += u.x;
       v.y += u.y;
       v.z += u.z;
@@ -175,11 +171,13 @@ __global__ void to_bf16_kernel(const float4* __restrict__ src, size_t n4, uint2*
 }
 
 // stats[0] += tiles, stats[1] += skipped tiles of one chunk's survival map
-// (nb rows of ncols bytes, pitch bm_ld).  One block; launches run in stream
-// order, so the sums are deterministic.
-__global__ void stats_add_kernel(const uint8_t* __restrict__ bitmap, int nb, int ncols, int bm_ld,
-                                 int64_t* __restrict__ stats) {
+// (ceil(rows / 128) rows of ncols bytes, pitch bm_ld; rows = clamp(*n_dev -
+// n_row0, 0, max_rows)).  One block; launches run in stream order, so the
+// sums are deterministic.
+__global__ void stats_add_kernel(const uint8_t* __restrict__ bitmap, const int* __restrict__ n_dev, int n_row0,
+                                 int max_rows, int ncols, int bm_ld, int64_t* __restrict__ stats) {
   __shared__ long long sz[1024];
+  const int nb = (max(0, min(max_rows, *n_dev - n_row0)) + 127) / 128;
   const long long n = static_cast<long long>(nb) * ncols;
   long long z = 0;
   for (long long i = threadIdx.x; i < n; i += blockDim.x) z += bitmap[(i / ncols) * bm_ld + (i % ncols)] == 0 ? 1 : 0;
@@ -224,37 +222,32 @@ int grid_cap(size_t work, int per_block, int cap) {
 
 }  // namespace
 
-cudaError_t launch_count_rows(const int64_t* x, int64_t N, int64_t V, long long ignore_index, int* count,
-                              cudaStream_t s, int* launches) {
-  count_rows_kernel<<<1, 1024, 0, s>>>(x, static_cast<int>(N), static_cast<int>(V), ignore_index, count);
-  ++*launches;
-  return cudaGetLastError();
-}
-
 cudaError_t launch_gpass(uint16_t* stage, int64_t pitch, const float* mtile, int64_t rows, int64_t V,
                          const int64_t* x, long long ignore_index, const float* lse, const int* count, int reduction,
                          float softcap, float eps, bool store_skipped, uint8_t* bitmap, uint8_t* bitmapT,
-                         int64_t bm_ld, cudaStream_t s, int* launches) {
+                         int64_t bm_ld, const int* n_dev, int64_t n_row0, cudaStream_t s, int* launches) {
   const int nb = static_cast<int>((rows + 127) / 128);
   const dim3 grid(static_cast<unsigned>((V + 127) / 128), static_cast<unsigned>(nb));
   if (softcap > 0.0f) {
     gpass_kernel<true><<<grid, 256, 0, s>>>(stage, static_cast<int>(pitch), mtile, static_cast<int>(rows),
                                             static_cast<int>(V), x, ignore_index, lse, count, reduction, softcap, eps,
-                                            store_skipped ? 1 : 0, bitmap, bitmapT, static_cast<int>(bm_ld), nb);
+                                            store_skipped ? 1 : 0, bitmap, bitmapT, static_cast<int>(bm_ld), nb, n_dev,
+                                            static_cast<int>(n_row0));
   } else {
     gpass_kernel<false><<<grid, 256, 0, s>>>(stage, static_cast<int>(pitch), mtile, static_cast<int>(rows),
                                              static_cast<int>(V), x, ignore_index, lse, count, reduction, softcap,
-                                             eps, store_skipped ? 1 : 0, bitmap, bitmapT, static_cast<int>(bm_ld), nb);
+                                             eps, store_skipped ? 1 : 0, bitmap, bitmapT, static_cast<int>(bm_ld), nb,
+                                             n_dev, static_cast<int>(n_row0));
   }
   ++*launches;
   return cudaGetLastError();
 }
 
-cudaError_t launch_finalize_de_slabs(const float* acc, int S, int64_t slab, int64_t N, int64_t D, void* dE,
-                                     cudaStream_t s, int sms, int* launches) {
+cudaError_t launch_finalize_de_slabs(const float* acc, int S, int64_t slab, int64_t N, int64_t D, const int* pos,
+                                     void* dE, cudaStream_t s, int sms, int* launches) {
   const size_t n4 = static_cast<size_t>(N) * D / 4;
   finalize_de_slabs_kernel<<<grid_cap(n4, 256, sms * 8), 256, 0, s>>>(
-      reinterpret_cast<const float4*>(acc), S, static_cast<int>(slab), static_cast<int>(N), static_cast<int>(D),
+      reinterpret_cast<const float4*>(acc), S, static_cast<int>(slab), static_cast<int>(N), static_cast<int>(D), pos,
       static_cast<uint2*>(dE));
   ++*launches;
   return cudaGetLastError();
@@ -268,10 +261,10 @@ cudaError_t launch_to_bf16(const float* src, int64_t n, void* dst, cudaStream_t 
   return cudaGetLastError();
 }
 
-cudaError_t launch_stats_add(const uint8_t* bitmap, int64_t nb, int64_t ncols, int64_t bm_ld, int64_t* stats,
-                             cudaStream_t s, int* launches) {
-  stats_add_kernel<<<1, 1024, 0, s>>>(bitmap, static_cast<int>(nb), static_cast<int>(ncols), static_cast<int>(bm_ld),
-                                      stats);
+cudaError_t launch_stats_add(const uint8_t* bitmap, const int* n_dev, int64_t n_row0, int64_t max_rows,
+                             int64_t ncols, int64_t bm_ld, int64_t* stats, cudaStream_t s, int* launches) {
+  stats_add_kernel<<<1, 1024, 0, s>>>(bitmap, n_dev, static_cast<int>(n_row0), static_cast<int>(max_rows),
+                                      static_cast<int>(ncols), static_cast<int>(bm_ld), stats);
   ++*launches;
   return cudaGetLastError();
 }

@@ -73,12 +73,12 @@ struct Dims {
 
 template <int MODE>
 __device__ __forceinline__ Dims dims_of(const GemmArgs& a) {
-  const int n = a.n_dev ? *a.n_dev : a.N;
+  const int n = a.n_dev ? max(0, min(a.N, *a.n_dev - a.n_row0)) : a.N;
   Dims d;
   d.nb = (n + BM - 1) / BM;
   d.dc_kb = (n + BK - 1) / BK;
   if constexpr (MODE == MODE_FWD || MODE == MODE_FWD_STAGE) {
-    d.items = a.items;
+    d.items = a.n_dev ? d.nb * a.splits : a.items;
   } else if constexpr (MODE == MODE_BWD_G) {
     d.items = d.nb * a.v_tiles;
   } else {
@@ -91,7 +91,8 @@ __device__ __forceinline__ Dims dims_of(const GemmArgs& a) {
 template <int MODE, typename F>
 __device__ __forceinline__ bool for_each_tile_of_item(const GemmArgs& a, const Dims& dm, int item, F&& f) {
   if constexpr (MODE == MODE_FWD || MODE == MODE_FWD_STAGE) {
-    const int m = item % a.n_blocks, s = item / a.n_blocks;
+    const int nbx = a.n_dev ? dm.nb : a.n_blocks;  // items only exist when nbx > 0
+    const int m = item % nbx, s = item / nbx;
     const int t0 = static_cast<int>(static_cast<long long>(s) * a.v_tiles / a.splits);
     const int t1 = static_cast<int>(static_cast<long long>(s + 1) * a.v_tiles / a.splits);
     for (int t = t0; t < t1; ++t) {

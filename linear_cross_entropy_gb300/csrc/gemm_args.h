@@ -68,10 +68,12 @@ struct GemmArgs {
   // dynamic scheduling: work items are handed out by atomicAdd on *counter
   int* counter;     // zeroed before the launch
   int items;        // FWD: work items (BWD_G / GRAD derive theirs from the row count)
-  // BWD_G / GRAD: device-side number of token rows taking part (the backward
-  // compacts away ignored rows on the device); N and n_blocks above are the
-  // allocated upper bounds.  Null: all N rows.
+  // Device-side number of token rows taking part (rows that take no part are
+  // compacted away on the device); the launch covers rows n_row0 .. of that
+  // compact list, at most N of them: n = clamp(*n_dev - n_row0, 0, N).  N and
+  // n_blocks above are the upper bounds.  Null: all N rows.
   const int* n_dev;
+  int n_row0;
   const int64_t* x;
   long long ignore_index;
   float* part_m;  // FWD: [splits][N] running max (log2 units)

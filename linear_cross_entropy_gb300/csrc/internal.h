@@ -40,21 +40,21 @@ cudaError_t launch_gather_vocab_rows(const void* src, const int* rows, int64_t c
                                      void* dst, cudaStream_t s, int sms, int* launches);
 
 // Single call (cce_flce.cu).
-cudaError_t launch_count_rows(const int64_t* x, int64_t N, int64_t V, long long ignore_index, int* count,
-                              cudaStream_t s, int* launches);
-// Staged fp16 logits (minus the 32-column chunk maxima in mtile) of `rows`
-// rows -> bf16 G-hat in place, and
+// Staged fp16 logits (minus the 32-column chunk maxima in mtile) of the
+// chunk's rows -> bf16 G-hat in place, and
 // the chunk's survival map (bitmap [ceil(rows/128)][bm_ld], bitmapT
 // [bm_ld][ceil(rows/128)]).
 cudaError_t launch_gpass(uint16_t* stage, int64_t pitch, const float* mtile, int64_t rows, int64_t V,
                          const int64_t* x, long long ignore_index, const float* lse, const int* count, int reduction,
                          float softcap, float eps, bool store_skipped, uint8_t* bitmap, uint8_t* bitmapT,
-                         int64_t bm_ld, cudaStream_t s, int* launches);
-cudaError_t launch_finalize_de_slabs(const float* acc, int S, int64_t slab, int64_t N, int64_t D, void* dE,
-                                     cudaStream_t s, int sms, int* launches);
+                         int64_t bm_ld, const int* n_dev, int64_t n_row0, cudaStream_t s, int* launches);
+// the chunk has clamp(*n_dev - n_row0, 0, rows) rows (rows when n_dev is null);
+// rows is also the pitch of mtile.
+cudaError_t launch_finalize_de_slabs(const float* acc, int S, int64_t slab, int64_t N, int64_t D, const int* pos,
+                                     void* dE, cudaStream_t s, int sms, int* launches);
 cudaError_t launch_to_bf16(const float* src, int64_t n, void* dst, cudaStream_t s, int sms, int* launches);
-cudaError_t launch_stats_add(const uint8_t* bitmap, int64_t nb, int64_t ncols, int64_t bm_ld, int64_t* stats,
-                             cudaStream_t s, int* launches);
+cudaError_t launch_stats_add(const uint8_t* bitmap, const int* n_dev, int64_t n_row0, int64_t max_rows,
+                             int64_t ncols, int64_t bm_ld, int64_t* stats, cudaStream_t s, int* launches);
 cudaError_t launch_scale_bf16(void* a, int64_t na, void* b, int64_t nb, const float* g, cudaStream_t s, int sms,
                               int* launches);
 

@@ -96,19 +96,21 @@ def test_sorted_workspace_adds_keys_order_and_two_chunks(lib, N, D, V):
 
 @pytest.mark.parametrize("N,D,V", [(4096, 896, 151936), (16384, 4096, 128256), (300, 136, 5000)])
 def test_single_call_workspace(lib, N, D, V):
-    """The single call's workspace holds one chunk of fp16 staged logits
-    within the staging budget (whole 256-row chunks, at least one), dE slabs
-    and, with several chunks, an fp32 dC accumulator."""
+    """The single call's workspace holds the compacted rows (E and x), one
+    chunk of fp16 staged logits within the staging budget (whole 256-row
+    chunks, at least one) with its 32-column maxima, dE slabs and, with
+    several chunks, an fp32 dC accumulator."""
     vp_ = -(-V // 256) * 256
     for budget in (0, 64 << 20, 1):
         b = lib.cce_loss_and_grad_workspace_bytes(N, D, V, budget)
         cap = (2 << 30) if budget == 0 else budget
         nc = min(max(256, cap // (vp_ * 2) // 256 * 256), -(-N // 256) * 256)
         chunks = -(-N // nc)
-        assert b >= nc * vp_ * 2 + N * D * 4 + (V * D * 4 if chunks > 1 else 0)
+        assert b >= nc * vp_ * 2 + N * D * 4 + N * D * 2 + (V * D * 4 if chunks > 1 else 0)
         assert b <= nc * vp_ * 2 + 8 * (-(-N // 128) * 128) * D * 4 + (V * D * 4 if chunks > 1 else 0) \
-            + 4 * (vp_ // 256) * nc + 8 * (vp_ // 1024 + 1) * nc + 16 * N + 3 * (nc // 128 + 1) * (V // 128 + 1) \
-            + 64 * 1024  # tile maxima, split partials, LSE and loss blocks, survival maps, alignment
+            + N * D * 2 + 4 * (vp_ // 32) * nc + 8 * (vp_ // 1024 + 1) * nc + 32 * N \
+            + 3 * (nc // 128 + 1) * (V // 128 + 1) \
+            + 64 * 1024  # compact rows, chunk maxima, split partials, LSE, maps and loss blocks, survival maps
 
 
 def test_workspace_rejects_bad_sizes(lib):
@@ -187,6 +189,11 @@ def test_extended_entry_points_reject_bad_options(lib):
     assert lib.cce_loss_and_grad(*fargs, 0, 0.0, 2.0 ** -12, 3, 0, *ftail) == 4   # reduction none
     assert lib.cce_loss_and_grad(*fargs, 2, 0.0, 2.0 ** -12, 4 | 3, 0, *ftail) == 4  # sorting not offered
     assert lib.cce_loss_and_grad(*fargs, 2, -1.0, 2.0 ** -12, 3, 0, *ftail) == 4  # negative softcap
+    assert lib.cce_forward_ex2(*args, 0.0, 2, vp(FAKE), vp(FAKE), vp(FAKE), 1 << 40, vp(0), vp(0)) == 4  # bad flag
+    assert lib.cce_forward_workspace_bytes_ex(256, 128, 4096, 2) == 0
+    assert lib.cce_forward_workspace_bytes_ex(256, 128, 4096, 0) == lib.cce_forward_workspace_bytes(256, 128, 4096)
+    assert lib.cce_forward_workspace_bytes_ex(256, 128, 4096, 1) >= \
+        lib.cce_forward_workspace_bytes(256, 128, 4096) + 256 * 128 * 2 + 256 * 24
     assert lib.cce_backward_ex(*bargs, 0.0, 2.0 ** -12, 8, *tail) == 4      # unknown flag bit
     assert lib.cce_backward_ex(*bargs, 0.0, 2.0 ** -12, 4 | 16, *tail) == 4  # sort plus an unknown bit
     assert lib.cce_backward_ex(*bargs, -3.0, 2.0 ** -12, 3, *tail) == 4     # negative softcap

@@ -10,8 +10,8 @@ import torch
 
 import cce_workloads as W
 import oracle as O
-from tests.gpu_util import (TOL_GRAD, TOL_GRAD_FILTERED, assert_forward_close, assert_grads_close, make,
-                            oracle_full, rel_fro, run_cuda)
+from tests.gpu_util import (TOL_GRAD, TOL_GRAD_FILTERED, TOL_LSE, assert_forward_close, assert_grads_close,
+                            bf16_to_f64, make, oracle_full, rel_fro, run_cuda, to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -248,3 +248,33 @@ def test_mostly_ignored_batch_is_compacted():
         if eps:
             assert rel_fro(got["dE"], ref["dE_f"]) <= TOL_GRAD
             assert got["stats"]["tiles"] == ref["keep"].size
+
+
+@pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
+def test_forward_skipping_ignored_rows(reduction):
+    """CCE_FWD_SKIP_IGNORED: the GEMM runs over the compacted rows only; the
+    loss is the oracle's, the LSE of rows that take part too, and the other
+    rows read 0; the backward fed with that LSE gives the oracle's gradients."""
+    import linear_cross_entropy_gb300 as cce
+    w = W.small("skip", 700, 136, 5000, ignore_frac=0.3, reduction=reduction)
+    E_bits, C_bits, x = W.make_inputs(w)
+    x = x.copy()
+    x[[3, 4, 5]] = O.IGNORE_INDEX
+    E, C, xt = to_device(E_bits, C_bits, x)
+    loss, lse = cce.cce_forward(E, C, xt, reduction=reduction, skip_ignored=True)
+    g = torch.ones(x.shape[0] if reduction == "none" else 1, dtype=torch.float32, device="cuda")
+    dE, dC = cce.cce_backward(E, C, xt, lse, g, reduction=reduction, filter_eps=0.0)
+    torch.cuda.synchronize()
+    ref = oracle_full(E_bits, C_bits, x, reduction=reduction)
+    valid = x != O.IGNORE_INDEX
+    lse_got = lse.double().cpu().numpy()
+    err = np.abs(lse_got[valid] - ref["lse"][valid]) / np.abs(ref["lse"][valid])
+    assert err.max() <= TOL_LSE and np.all(lse_got[~valid] == 0.0)
+    if reduction == "none":
+        rows = loss.double().cpu().numpy()
+        assert np.all(np.abs(rows - ref["loss_rows"]) <= TOL_LSE * np.abs(ref["lse"]) + 1e-30)
+        assert np.all(rows[~valid] == 0.0)
+    else:
+        assert abs(loss.item() - float(ref["loss"])) <= TOL_LSE * abs(float(ref["loss"]))
+    got = {"dE": bf16_to_f64(dE), "dC": bf16_to_f64(dC), "dE_raw": dE}
+    assert_grads_close(got, ref["dE"], ref["dC"], TOL_GRAD, x)

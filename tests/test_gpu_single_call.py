@@ -2,13 +2,14 @@
 "fused-linear-cross-entropy" page, section "2. Fused Linear Cross-Entropy
 (FLCE)") against the fp64 oracle's loss_and_grad, through the C ABI.
 
-Covered: both reductions, ignored rows, a ragged vocabulary (V not a
-multiple of 256), several token chunks (dC accumulated in fp32 over chunks,
-dE rows of every chunk), the vocabulary split of the dE tiles, the filter on
-inputs where it bites (gradients within the filtered tolerance of the
-oracle's filtered gradients, skipped-tile count against the oracle's map),
-softcapping, the autograd wrapper with an upstream gradient other than 1,
-and determinism.
+Covered: both reductions, ignored rows (compacted away before the GEMMs: the
+LSE is checked on the rows that take part and must be 0 on the others), a
+ragged vocabulary (V not a multiple of 256), several token chunks (dC
+accumulated in fp32 over chunks, dE rows of every chunk), the vocabulary
+split of the dE tiles, the filter on inputs where it bites (gradients within
+the filtered tolerance of the oracle's filtered gradients, skipped-tile count
+against the oracle's map), softcapping, the autograd wrapper with an upstream
+gradient other than 1, a fully ignored batch, and determinism.
 """
 import numpy as np
 import pytest
@@ -39,8 +40,10 @@ def _run(E_bits, C_bits, x, **kw):
 
 
 def _check(got, ref, x, tol, ignore_index=-100):
-    lse_err = np.abs(got["lse"] - ref["lse"]) / np.abs(ref["lse"])
+    part = (x != ignore_index) & (x >= 0) & (x < ref["dC"].shape[0])
+    lse_err = np.abs(got["lse"][part] - ref["lse"][part]) / np.abs(ref["lse"][part])
     assert lse_err.max() <= TOL_LSE, f"LSE rel err {lse_err.max():.3e}"
+    assert np.all(got["lse"][~part] == 0.0)
     assert abs(got["loss"] - ref["loss"]) <= TOL_LSE * abs(ref["loss"]), (got["loss"], ref["loss"])
     eE, eC = rel_fro(got["dE"], ref["dE"]), rel_fro(got["dC"], ref["dC"])
     assert eE <= tol and eC <= tol, f"dE {eE:.3e} dC {eC:.3e}"
@@ -115,6 +118,15 @@ def test_single_call_is_deterministic():
     assert a["loss"] == b["loss"] and np.array_equal(a["lse"], b["lse"])
     assert torch.equal(a["dE_raw"].view(torch.int16), b["dE_raw"].view(torch.int16))
     assert np.array_equal(a["dC"], b["dC"]) and a["stats"] == b["stats"]
+
+
+def test_single_call_fully_ignored_batch():
+    E_bits, C_bits, x = W.make_inputs(W.small("z", 300, 64, 3000))
+    x = np.full_like(x, -100)
+    got = _run(E_bits, C_bits, x, reduction="mean", max_staging_bytes=256 * 3072 * 2)
+    assert got["loss"] == 0.0 and np.all(got["lse"] == 0.0)
+    assert np.all(got["dE"] == 0.0) and np.all(got["dC"] == 0.0)
+    assert got["stats"]["tiles"] == 0
 
 
 def test_single_call_rejects_reduction_none():
