@@ -283,7 +283,8 @@ cce_status cce_vocab_order(const float* keys, int64_t V, int32_t* perm, void* wo
  * in cce_backward_ex; CCE_SORT_VOCAB is not accepted) works on tiles of 128
  * consecutive compact rows x 128 vocabulary entries, as in cce_backward.
  * With more than one chunk dC is accumulated in an fp32 buffer in the
- * workspace; dE always goes through fp32 slabs.
+ * workspace (the last chunk adds it and writes bf16); dE always goes through
+ * fp32 slabs.
  *
  *   loss   [1] fp32 (written).
  *   lse    [N] fp32 (written) or NULL: the LSE of rows that take part, 0 on

@@ -1143,7 +1143,10 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
       ok = ok && make_tmap(&r.tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Ec, D, rows, D, 64, 64) &&
            make_tmap(&r.tmB2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, D, V, D, 64, 64);
     }
-    if (multi) {
+    // dC: fp32 accumulator for all chunks but the last, which adds the
+    // accumulator and writes bf16 (a single chunk writes bf16 directly)
+    const bool last = c == W.nchunks - 1;
+    if (!last) {
       ok = ok && make_tmap(&r.tmOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dcacc, D, V, D, 32, 32);
     } else {
       ok = ok && make_tmap(&r.tmOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dC, D, V, D, 32, 32,
@@ -1179,8 +1182,9 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
     r.de_slab = static_cast<int>(W.slab);
     r.de_row0 = static_cast<int>(r0);
     r.first_chunk = 1;  // every dE slab row is written once
-    r.dc_f32 = multi ? 1 : 0;
-    r.dc_reduce = (multi && c > 0) ? 1 : 0;
+    r.dc_f32 = last ? 0 : 1;
+    r.dc_reduce = (!last && c > 0) ? 1 : 0;
+    r.dc_acc = (last && multi) ? dcacc : nullptr;
     r.dc_first = 2 * nb >= W.kps ? 1 : 0;  // longest tiles first
     r.counter = counters + 2 * c + 1;
     {
@@ -1208,7 +1212,6 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
     }
     int launched = 0;
     cudaError_t e = launch_finalize_de_slabs(deacc, W.Sde, W.slab, N, D, pos, dE, s, sms, &launched);
-    if (e == cudaSuccess && multi) e = launch_to_bf16(dcacc, V * D, dC, s, sms, &launched);
     g_launches += static_cast<uint64_t>(launched);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_status(e);

@@ -156,20 +156,6 @@ __global__ void finalize_de_slabs_kernel(const float4* __restrict__ acc, int S, 
   }
 }
 
-// fp32 -> bf16 (round to nearest even), four values per thread.
-__global__ void to_bf16_kernel(const float4* __restrict__ src, size_t n4, uint2* __restrict__ dst) {
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const float4 v = src[i];
-    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
-    const __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
-    uint2 out;
-    std::memcpy(&out.x, &lo, 4);
-    std::memcpy(&out.y, &hi, 4);
-    dst[i] = out;
-  }
-}
-
 // stats[0] += tiles, stats[1] += skipped tiles of one chunk's survival map
 // (ceil(rows / 128) rows of ncols bytes, pitch bm_ld; rows = clamp(*n_dev -
 // n_row0, 0, max_rows)).  One block; launches run in stream order, so the
@@ -249,14 +235,6 @@ cudaError_t launch_finalize_de_slabs(const float* acc, int S, int64_t slab, int6
   finalize_de_slabs_kernel<<<grid_cap(n4, 256, sms * 8), 256, 0, s>>>(
       reinterpret_cast<const float4*>(acc), S, static_cast<int>(slab), static_cast<int>(N), static_cast<int>(D), pos,
       static_cast<uint2*>(dE));
-  ++*launches;
-  return cudaGetLastError();
-}
-
-cudaError_t launch_to_bf16(const float* src, int64_t n, void* dst, cudaStream_t s, int sms, int* launches) {
-  const size_t n4 = static_cast<size_t>(n) / 4;
-  to_bf16_kernel<<<grid_cap(n4, 256, sms * 8), 256, 0, s>>>(reinterpret_cast<const float4*>(src), n4,
-                                                            static_cast<uint2*>(dst));
   ++*launches;
   return cudaGetLastError();
 }

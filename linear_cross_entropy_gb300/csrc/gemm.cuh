@@ -855,16 +855,38 @@ __device__ __forceinline__ void epi_dc(const GemmArgs& a, const Dims& dm, const 
   }
   // boxes that start inside the chunk and dC (no store may start outside the tensor)
   const int nbox = (ly < a.chunk_w) ? min(a.bn / 32, (a.D - x0 + 31) / 32) : 0;
+  // dc_acc (single call, last token chunk): add the fp32 sum of the earlier
+  // chunks, read by each lane for its own row, before rounding to bf16
+  const int arow = ly + static_cast<int>(lane);
+  const float* accrow = (a.dc_acc && arow < a.chunk_w) ? a.dc_acc + static_cast<size_t>(a.c_row0 + arow) * a.D : nullptr;
 #pragma unroll 1
   for (int j = 0; j < nbox; ++j) {
     const int b = j & 1;
     uint8_t* buf = e.buf + b * 4096;
     staging_acquire(e, b);
     const uint32_t sb = smem_u32(buf);
-    if (!empty) {
+    if (!empty || a.dc_acc) {
       uint32_t r[32];
-      tmem_ld32(tbase + 32 * j, r);
-      tmem_ld_wait();
+      if (!empty) {
+        tmem_ld32(tbase + 32 * j, r);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) r[u] = 0u;
+      }
+      if (accrow) {
+        const int c0 = x0 + 32 * j;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (c0 + 4 * u < a.D) {  // D % 8 == 0: groups of four lie wholly inside or outside
+            const float4 v = *reinterpret_cast<const float4*>(accrow + c0 + 4 * u);
+            r[4 * u + 0] = __float_as_uint(__uint_as_float(r[4 * u + 0]) + v.x);
+            r[4 * u + 1] = __float_as_uint(__uint_as_float(r[4 * u + 1]) + v.y);
+            r[4 * u + 2] = __float_as_uint(__uint_as_float(r[4 * u + 2]) + v.z);
+            r[4 * u + 3] = __float_as_uint(__uint_as_float(r[4 * u + 3]) + v.w);
+          }
+        }
+      }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         st_shared_v4(sb + swz64(lane, u), pack_bf16x2(__uint_as_float(r[8 * u + 0]), __uint_as_float(r[8 * u + 1])),

@@ -106,6 +106,9 @@ struct GemmArgs {
   // stored (dc_reduce = 0) or reduce-added (1), instead of bf16
   int dc_f32;
   int dc_reduce;
+  // GRAD, bf16 dC tiles: when set, the fp32 [V][D] sum of earlier chunks that
+  // each tile adds to its result before rounding (single call, last chunk)
+  const float* dc_acc;
   int32_t* dev_err;
 };
 

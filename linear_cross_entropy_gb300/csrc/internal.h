@@ -52,7 +52,6 @@ cudaError_t launch_gpass(uint16_t* stage, int64_t pitch, const float* mtile, int
 // rows is also the pitch of mtile.
 cudaError_t launch_finalize_de_slabs(const float* acc, int S, int64_t slab, int64_t N, int64_t D, const int* pos,
                                      void* dE, cudaStream_t s, int sms, int* launches);
-cudaError_t launch_to_bf16(const float* src, int64_t n, void* dst, cudaStream_t s, int sms, int* launches);
 cudaError_t launch_stats_add(const uint8_t* bitmap, const int* n_dev, int64_t n_row0, int64_t max_rows,
                              int64_t ncols, int64_t bm_ld, int64_t* stats, cudaStream_t s, int* launches);
 cudaError_t launch_scale_bf16(void* a, int64_t na, void* b, int64_t nb, const float* g, cudaStream_t s, int sms,
