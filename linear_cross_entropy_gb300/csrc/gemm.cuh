@@ -286,15 +286,23 @@ __device__ __forceinline__ void producer_loop(const GemmArgs& a, const SmemLayou
   uint32_t phase = 0;
   uint32_t issued_mask = 0, issued_par = 0;  // per stage: ever issued, parity of last issue
   const Dims dm = dims_of<MODE>(a);
+  // BWD_G: the next work item is fetched while the current one's loads are
+  // issued; the atomic's latency (about a microsecond) would otherwise stall
+  // the pipeline at every boundary of its short one-tile items.  The other
+  // modes fetch when they need one: their items are long, and holding a
+  // reserved item while busy would unbalance the end of a launch.
+  constexpr bool kAhead = MODE == MODE_BWD_G;
+  int next = kAhead ? atomicAdd(a.counter, 1) : 0;
   for (int k = 0;; ++k) {
     const int slot = k % RING;
     if (!wait_bounded(&L.ring_empty[slot], static_cast<uint32_t>(((k / RING) & 1) ^ 1), abort_flag, a.dev_err))
       break;
-    int item = atomicAdd(a.counter, 1);
+    int item = kAhead ? next : atomicAdd(a.counter, 1);
     if (item >= dm.items) item = -1;
     L.ring_ids[slot] = item;
     mbar_arrive(&L.ring_full[slot]);  // release: the id is visible to the waiting consumers
     if (item < 0) break;
+    if (kAhead) next = atomicAdd(a.counter, 1);
     const bool ok = for_each_tile_of_item<MODE>(a, dm, item, [&](const Tile& t) -> bool {
       const int nk = kblocks_of<MODE>(a, dm, t);
       int kb = next_kblock<MODE>(a, t, kblock_begin<MODE>(a, t), nk);
