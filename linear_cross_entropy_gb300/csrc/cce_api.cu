@@ -28,7 +28,7 @@ constexpr size_t ALIGN = 256;         // sub-buffer alignment inside a workspace
 #define CCE_G_CHUNK_BUDGET_MIB 512
 #endif
 constexpr size_t G_CHUNK_BUDGET = size_t(CCE_G_CHUNK_BUDGET_MIB) << 20;  // bytes of the backward G chunk buffer
-constexpr int64_t MIN_CHUNK = 2048, MAX_CHUNK = 32768;
+constexpr int64_t MIN_CHUNK = 2048, MAX_CHUNK = 65536;
 constexpr int COMBINE_THREADS = 256;
 
 std::atomic<uint64_t> g_launches{0};
