@@ -28,11 +28,13 @@ __device__ __forceinline__ float ex2f(float v) {
   return r;
 }
 
-// One 128-row x 128-column tile per block (256 threads: 16 threads of eight
-// columns per row, 16 rows per pass, 8 passes).  G = exp(a - LSE) - onehot
-// with a = staged value + the row's max over its 32-column chunk, computed as
-// exp2(h * log2e + c_row), c_row = (max - LSE) * log2e; rows that take no
-// part get c_row = -inf, so their G is 0.  The vote is any |G| >= eps
+// One 128-row x 128-column tile per block (256 threads).  First the block
+// loads, coalesced, each row's target, LSE and the four 32-column chunk
+// maxima of the tile into shared memory (c_row = (max - LSE) * log2e, -inf
+// for rows that take no part, so their G is 0); then every thread issues its
+// eight independent 16-byte loads of staged values (16 threads of eight
+// columns per row, 16 rows per pass, 8 passes) and computes
+// G = exp2(h * log2e + c_row) - onehot.  The vote is any |G| >= eps
 // (unscaled G, before the softcap slope); the stored value is w * G * slope
 // in bf16.  A tile that both outputs skip is not written back (nothing reads
 // it).
@@ -45,6 +47,9 @@ __global__ void __launch_bounds__(256, CAP ? 3 : 4) gpass_kernel(uint16_t* __res
                                                     uint8_t* __restrict__ bitmap, uint8_t* __restrict__ bitmapT,
                                                     int bm_ld, int n_blocks, const int* __restrict__ n_dev,
                                                     int n_row0) {
+  __shared__ float s_c[4][128];  // c_row per 32-column chunk of the tile
+  __shared__ float s_m[4][128];  // the chunk maxima (softcap slope)
+  __shared__ int s_rel[128];     // target column within the tile, or -1
   const int vt = blockIdx.x, tb = blockIdx.y;
   // Compact rows that exist (their count is in device memory): row blocks
   // past them are never read and get no survival byte.  Inside the last
@@ -52,39 +57,61 @@ __global__ void __launch_bounds__(256, CAP ? 3 : 4) gpass_kernel(uint16_t* __res
   // they get G = 0 below (the gradient GEMM reads them as part of its K).
   const int nrows = n_dev ? max(0, min(rows, *n_dev - n_row0)) : rows;
   if (tb * 128 >= nrows) return;
-  const int c8 = threadIdx.x & 15;
-  const int r_in = threadIdx.x >> 4;
+  const int t = threadIdx.x;
+  {
+    const int r = t & 127, row = tb * 128 + r;
+    const bool ok = row < rows;
+    const long long xr = ok ? static_cast<long long>(x[row]) : ignore_index;
+    const bool part = xr != ignore_index && xr >= 0 && xr < V;
+    const float l = part ? lse[row] : 0.0f;
+    const int c_lo = (t >> 7) * 2;  // threads 0..127: chunks 0, 1; 128..255: chunks 2, 3
+#pragma unroll
+    for (int c = c_lo; c < c_lo + 2; ++c) {
+      const float m = ok ? mtile[static_cast<size_t>(vt * 4 + c) * rows + row] : 0.0f;
+      s_m[c][r] = m;
+      s_c[c][r] = part ? (m - l) * LOG2E_F : -INFINITY;
+    }
+    if (t < 128) {
+      const long long rel = xr - static_cast<long long>(vt) * 128;
+      s_rel[r] = (part && rel >= 0 && rel < 128) ? static_cast<int>(rel) : -1;
+    }
+  }
+  const int c8 = t & 15;
+  const int r_in = t >> 4;
   const int col0 = vt * 128 + c8 * 8;
+  const int ch = c8 >> 2;  // 32-column chunk of these eight columns
+  uint4 h[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int row = tb * 128 + r_in + 16 * k;
+    h[k] = row < rows ? *reinterpret_cast<const uint4*>(stage + static_cast<size_t>(row) * pitch + col0)
+                      : make_uint4(0u, 0u, 0u, 0u);
+  }
+  __syncthreads();
   const bool ragged = col0 + 8 > V;  // only in the last column tile
   const float w = reduction == CCE_RED_SUM ? 1.0f : 1.0f / static_cast<float>(max(*count, 1));
   const float inv_cap = CAP ? 1.0f / softcap : 0.0f;
   float amax = 0.0f;  // largest unscaled |G| this thread saw
-  uint32_t pk[8][4];  // the eight rows' results, bf16 pairs
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    const int row = tb * 128 + r_in + 16 * k;
-    const bool ok = row < rows;
-    const uint4 h = ok ? *reinterpret_cast<const uint4*>(stage + static_cast<size_t>(row) * pitch + col0)
-                       : make_uint4(0u, 0u, 0u, 0u);
-    const long long xr = ok ? static_cast<long long>(x[row]) : ignore_index;
-    const bool part = xr != ignore_index && xr >= 0 && xr < V;
-    const float m = ok ? mtile[static_cast<size_t>(col0 >> 5) * rows + row] : 0.0f;
-    const float cr = part ? (m - lse[row]) * LOG2E_F : -INFINITY;
-    const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
+    const int r = r_in + 16 * k;
+    const float cr = s_c[ch][r];
+    const uint32_t hw[4] = {h[k].x, h[k].y, h[k].z, h[k].w};
     float g[8];
-    float sl[8];  // softcap slope 1 - tanh^2 (the staged value + m is the capped logit)
+    float sl[8];  // softcap slope 1 - tanh^2 (the staged value + max is the capped logit)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hw[j]));
       g[2 * j] = ex2f(fmaf(f.x, LOG2E_F, cr));
       g[2 * j + 1] = ex2f(fmaf(f.y, LOG2E_F, cr));
       if constexpr (CAP) {
+        const float m = s_m[ch][r];
         const float t0 = (f.x + m) * inv_cap, t1 = (f.y + m) * inv_cap;
         sl[2 * j] = 1.0f - t0 * t0;
         sl[2 * j + 1] = 1.0f - t1 * t1;
       }
     }
-    const long long rel = part ? xr - col0 : -1;
+    const int rel = s_rel[r] - c8 * 8;
     if (rel >= 0 && rel < 8) {  // the target column is one of these eight (one thread per row)
 #pragma unroll
       for (int j = 0; j < 8; ++j)
@@ -95,6 +122,7 @@ __global__ void __launch_bounds__(256, CAP ? 3 : 4) gpass_kernel(uint16_t* __res
       for (int j = 0; j < 8; ++j)
         if (col0 + j >= V) g[j] = 0.0f;
     }
+    uint32_t out[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       amax = fmaxf(amax, fmaxf(fabsf(g[2 * j]), fabsf(g[2 * j + 1])));
@@ -104,20 +132,19 @@ __global__ void __launch_bounds__(256, CAP ? 3 : 4) gpass_kernel(uint16_t* __res
         a1 = g[2 * j + 1] != 0.0f ? a1 * sl[2 * j + 1] : 0.0f;
       }
       const __nv_bfloat162 b2 = __floats2bfloat162_rn(a0, a1);
-      std::memcpy(&pk[k][j], &b2, 4);
+      std::memcpy(&out[j], &b2, 4);
     }
+    h[k] = make_uint4(out[0], out[1], out[2], out[3]);
   }
   const bool keep = __syncthreads_or(!(eps > 0.0f) || amax >= eps) != 0;  // eps = 0: nothing is skipped
   if (keep || store_skipped) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int row = tb * 128 + r_in + 16 * k;
-      if (row < rows)
-        *reinterpret_cast<uint4*>(stage + static_cast<size_t>(row) * pitch + col0) =
-            make_uint4(pk[k][0], pk[k][1], pk[k][2], pk[k][3]);
+      if (row < rows) *reinterpret_cast<uint4*>(stage + static_cast<size_t>(row) * pitch + col0) = h[k];
     }
   }
-  if (threadIdx.x == 0) {
+  if (t == 0) {
     bitmap[static_cast<size_t>(tb) * bm_ld + vt] = keep ? 1 : 0;
     bitmapT[static_cast<size_t>(vt) * n_blocks + tb] = keep ? 1 : 0;
   }
