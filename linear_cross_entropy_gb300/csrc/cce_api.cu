@@ -174,7 +174,8 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ E, const int64_t* _
     if (k < n) {
       const int r = ridx[k];
       const uint4* src = E + static_cast<size_t>(r) * per_row;
-      for (int j = lane; j < per_row; j += 32) dst[j] = src[j];
+#pragma unroll 4
+      for (int j = lane; j < per_row; j += 32) dst[j] = src[j];  // several 16-byte loads in flight per lane
       if (lane == 0) {
         xc[k] = x[r];
         if (lsec) lsec[k] = lse[r];

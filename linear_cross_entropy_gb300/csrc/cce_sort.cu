@@ -274,7 +274,8 @@ __global__ void gather_vocab_rows_kernel(const uint4* __restrict__ src, const in
     uint4* d = dst + static_cast<size_t>(j) * per_row;
     if (j < count) {
       const uint4* s = src + static_cast<size_t>(rows[j]) * per_row;
-      for (int c = lane; c < per_row; c += 32) d[c] = s[c];
+#pragma unroll 4
+      for (int c = lane; c < per_row; c += 32) d[c] = s[c];  // several 16-byte loads in flight per lane
     } else {
       for (int c = lane; c < per_row; c += 32) d[c] = make_uint4(0u, 0u, 0u, 0u);
     }
