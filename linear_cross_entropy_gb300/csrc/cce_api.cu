@@ -273,10 +273,21 @@ int64_t bwd_chunk_cols(int64_t N, int64_t V) {
   return std::min(vc, vpad);
 }
 
+// Token blocks per raster group of the logit GEMMs: the group's E rows
+// (group_n * 128 * D * 2 bytes) stay around 32 MiB, a quarter of L2.
+int raster_group(int64_t n_blocks, int64_t D) {
+  return static_cast<int>(std::max<int64_t>(
+      1, std::min<int64_t>(n_blocks, std::max<int64_t>(8, (int64_t(32) << 20) / (BM * 2 * D)))));
+}
+
 // Width of the D tiles of the gradient GEMMs.  Measured on GB300: MMAs with
 // N = 256 run fastest (N = 224 about 10% slower per column, N = 192 and 128
 // far slower), so tiles are 256 wide even when that pads D (D = 896: 1024),
-// and only narrower when D itself is smaller (rounded up to `step`).
+// and only narrower when D itself is smaller (rounded up to `step`).  Cutting
+// D = 896 into 4 x 224 measured 16% slower in the gradient GEMM with the B
+// operand in four 64-column 2-D boxes per stage, and still 2% slower with B
+// in one 3-D box of seven 64-byte-swizzled 32-column groups, although both
+// issue 1/8 fewer MMAs.
 int grad_tile_width(int64_t D, int step) {
   if (D >= BN) return BN;
   return static_cast<int>(cdiv(D, step) * step);
@@ -747,6 +758,7 @@ static cce_status forward_impl(const void* E, const void* C, const int64_t* x, i
   a.k_blocks = static_cast<int>(cdiv(D, BK));
   a.splits = W.S;
   a.v_tiles = static_cast<int>(cdiv(V, BN));
+  a.group_n = raster_group(a.n_blocks, D);
   a.x = xg;
   a.ignore_index = ignore_index;
   a.part_m = reinterpret_cast<float*>(ws + W.part_m);
@@ -943,9 +955,7 @@ cce_status cce_backward_ex(const void* E, const void* C, const int64_t* x, const
     p->dev_err = dev_err;
   }
   g.k_blocks = static_cast<int>(cdiv(D, BK));
-  // Raster groups whose E rows (group_n * 128 * D * 2 bytes) stay around 32 MiB.
-  g.group_n = static_cast<int>(std::max<int64_t>(
-      1, std::min<int64_t>(cdiv(N, BM), std::max<int64_t>(8, (int64_t(32) << 20) / (BM * 2 * D)))));
+  g.group_n = raster_group(cdiv(N, BM), D);
   r.bn = grad_tile_width(D, r.b3d ? 64 : 32);
   r.n_tiles = static_cast<int>(cdiv(D, r.bn));
 
@@ -1093,6 +1103,7 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
     f.k_blocks = static_cast<int>(cdiv(D, BK));
     f.splits = W.S;
     f.v_tiles = static_cast<int>(cdiv(V, BN));
+    f.group_n = raster_group(nb, D);
     f.items = f.n_blocks * f.splits;  // upper bound; the kernel uses the device count
     f.n_dev = count;
     f.n_row0 = static_cast<int>(r0);

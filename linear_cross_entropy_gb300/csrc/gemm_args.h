@@ -55,7 +55,7 @@ struct GemmArgs {
   // dC tiles then write dC_out [V, D] bf16 rows directly (null: TMA stores)
   const int* dc_rows;
   uint16_t* dC_out;
-  int group_n;   // BWD_G: token blocks per raster group
+  int group_n;   // FWD, FWD_STAGE, BWD_G: token blocks per raster group (>= 1)
   // GRAD
   int bn;           // width of a D tile (multiple of 32, <= 256; of 64 when b3d)
   int b3d;          // 1: the MN-major B operands come in one 3-D box per stage (D % 64 == 0)

@@ -41,6 +41,8 @@ def test_tiny_config(filter_on):
     (1, 64, 300),       # a single token
     (1000, 256, 5000),  # several row blocks and vocabulary tiles
     (640, 128, 9000),   # several backward chunks
+    (300, 448, 3000),   # two gradient D tiles, the second one ragged (192 of 256 columns)
+    (260, 600, 2000),   # three gradient D tiles, the last one ragged (88 of 256 columns)
 ])
 @pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
 def test_ragged_shapes_unfiltered(N, D, V, reduction):
@@ -151,6 +153,39 @@ def test_out_of_range_target_is_reported():
     assert torch.isfinite(lse).all()
     with pytest.raises(cce.CCEError):
         cce.cce_backward(Et, Ct, xt, lse, torch.ones(1, device="cuda"))
+
+
+def test_autograd_path_reports_errors_without_stalling():
+    """The autograd wrappers do not wait for the GPU to check the error word:
+    the error of a bad target surfaces at raise_pending_errors()."""
+    import linear_cross_entropy_gb300 as cce
+    from tests.gpu_util import to_device
+    w, (E, C, x) = make(W.small("o", 64, 64, 500, ignore_frac=0.0))
+    x = x.copy()
+    x[5] = 777
+    Et, Ct, xt = to_device(E, C, x)
+    for fn, calls in ((cce.linear_cross_entropy, 2), (cce.fused_linear_cross_entropy, 1)):
+        Eg, Cg = Et.clone().requires_grad_(True), Ct.clone().requires_grad_(True)
+        reported = []
+        try:  # the backward may already report the forward's word
+            fn(Eg, Cg, xt).backward()
+        except cce.CCEError as e:
+            reported.append(e.status)
+        while True:
+            try:
+                cce.raise_pending_errors()
+                break
+            except cce.CCEError as e:
+                reported.append(e.status)
+        # every library call of the step flagged the bad target, each once
+        assert reported == [8] * calls
+        cce.raise_pending_errors()
+    # a clean batch after the bad one raises nothing
+    x[5] = 3
+    Et, Ct, xt = to_device(E, C, x)
+    Eg = Et.clone().requires_grad_(True)
+    cce.linear_cross_entropy(Eg, Ct, xt).backward()
+    cce.raise_pending_errors()
 
 
 def test_autograd_function_matches_oracle():

@@ -60,6 +60,7 @@ CASES = [
     ("ragged-sum", W.small("r", 300, 136, 5000), "sum", 0),
     ("three-chunks", W.small("c", 700, 64, 5000), "mean", 256 * 5120 * 2),
     ("split-dE", W.small("s", 512, 128, 20000), "sum", 256 * 20224 * 2),
+    ("wide-D", W.small("w", 300, 600, 3000), "mean", 0),
 ]
 
 
