@@ -31,7 +31,7 @@ __all__ = [
     "linear_cross_entropy", "cce_forward", "cce_backward", "CCEError", "FILTER_EPS",
     "forward_workspace_bytes", "backward_workspace_bytes", "memory_report", "kernel_launch_count",
     "Profiler", "vocab_logit_sums", "vocab_order", "cce_loss_and_grad", "fused_linear_cross_entropy",
-    "loss_and_grad_workspace_bytes",
+    "loss_and_grad_workspace_bytes", "raise_pending_errors",
 ]
 
 _lib.load()
@@ -79,12 +79,59 @@ def kernel_launch_count() -> int:
     return int(_lib.load().cce_kernel_launch_count())
 
 
-def _raise_dev_err(dev_err):
-    v = int(dev_err.item())
+def _raise_word(v, what=""):
+    where = f" ({what})" if what else ""
     if v & DEVERR_TIMEOUT:
-        raise CCEError(9, "a kernel pipeline wait timed out")
+        raise CCEError(9, "a kernel pipeline wait timed out" + where)
     if v & DEVERR_TARGET_RANGE:
-        raise CCEError(8, "target index outside [0, V) and not ignore_index")
+        raise CCEError(8, "target index outside [0, V) and not ignore_index" + where)
+
+
+def _raise_dev_err(dev_err):
+    _raise_word(int(dev_err.item()))
+
+
+class _DeferredErrors:
+    """Device error words of the autograd calls, checked without stalling the
+    host.  Each call's word is copied to pinned host memory behind its kernels
+    and read once that copy has landed: at a later call, or in
+    raise_pending_errors().  A training step therefore never waits for the
+    GPU mid-step; an error surfaces one call or more after the call that set
+    it (the kernels treat the offending rows as ignored and complete), and
+    each call's word is reported at most once."""
+
+    def __init__(self):
+        self._pending = []  # (pinned word, event, call name), in issue order
+
+    def watch(self, dev_err, what):
+        host = torch.empty(1, dtype=torch.int32, pin_memory=True)
+        host.copy_(dev_err, non_blocking=True)
+        ev = torch.cuda.Event()
+        ev.record()
+        self._pending.append((host, ev, what))
+        self.poll(keep_last=True)
+
+    def poll(self, wait=False, keep_last=False):
+        """Raises for the oldest landed word that is not clean; keep_last
+        leaves the newest call's word for later."""
+        while len(self._pending) > (1 if keep_last else 0):
+            host, ev, what = self._pending[0]
+            if wait:
+                ev.synchronize()
+            elif not ev.query():
+                return
+            self._pending.pop(0)
+            _raise_word(int(host[0]), what)
+
+
+_deferred = _DeferredErrors()
+
+
+def raise_pending_errors():
+    """Waits for the autograd calls issued so far (linear_cross_entropy,
+    fused_linear_cross_entropy) and raises CCEError if one of them set a
+    device error word."""
+    _deferred.poll(wait=True)
 
 
 def cce_forward(E, C, x, ignore_index=-100, reduction="mean", *, softcap=0.0, skip_ignored=False, stream=None,
@@ -167,7 +214,9 @@ def cce_backward(E, C, x, lse, grad_out, ignore_index=-100, reduction="mean", fi
 class LinearCrossEntropyFunction(torch.autograd.Function):
     @staticmethod
     def forward(ctx, E, C, x, ignore_index, reduction, filter_eps, filter_outputs, softcap, vocab_sort):
-        loss, lse = cce_forward(E, C, x, ignore_index, reduction, softcap=softcap)
+        err = torch.zeros(1, dtype=torch.int32, device=E.device)
+        loss, lse = cce_forward(E, C, x, ignore_index, reduction, softcap=softcap, check_errors=False, dev_err=err)
+        _deferred.watch(err, "cce_forward")
         ctx.save_for_backward(E, C, x, lse)
         ctx.cfg = (ignore_index, reduction, filter_eps, filter_outputs, softcap, vocab_sort)
         return loss
@@ -176,8 +225,11 @@ class LinearCrossEntropyFunction(torch.autograd.Function):
     def backward(ctx, grad_loss):
         E, C, x, lse = ctx.saved_tensors
         ignore_index, reduction, filter_eps, filter_outputs, softcap, vocab_sort = ctx.cfg
+        err = torch.zeros(1, dtype=torch.int32, device=E.device)
         dE, dC = cce_backward(E, C, x, lse, grad_loss, ignore_index, reduction, filter_eps,
-                              filter_outputs=filter_outputs, softcap=softcap, vocab_sort=vocab_sort)
+                              filter_outputs=filter_outputs, softcap=softcap, vocab_sort=vocab_sort,
+                              check_errors=False, dev_err=err)
+        _deferred.watch(err, "cce_backward")
         return dE, dC, None, None, None, None, None, None, None
 
 
@@ -189,7 +241,9 @@ def linear_cross_entropy(E, C, x, ignore_index=-100, reduction="mean", filter_ep
     int64.  filter_eps is the backward's tile-skip threshold (0 disables);
     filter_outputs picks which gradients it applies to ("both", "dE", "dC",
     "none"); softcap > 0 caps the logits as softcap * tanh(logit / softcap);
-    vocab_sort filters over the vocabulary sorted by average logit."""
+    vocab_sort filters over the vocabulary sorted by average logit.
+    Device errors (a target outside [0, V)) are raised without stalling the
+    step: at a later call or at raise_pending_errors()."""
     return LinearCrossEntropyFunction.apply(E, C, x, ignore_index, reduction, filter_eps, filter_outputs,
                                             softcap, vocab_sort)
 
@@ -246,9 +300,12 @@ class FusedLinearCrossEntropyFunction(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, E, C, x, ignore_index, reduction, filter_eps, filter_outputs, softcap, max_staging_bytes):
+        err = torch.zeros(1, dtype=torch.int32, device=E.device)
         loss, _, dE, dC = cce_loss_and_grad(E, C, x, ignore_index, reduction, filter_eps,
                                             filter_outputs=filter_outputs, softcap=softcap,
-                                            max_staging_bytes=max_staging_bytes, lse=False)
+                                            max_staging_bytes=max_staging_bytes, lse=False,
+                                            check_errors=False, dev_err=err)
+        _deferred.watch(err, "cce_loss_and_grad")
         ctx.save_for_backward(dE, dC)
         return loss
 
@@ -267,7 +324,8 @@ def fused_linear_cross_entropy(E, C, x, ignore_index=-100, reduction="mean", fil
                                filter_outputs="both", softcap=0.0, max_staging_bytes=0):
     """linear_cross_entropy computed by the single call: loss and gradients in
     the forward (token chunks of staged logits, no recompute), the backward
-    only scales.  reduction "sum" or "mean"."""
+    only scales.  reduction "sum" or "mean".  Device errors are raised as
+    for linear_cross_entropy."""
     return FusedLinearCrossEntropyFunction.apply(E, C, x, ignore_index, reduction, filter_eps, filter_outputs,
                                                  softcap, max_staging_bytes)
 
