@@ -287,13 +287,18 @@ def run_gpu(args, rank, world, local_rank):
     copied = [torch.cuda.Event() for _ in range(2)]
     consumed = [torch.cuda.Event() for _ in range(2)]
 
+    copy_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(e2e_steps)]
+
     def e2e_copy(j, stream):
         Ed, Cd, xd = bufs[j % 2]
         with torch.cuda.stream(stream):
             stream.wait_event(consumed[j % 2])
+            copy_ev[j][0].record(stream)
             Ed.copy_(Eh, non_blocking=True)
             Cd.copy_(Ch, non_blocking=True)
             xd.copy_(xh, non_blocking=True)
+            copy_ev[j][1].record(stream)
             copied[j % 2].record(stream)
 
     comp_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -338,18 +343,20 @@ def run_gpu(args, rank, world, local_rank):
         if not bool(torch.isfinite(loss_h).all()) or float(loss_h.min()) != float(loss_h.max()):
             raise RuntimeError(f"end-to-end losses differ across steps: {loss_h.tolist()}")
         dev_ms = sum(a.elapsed_time(b) for a, b in comp_ev) / e2e_steps
-        return N * e2e_steps / dt, 1e3 * t_host / e2e_steps, dev_ms
+        h2d_ms = sum(a.elapsed_time(b) for a, b in copy_ev) / e2e_steps
+        return N * e2e_steps / dt, 1e3 * t_host / e2e_steps, dev_ms, h2d_ms
 
     e2e_run(True)
-    e2e_serial, _, _ = e2e_run(False)
-    e2e_value, host_ms, dev_ms = e2e_run(True)
+    e2e_serial, _, _, h2d_serial_ms = e2e_run(False)
+    e2e_value, host_ms, dev_ms, h2d_ms = e2e_run(True)
     e2e = {"value": e2e_value, "unit": UNIT,
            "h2d_bytes_per_step": Eh.numel() * 2 + Ch.numel() * 2 + xh.numel() * 8, "d2h_bytes_per_step": 4,
            "steps": e2e_steps, "api": ("fused_linear_cross_entropy" if single else "linear_cross_entropy")
            + " + backward (autograd Function over the C ABI)",
            "overlap": "inputs of step i+1 copied on a second stream while step i computes (two buffer sets)",
            "serial_value": e2e_serial, "host_enqueue_ms_per_step": round(host_ms, 3),
-           "compute_stream_ms_per_step": round(dev_ms, 3)}
+           "compute_stream_ms_per_step": round(dev_ms, 3), "h2d_ms_per_step": round(h2d_ms, 3),
+           "h2d_ms_per_step_serial": round(h2d_serial_ms, 3)}
 
     # roofline of the dominant GEMM phase, timed live with the library's events
     peaks, peak_src = load_peaks()
