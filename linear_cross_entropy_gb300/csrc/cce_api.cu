@@ -468,12 +468,13 @@ struct DeviceInfo {
   bool init = false;
   bool ok = false;
   int sms = 0;
+  int pair_clusters = 0;  // CTA pairs of the forward GEMM resident at once
 };
 std::mutex g_mu;
 DeviceInfo g_dev[64];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-cce_status device_check(int* sms) {
+cce_status device_check(int* sms, int* pair_clusters = nullptr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
     cudaGetLastError();
@@ -496,6 +497,7 @@ cce_status device_check(int* sms) {
         cudaGetLastError();
         return CCE_ERR_CUDA;
       }
+      d.pair_clusters = gemm_pair_clusters(sms);
       if (!g_encode) {
         cudaDriverEntryPointQueryResult q;
         void* fn = nullptr;
@@ -512,6 +514,7 @@ cce_status device_check(int* sms) {
   }
   if (!d.ok) return CCE_ERR_DEVICE;
   *sms = d.sms;
+  if (pair_clusters) *pair_clusters = d.pair_clusters;
   return CCE_OK;
 }
 
@@ -709,8 +712,8 @@ static cce_status forward_impl(const void* E, const void* C, const int64_t* x, i
   const bool compact = (flags & CCE_FWD_SKIP_IGNORED) != 0;
   const FwdLayout W = fwd_layout(N, V, D, compact);
   if (ws_bytes < W.total) return CCE_ERR_WORKSPACE;
-  int sms = 0;
-  cce_status st = device_check(&sms);
+  int sms = 0, pair_clusters = 0;
+  cce_status st = device_check(&sms, &pair_clusters);
   if (st != CCE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -769,13 +772,22 @@ static cce_status forward_impl(const void* E, const void* C, const int64_t* x, i
   a.dev_err = dev_err;
   a.counter = reinterpret_cast<int*>(ws + W.counter);
   a.n_dev = count;  // null without compaction: all N rows
-  const int units = a.n_blocks * a.splits;
+  // All rows and an even number of token blocks: clusters of two CTAs share
+  // each MMA (M = 256), each CTA loading its 128 rows of E and half of the C
+  // tile, so a CTA moves two thirds of the operand bytes per MMA.
+  const bool pairs = !compact && pair_clusters > 0 && a.n_blocks % 2 == 0;
+  if (pairs) {
+    if (!make_tmap(&a.tmB2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, D, V, D, BK, BN / 2)) return CCE_ERR_CUDA;
+    a.group_n = std::max(2, a.group_n & ~1);
+  }
+  const int units = pairs ? (a.n_blocks / 2) * a.splits : a.n_blocks * a.splits;
   a.items = units;
   {
     PhaseScope ps(0, s);
     cudaError_t e = cudaMemsetAsync(a.counter, 0, sizeof(int), s);
     if (e != cudaSuccess) return cuda_status(e);
-    e = launch_gemm(MODE_FWD, a, std::min(units, sms), s);
+    e = pairs ? launch_gemm_fwd_pairs(a, std::min(units, pair_clusters), s)
+              : launch_gemm(MODE_FWD, a, std::min(units, sms), s);
     g_launches++;
     if (e != cudaSuccess) return cuda_status(e);
   }

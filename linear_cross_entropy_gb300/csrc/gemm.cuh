@@ -88,9 +88,26 @@ __device__ __forceinline__ Dims dims_of(const GemmArgs& a) {
 }
 
 // Calls f(tile) for every tile of work item `item`; false if f asked to stop.
-template <int MODE, typename F>
+template <int MODE, bool PAIR = false, typename F>
 __device__ __forceinline__ bool for_each_tile_of_item(const GemmArgs& a, const Dims& dm, int item, F&& f) {
-  if constexpr (MODE == MODE_FWD || MODE == MODE_FWD_STAGE) {
+  if constexpr (PAIR) {
+    // CTA pairs (FWD, all rows, an even number of token blocks): an item is a
+    // pair of neighbouring token blocks and a vocabulary split, in the same
+    // grouped raster (group_n even); the CTA of rank r takes block 2p + r.
+    static_assert(MODE == MODE_FWD, "CTA pairs run the plain forward only");
+    const int gp = a.group_n >> 1;
+    const int per_group = gp * a.splits;
+    const int g = item / per_group, j = item - g * per_group;
+    const int gpn = min(gp, (a.n_blocks >> 1) - g * gp);
+    const int m = g * a.group_n + 2 * (j % gpn) + static_cast<int>(cluster_ctarank());
+    const int s = j / gpn;
+    const int t0 = static_cast<int>(static_cast<long long>(s) * a.v_tiles / a.splits);
+    const int t1 = static_cast<int>(static_cast<long long>(s + 1) * a.v_tiles / a.splits);
+    for (int t = t0; t < t1; ++t) {
+      if (!f(Tile{KIND_MAIN, m, t, s, t == t0, t == t1 - 1})) return false;
+    }
+    return true;
+  } else if constexpr (MODE == MODE_FWD || MODE == MODE_FWD_STAGE) {
     // Grouped raster as in BWD_G: groups of group_n token blocks, the token
     // block fastest inside a group, then the vocabulary split.  The CTAs of
     // a split share its C tiles, and a group's E rows stay in L2 while the
@@ -242,6 +259,8 @@ struct SmemLayout {
   int* flags;       // [2 parity][2 half][4 warps]
   int* ring_ids;    // [RING]
   int* stage_meta;  // [STAGES] what the producer put in the stage (META_*)
+  // CTA pairs: cluster address of the even CTA's tmem_empty[0] (0: no pair)
+  uint32_t tmem_empty_lead;
 };
 
 // Stage tags written by the producer before it arms the stage's full
@@ -270,6 +289,7 @@ __device__ __forceinline__ SmemLayout carve_smem(uint8_t* raw) {
   L.flags = reinterpret_cast<int*>(tail + 8);      // 16 ints
   L.ring_ids = reinterpret_cast<int*>(tail + 72);  // RING ints
   L.stage_meta = reinterpret_cast<int*>(tail + 72 + 4 * RING);  // STAGES ints
+  L.tmem_empty_lead = 0;
   return L;
 }
 
@@ -302,7 +322,7 @@ __device__ __forceinline__ void prefetch_next_b(const GemmArgs& a, const Dims& d
 }
 
 // ---------------------------------------------------------------- producer
-template <int MODE>
+template <int MODE, bool PAIR = false>
 __device__ __forceinline__ void producer_loop(const GemmArgs& a, const SmemLayout& L) {
   volatile int* abort_flag = L.abort_flag;
   int stage = 0;
@@ -316,17 +336,24 @@ __device__ __forceinline__ void producer_loop(const GemmArgs& a, const SmemLayou
   // reserved item while busy would unbalance the end of a launch.
   constexpr bool kAhead = MODE == MODE_BWD_G;
   int next = kAhead ? atomicAdd(a.counter, 1) : 0;
+  // CTA pairs take items in a fixed order (cluster c: c, c + clusters, ...),
+  // the same in both CTAs, so neither needs the other's schedule; forward
+  // items are all of one size.  The even CTA's full barriers count both
+  // CTAs' copies.
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int pair_first = PAIR ? static_cast<int>(cluster_id_x()) : 0;
+  const int pair_step = PAIR ? static_cast<int>(cluster_count_x()) : 0;
   for (int k = 0;; ++k) {
     const int slot = k % RING;
     if (!wait_bounded(&L.ring_empty[slot], static_cast<uint32_t>(((k / RING) & 1) ^ 1), abort_flag, a.dev_err))
       break;
-    int item = kAhead ? next : atomicAdd(a.counter, 1);
+    int item = PAIR ? pair_first + k * pair_step : (kAhead ? next : atomicAdd(a.counter, 1));
     if (item >= dm.items) item = -1;
     L.ring_ids[slot] = item;
     mbar_arrive(&L.ring_full[slot]);  // release: the id is visible to the waiting consumers
     if (item < 0) break;
     if (kAhead) next = atomicAdd(a.counter, 1);
-    const bool ok = for_each_tile_of_item<MODE>(a, dm, item, [&](const Tile& t) -> bool {
+    const bool ok = for_each_tile_of_item<MODE, PAIR>(a, dm, item, [&](const Tile& t) -> bool {
       const int nk = kblocks_of<MODE>(a, dm, t);
       if (MODE == MODE_FWD_STAGE) prefetch_next_b(a, dm, t);
       int kb = next_kblock<MODE>(a, t, kblock_begin<MODE>(a, t), nk);
@@ -350,12 +377,19 @@ __device__ __forceinline__ void producer_loop(const GemmArgs& a, const SmemLayou
         uint8_t* sA = L.stages + stage * STAGE_BYTES;
         uint8_t* sB = sA + A_STAGE_BYTES;
         uint64_t* fb = &L.full[stage];
-        mbar_arrive_expect_tx(fb, STAGE_BYTES);
         const int k0 = kb * BK;
-        if (MODE != MODE_GRAD) {
+        if constexpr (PAIR) {
+          // this CTA's 128 rows of A and its half (128 rows) of the B tile
+          const uint32_t fb_lead = mapa_shared(smem_u32(fb), 0);
+          if (rank == 0) mbar_arrive_expect_tx(fb, 2 * PAIR_STAGE_BYTES);
+          tma_load_2d_pair(&a.tmA, fb_lead, sA, k0, t.m * BM);
+          tma_load_2d_pair(&a.tmB2, fb_lead, sB, k0, a.c_row0 + t.n * BN + static_cast<int>(rank) * (BN / 2));
+        } else if (MODE != MODE_GRAD) {
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
           tma_load_2d(&a.tmA, fb, sA, k0, t.m * BM);
           tma_load_2d(&a.tmB, fb, sB, k0, a.c_row0 + t.n * BN);
         } else if (t.kind == KIND_DC) {
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
           tma_load_3d(&a.tmA, fb, sA, 0, k0, (t.m * BM) >> 6);  // both 64-column groups of A
           if (a.b3d) {  // the four 64-column groups of B in one instruction
             tma_load_3d(&a.tmB, fb, sB, 0, k0, (t.n * a.bn) >> 6);
@@ -363,6 +397,7 @@ __device__ __forceinline__ void producer_loop(const GemmArgs& a, const SmemLayou
             for (int j = 0; j < BN / 64; ++j) tma_load_2d(&a.tmB, fb, sB + j * 8192, t.n * a.bn + j * 64, k0);
           }
         } else {
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
           tma_load_2d(&a.tmA2, fb, sA, k0, t.m * BM);
           if (a.b3d) {
             tma_load_3d(&a.tmB2, fb, sB, 0, a.c_row0 + k0, (t.n * a.bn) >> 6);
@@ -383,7 +418,13 @@ __device__ __forceinline__ void producer_loop(const GemmArgs& a, const SmemLayou
     });
     if (!ok) break;
   }
-  if (*abort_flag) {
+  if (PAIR && rank != 0 && *abort_flag) {
+    // This CTA's copies complete on the even CTA's barriers; give any still
+    // in flight a bounded 10 ms to land before the CTA exits.
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 10000000ull) {
+    }
+  } else if (*abort_flag) {
     // Let every copy this thread issued land before the CTA exits.
     for (int s = 0; s < STAGES; ++s) {
       if (issued_mask & (1u << s)) {
@@ -395,8 +436,11 @@ __device__ __forceinline__ void producer_loop(const GemmArgs& a, const SmemLayou
 }
 
 // --------------------------------------------------------------------- MMA
-template <int MODE>
+template <int MODE, bool PAIR = false>
 __device__ __forceinline__ void mma_loop(const GemmArgs& a, const SmemLayout& L, uint32_t tmem_base) {
+  // CTA pairs: the even CTA issues every MMA (M = 256) for both; the odd
+  // CTA's MMA thread has nothing to do.
+  if (PAIR && cluster_ctarank() != 0) return;
   volatile int* abort_flag = L.abort_flag;
   int stage = 0;
   uint32_t phase = 0;
@@ -407,12 +451,12 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& a, const SmemLayout& L,
   for (int k = 0;; ++k) {
     const int item = ring_take(L, k, a);
     if (item < 0) break;
-    const bool ok = for_each_tile_of_item<MODE>(a, dm, item, [&](const Tile& t) -> bool {
+    const bool ok = for_each_tile_of_item<MODE, PAIR>(a, dm, item, [&](const Tile& t) -> bool {
       // Operand majorness and tile width of this tile.
       const bool a_mn = (MODE == MODE_GRAD) && t.kind == KIND_DC;
       const bool b_mn = (MODE == MODE_GRAD);
       const int n = (MODE == MODE_GRAD) ? a.bn : BN;
-      const uint32_t idesc = idesc_bf16(BM, n, a_mn, b_mn);
+      const uint32_t idesc = idesc_bf16(PAIR ? 2 * BM : BM, n, a_mn, b_mn);
       const uint32_t a_lbo = a_mn ? 8192u : 16u, b_lbo = b_mn ? 8192u : 16u;
       const uint64_t a_step = a_mn ? (2048u >> 4) : (32u >> 4);  // one K=16 step, encoded
       const uint64_t b_step = b_mn ? (2048u >> 4) : (32u >> 4);
@@ -444,30 +488,46 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& a, const SmemLayout& L,
         const uint64_t bdesc = smem_desc_sw128(sB, b_lbo, 1024u);
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
-          mma_bf16(d_tmem, adesc + a_step * kk, bdesc + b_step * kk, idesc, (any || kk > 0) ? 1u : 0u);
+          if constexpr (PAIR) {
+            mma_bf16_pair(d_tmem, adesc + a_step * kk, bdesc + b_step * kk, idesc, (any || kk > 0) ? 1u : 0u);
+          } else {
+            mma_bf16(d_tmem, adesc + a_step * kk, bdesc + b_step * kk, idesc, (any || kk > 0) ? 1u : 0u);
+          }
         }
         any = true;
         issued_any = true;
-        mma_commit(&L.empty[stage]);
+        if constexpr (PAIR) {
+          mma_commit_pair_both(&L.empty[stage]);  // frees the stage in both CTAs
+        } else {
+          mma_commit(&L.empty[stage]);
+        }
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
         }
         if (MODE == MODE_GRAD && (meta & META_LAST)) break;
       }
-      if (any) {
+      if (PAIR) {
+        mma_commit_pair_both(&L.tmem_full[acc]);  // FWD tiles always have MMAs
+      } else if (any) {
         mma_commit(&L.tmem_full[acc]);
       } else {
         mbar_arrive(&L.tmem_full[acc]);  // nothing to wait for: the epilogue writes zeros
       }
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
+      if (++acc == (PAIR ? PAIR_ACCS : 2)) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
       return true;
     });
     if (!ok) break;
   }
   if (*abort_flag && issued_any) {
-    mma_commit(L.drain);  // fires once every MMA issued so far has finished
+    if constexpr (PAIR) {
+      mma_commit_pair_local(L.drain);
+    } else {
+      mma_commit(L.drain);  // fires once every MMA issued so far has finished
+    }
     volatile int dummy = 0;
     wait_bounded(L.drain, 0, &dummy, nullptr);
   }
@@ -499,7 +559,13 @@ __device__ __forceinline__ void staging_acquire(EpiCtx& e, int b) {
 __device__ __forceinline__ void release_tmem(const SmemLayout& L, int acc) {
   tc_fence_before();
   __syncwarp();
-  if (lane_id() == 0) mbar_arrive(&L.tmem_empty[acc]);
+  if (lane_id() == 0) {
+    if (L.tmem_empty_lead) {  // CTA pairs: the even CTA's MMA thread waits for both CTAs
+      mbar_arrive_cluster(L.tmem_empty_lead + 8u * static_cast<uint32_t>(acc));
+    } else {
+      mbar_arrive(&L.tmem_empty[acc]);
+    }
+  }
 }
 
 // FWD: fold a 128 x 256 logit tile into the running (max, sumexp) of each row.
@@ -961,7 +1027,7 @@ __device__ __forceinline__ void epi_de(const GemmArgs& a, const Dims& dm, const 
   release_tmem(L, acc);
 }
 
-template <int MODE, bool CAP>
+template <int MODE, bool CAP, bool PAIR = false>
 __device__ __forceinline__ void epilogue_loop(const GemmArgs& a, const SmemLayout& L, uint32_t tmem_base,
                                               int warp) {
   EpiCtx e;
@@ -979,7 +1045,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& a, const SmemLayou
     if (lane_id() == 0) item = ring_take(L, k, a);
     item = __shfl_sync(0xffffffffu, item, 0);
     if (item < 0) break;
-    const bool ok = for_each_tile_of_item<MODE>(a, dm, item, [&](const Tile& t) -> bool {
+    const bool ok = for_each_tile_of_item<MODE, PAIR>(a, dm, item, [&](const Tile& t) -> bool {
       if (!warp_wait_bounded(&L.tmem_full[acc], acc_phase, L.abort_flag, a.dev_err)) return false;
       tc_fence_after();
       bool r = true;
@@ -997,8 +1063,10 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& a, const SmemLayou
         }
       }
       ++e.iter;
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
+      if (++acc == (PAIR ? PAIR_ACCS : 2)) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
       return r;
     });
     if (!ok) break;
@@ -1009,11 +1077,14 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& a, const SmemLayou
 
 // CAP: logit softcapping in the FWD / BWD_G epilogues (a separate
 // instantiation, so the common path carries none of its registers).
-template <int MODE, bool CAP = false>
+// PAIR: launched as clusters of two CTAs sharing each MMA (M = 256).
+template <int MODE, bool CAP = false, bool PAIR = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1) cce_gemm_kernel(const __grid_constant__ GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  const SmemLayout L = carve_smem(smem_raw);
+  SmemLayout L = carve_smem(smem_raw);
   const int warp = static_cast<int>(threadIdx.x >> 5);
+  const bool lead = !PAIR || cluster_ctarank() == 0;
+  if (PAIR) L.tmem_empty_lead = mapa_shared(smem_u32(&L.tmem_empty[0]), 0);
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&L.full[s], 1);
@@ -1021,12 +1092,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cce_gemm_kernel(const __grid_c
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&L.tmem_full[i], 1);
-      mbar_init(&L.tmem_empty[i], NUM_EPI_WARPS);
+      // pairs: the even CTA's accumulators are released by both CTAs' epilogues
+      mbar_init(&L.tmem_empty[i], PAIR ? 2 * NUM_EPI_WARPS : NUM_EPI_WARPS);
       mbar_init(&L.vote[i], NUM_EPI_WARPS);
     }
     for (int i = 0; i < RING; ++i) {
       mbar_init(&L.ring_full[i], 1);
-      mbar_init(&L.ring_empty[i], 1 + NUM_EPI_WARPS);  // the MMA thread and every epilogue warp
+      // the MMA thread (the odd CTA of a pair has none at work) and every epilogue warp
+      mbar_init(&L.ring_empty[i], (lead ? 1 : 0) + NUM_EPI_WARPS);
     }
     mbar_init(L.drain, 1);
     *L.abort_flag = 0;
@@ -1043,27 +1116,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cce_gemm_kernel(const __grid_c
     }
   }
   if (warp == 1) {
-    tmem_alloc(L.tmem_base, TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {  // one warp of each CTA of the pair, together
+      tmem_alloc_pair(L.tmem_base, PAIR_TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(L.tmem_base, TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // the peer's barriers exist before any copy or arrive reaches them
   tc_fence_after();
   const uint32_t tmem_base = *L.tmem_base;
 
   if (warp == 0) {
-    if (lane_id() == 0) producer_loop<MODE>(a, L);
+    if (lane_id() == 0) producer_loop<MODE, PAIR>(a, L);
   } else if (warp == 1) {
-    if (lane_id() == 0) mma_loop<MODE>(a, L, tmem_base);
+    if (lane_id() == 0) mma_loop<MODE, PAIR>(a, L, tmem_base);
   } else {
-    epilogue_loop<MODE, CAP>(a, L, tmem_base, warp);
+    epilogue_loop<MODE, CAP, PAIR>(a, L, tmem_base, warp);
   }
 
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // no CTA leaves while its peer may still signal its barriers
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if constexpr (PAIR) {
+      tmem_dealloc_pair(tmem_base, PAIR_TMEM_COLS);
+    } else {
+      tmem_dealloc(tmem_base, TMEM_COLS);
+    }
   }
 }
 

@@ -13,10 +13,14 @@ constexpr int STAGES = 4;
 constexpr int A_STAGE_BYTES = BM * BK * 2;                  // 16 KiB
 constexpr int B_STAGE_BYTES = BN * BK * 2;                  // 32 KiB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;  // 48 KiB
+constexpr int PAIR_STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES / 2;  // one CTA of a pair: A + half of B
 constexpr int NUM_EPI_WARPS = 4;
 constexpr int EPI_WARP_BYTES = 8192;
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
+// CTA pairs: TMEM columns allocated (together, by both CTAs) and accumulators
+constexpr uint32_t PAIR_TMEM_COLS = 512;
+constexpr int PAIR_ACCS = 2;
 constexpr int RING = 4;  // depth of the work-item ring between the scheduler and the consumers
 constexpr int BAR_BYTES = 512;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_EPI_WARPS * EPI_WARP_BYTES + BAR_BYTES;
@@ -38,7 +42,8 @@ struct GemmArgs {
   CUtensorMap tmB;
   CUtensorMap tmOut;
   // GRAD: the dE kind's A = G chunk (K-major boxes), B = C (MN-major: 3-D view
-  // {64 d, V, D/64} or 64x64 boxes), Out = dE accumulator (fp32).
+  // {64 d, V, D/64} or 64x64 boxes), Out = dE accumulator (fp32).  FWD run as
+  // CTA pairs: tmB2 = C in boxes of 64 x 128 rows (each CTA's half of a B tile).
   CUtensorMap tmA2;
   CUtensorMap tmB2;
   CUtensorMap tmOut2;

@@ -4,9 +4,10 @@
 
 namespace cce {
 
-template <int MODE, bool CAP>
+template <int MODE, bool CAP, bool PAIR = false>
 static cudaError_t set_smem() {
-  return cudaFuncSetAttribute(cce_gemm_kernel<MODE, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  return cudaFuncSetAttribute(cce_gemm_kernel<MODE, CAP, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              SMEM_BYTES);
 }
 
 cudaError_t prepare_gemm_kernels() {
@@ -17,7 +18,42 @@ cudaError_t prepare_gemm_kernels() {
   if ((e = set_smem<MODE_BWD_G, true>()) != cudaSuccess) return e;
   if ((e = set_smem<MODE_FWD_STAGE, false>()) != cudaSuccess) return e;
   if ((e = set_smem<MODE_FWD_STAGE, true>()) != cudaSuccess) return e;
+  if ((e = set_smem<MODE_FWD, false, true>()) != cudaSuccess) return e;
+  if ((e = set_smem<MODE_FWD, true, true>()) != cudaSuccess) return e;
   return set_smem<MODE_GRAD, false>();
+}
+
+static cudaLaunchConfig_t pair_config(int clusters, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  attr->id = cudaLaunchAttributeClusterDimension;
+  attr->val.clusterDim.x = 2;
+  attr->val.clusterDim.y = 1;
+  attr->val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+int gemm_pair_clusters(int sms) {
+  cudaLaunchAttribute attr;
+  cudaLaunchConfig_t cfg = pair_config(sms / 2, nullptr, &attr);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, cce_gemm_kernel<MODE_FWD, false, true>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+cudaError_t launch_gemm_fwd_pairs(const GemmArgs& args, int clusters, cudaStream_t stream) {
+  cudaLaunchAttribute attr;
+  const cudaLaunchConfig_t cfg = pair_config(clusters, stream, &attr);
+  if (args.softcap > 0.0f) return cudaLaunchKernelEx(&cfg, cce_gemm_kernel<MODE_FWD, true, true>, args);
+  return cudaLaunchKernelEx(&cfg, cce_gemm_kernel<MODE_FWD, false, true>, args);
 }
 
 // One thread waits on an mbarrier that nothing ever arrives on, through the
