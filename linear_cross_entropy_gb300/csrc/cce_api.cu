@@ -547,6 +547,14 @@ bool make_tmap_mn3(CUtensorMap* m, const void* ptr, uint64_t D, uint64_t rows, u
   return r == CUDA_SUCCESS;
 }
 
+// CTA pairs (FWD, BWD_G): B = C (or a chunk of sorted C rows,
+// `rows` of them) in 128-row boxes, each CTA's half of a 256-row tile; raster
+// groups hold whole pairs.
+bool pair_operands(GemmArgs* a, const void* C, int64_t D, int64_t rows) {
+  a->group_n = std::max(2, a->group_n & ~1);
+  return make_tmap(&a->tmB2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, D, rows, D, BK, BN / 2);
+}
+
 // ---------------------------------------------------------- phase timing
 struct PhaseRec {
   int phase;
@@ -772,21 +780,18 @@ static cce_status forward_impl(const void* E, const void* C, const int64_t* x, i
   a.dev_err = dev_err;
   a.counter = reinterpret_cast<int*>(ws + W.counter);
   a.n_dev = count;  // null without compaction: all N rows
-  // All rows and an even number of token blocks: clusters of two CTAs share
-  // each MMA (M = 256), each CTA loading its 128 rows of E and half of the C
-  // tile, so a CTA moves two thirds of the operand bytes per MMA.
-  const bool pairs = !compact && pair_clusters > 0 && a.n_blocks % 2 == 0;
-  if (pairs) {
-    if (!make_tmap(&a.tmB2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, D, V, D, BK, BN / 2)) return CCE_ERR_CUDA;
-    a.group_n = std::max(2, a.group_n & ~1);
-  }
-  const int units = pairs ? (a.n_blocks / 2) * a.splits : a.n_blocks * a.splits;
+  // Clusters of two CTAs share each MMA (M = 256), each CTA loading its 128
+  // rows of E and half of the C tile, so a CTA moves two thirds of the
+  // operand bytes per MMA.
+  const bool pairs = pair_clusters > 0;
+  if (pairs && !pair_operands(&a, C, D, V)) return CCE_ERR_CUDA;
+  const int units = pairs ? ((a.n_blocks + 1) / 2) * a.splits : a.n_blocks * a.splits;
   a.items = units;
   {
     PhaseScope ps(0, s);
     cudaError_t e = cudaMemsetAsync(a.counter, 0, sizeof(int), s);
     if (e != cudaSuccess) return cuda_status(e);
-    e = pairs ? launch_gemm_fwd_pairs(a, std::min(units, pair_clusters), s)
+    e = pairs ? launch_gemm_pairs(MODE_FWD, a, std::min(units, pair_clusters), s)
               : launch_gemm(MODE_FWD, a, std::min(units, sms), s);
     g_launches++;
     if (e != cudaSuccess) return cuda_status(e);
@@ -862,8 +867,8 @@ cce_status cce_backward_ex(const void* E, const void* C, const int64_t* x, const
   const bool sort = (filter_flags & CCE_SORT_VOCAB) != 0;
   const BwdLayout W = bwd_layout(N, D, V, sort);
   if (ws_bytes < W.total) return CCE_ERR_WORKSPACE;
-  int sms = 0;
-  cce_status st = device_check(&sms);
+  int sms = 0, pair_clusters = 0;
+  cce_status st = device_check(&sms, &pair_clusters);
   if (st != CCE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -968,6 +973,13 @@ cce_status cce_backward_ex(const void* E, const void* C, const int64_t* x, const
   }
   g.k_blocks = static_cast<int>(cdiv(D, BK));
   g.group_n = raster_group(cdiv(N, BM), D);
+  // The recompute as CTA pairs (see forward_impl) when there are many token
+  // blocks.  Its items are single tiles taken in a fixed order, and with an
+  // odd number of compacted blocks the last pair runs half empty; at 32
+  // blocks (the Qwen shape) that cost more than the pairs saved (0.737 ->
+  // 0.777 ms), at 64 and 128 blocks the pairs won (Llama: 9.85 -> 9.48 ms).
+  const bool pairs = pair_clusters > 0 && cdiv(N, BM) >= PAIR_MIN_BLOCKS;
+  if (pairs && !pair_operands(&g, Cg, D, c_rows)) return CCE_ERR_CUDA;
   r.bn = grad_tile_width(D, r.b3d ? 64 : 32);
   r.n_tiles = static_cast<int>(cdiv(D, r.bn));
 
@@ -1004,7 +1016,8 @@ cce_status cce_backward_ex(const void* E, const void* C, const int64_t* x, const
     }
     {
       PhaseScope ps(3, s);
-      e = launch_gemm(MODE_BWD_G, g, std::min(sms, g.n_blocks * g.v_tiles), s);
+      e = pairs ? launch_gemm_pairs(MODE_BWD_G, g, std::min(pair_clusters, ((g.n_blocks + 1) / 2) * g.v_tiles), s)
+                : launch_gemm(MODE_BWD_G, g, std::min(sms, g.n_blocks * g.v_tiles), s);
       g_launches++;
       if (e != cudaSuccess) return cuda_status(e);
     }
@@ -1116,6 +1129,9 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
     f.splits = W.S;
     f.v_tiles = static_cast<int>(cdiv(V, BN));
     f.group_n = raster_group(nb, D);
+    // One CTA per tile: as CTA pairs this kernel measured slower (Qwen shape:
+    // 0.702 -> 0.738 ms; Llama: 10.42 -> 10.47 ms), its epilogue's staging
+    // stores being the same per CTA while the pairs add a half-empty last pair.
     f.items = f.n_blocks * f.splits;  // upper bound; the kernel uses the device count
     f.n_dev = count;
     f.n_row0 = static_cast<int>(r0);

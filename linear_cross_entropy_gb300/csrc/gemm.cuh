@@ -61,6 +61,10 @@ struct Tile {
   int n;      // B-row block (256) or output column block
   int split;  // FWD: vocabulary split; GRAD dE: K range
   bool first, last;  // FWD: first / last tile of a (row block, split) unit
+  // false: the odd CTA's half of a pair whose second token block does not
+  // exist (an odd number of blocks): the MMA runs on whatever rows are there
+  // and the epilogue writes nothing
+  bool live = true;
 };
 
 // Work sizes that depend on the device-side row count (BWD_G / GRAD run over
@@ -71,13 +75,16 @@ struct Dims {
   int items;  // work items of the launch
 };
 
-template <int MODE>
+template <int MODE, bool PAIR = false>
 __device__ __forceinline__ Dims dims_of(const GemmArgs& a) {
   const int n = a.n_dev ? max(0, min(a.N, *a.n_dev - a.n_row0)) : a.N;
   Dims d;
   d.nb = (n + BM - 1) / BM;
   d.dc_kb = (n + BK - 1) / BK;
-  if constexpr (MODE == MODE_FWD || MODE == MODE_FWD_STAGE) {
+  if constexpr (PAIR) {  // items are pairs of token blocks
+    const int nbx = (MODE == MODE_BWD_G || a.n_dev) ? d.nb : a.n_blocks;
+    d.items = ((nbx + 1) >> 1) * (MODE == MODE_BWD_G ? a.v_tiles : a.splits);
+  } else if constexpr (MODE == MODE_FWD || MODE == MODE_FWD_STAGE) {
     d.items = a.n_dev ? d.nb * a.splits : a.items;
   } else if constexpr (MODE == MODE_BWD_G) {
     d.items = d.nb * a.v_tiles;
@@ -91,22 +98,32 @@ __device__ __forceinline__ Dims dims_of(const GemmArgs& a) {
 template <int MODE, bool PAIR = false, typename F>
 __device__ __forceinline__ bool for_each_tile_of_item(const GemmArgs& a, const Dims& dm, int item, F&& f) {
   if constexpr (PAIR) {
-    // CTA pairs (FWD, all rows, an even number of token blocks): an item is a
-    // pair of neighbouring token blocks and a vocabulary split, in the same
-    // grouped raster (group_n even); the CTA of rank r takes block 2p + r.
-    static_assert(MODE == MODE_FWD, "CTA pairs run the plain forward only");
-    const int gp = a.group_n >> 1;
-    const int per_group = gp * a.splits;
+    // CTA pairs (FWD, BWD_G): an item is a pair of neighbouring
+    // token blocks with a vocabulary split (FWD) or tile (BWD_G), in the same
+    // grouped raster (group_n even, so groups hold whole pairs); the CTA of
+    // rank r takes block 2p + r, which does not exist for the last pair of an
+    // odd number of blocks.
+    static_assert(MODE != MODE_GRAD, "the gradient GEMM runs one CTA per tile");
+    constexpr bool kFwd = MODE != MODE_BWD_G;
+    const int nbx = (!kFwd || a.n_dev) ? dm.nb : a.n_blocks;
+    const int nbp = (nbx + 1) >> 1, gp = a.group_n >> 1;
+    const int width = kFwd ? a.splits : a.v_tiles;
+    const int per_group = gp * width;
     const int g = item / per_group, j = item - g * per_group;
-    const int gpn = min(gp, (a.n_blocks >> 1) - g * gp);
-    const int m = g * a.group_n + 2 * (j % gpn) + static_cast<int>(cluster_ctarank());
-    const int s = j / gpn;
-    const int t0 = static_cast<int>(static_cast<long long>(s) * a.v_tiles / a.splits);
-    const int t1 = static_cast<int>(static_cast<long long>(s + 1) * a.v_tiles / a.splits);
-    for (int t = t0; t < t1; ++t) {
-      if (!f(Tile{KIND_MAIN, m, t, s, t == t0, t == t1 - 1})) return false;
+    const int gpn = min(gp, nbp - g * gp);
+    const int m = 2 * (g * gp + j % gpn) + static_cast<int>(cluster_ctarank());
+    const bool live = m < nbx;
+    if constexpr (!kFwd) {
+      return f(Tile{KIND_MAIN, m, j / gpn, 0, true, true, live});
+    } else {
+      const int s = j / gpn;
+      const int t0 = static_cast<int>(static_cast<long long>(s) * a.v_tiles / a.splits);
+      const int t1 = static_cast<int>(static_cast<long long>(s + 1) * a.v_tiles / a.splits);
+      for (int t = t0; t < t1; ++t) {
+        if (!f(Tile{KIND_MAIN, m, t, s, t == t0, t == t1 - 1, live})) return false;
+      }
+      return true;
     }
-    return true;
   } else if constexpr (MODE == MODE_FWD || MODE == MODE_FWD_STAGE) {
     // Grouped raster as in BWD_G: groups of group_n token blocks, the token
     // block fastest inside a group, then the vocabulary split.  The CTAs of
@@ -328,13 +345,13 @@ __device__ __forceinline__ void producer_loop(const GemmArgs& a, const SmemLayou
   int stage = 0;
   uint32_t phase = 0;
   uint32_t issued_mask = 0, issued_par = 0;  // per stage: ever issued, parity of last issue
-  const Dims dm = dims_of<MODE>(a);
+  const Dims dm = dims_of<MODE, PAIR>(a);
   // BWD_G: the next work item is fetched while the current one's loads are
   // issued; the atomic's latency (about a microsecond) would otherwise stall
   // the pipeline at every boundary of its short one-tile items.  The other
   // modes fetch when they need one: their items are long, and holding a
   // reserved item while busy would unbalance the end of a launch.
-  constexpr bool kAhead = MODE == MODE_BWD_G;
+  constexpr bool kAhead = MODE == MODE_BWD_G && !PAIR;
   int next = kAhead ? atomicAdd(a.counter, 1) : 0;
   // CTA pairs take items in a fixed order (cluster c: c, c + clusters, ...),
   // the same in both CTAs, so neither needs the other's schedule; forward
@@ -447,7 +464,7 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& a, const SmemLayout& L,
   int acc = 0;
   uint32_t acc_phase = 0;
   bool issued_any = false;
-  const Dims dm = dims_of<MODE>(a);
+  const Dims dm = dims_of<MODE, PAIR>(a);
   for (int k = 0;; ++k) {
     const int item = ring_take(L, k, a);
     if (item < 0) break;
@@ -623,7 +640,7 @@ template <bool CAP>
 __device__ __forceinline__ void epi_fwd(const GemmArgs& a, const SmemLayout& L, const Tile& t, int acc,
                                         EpiCtx& e, FwdState& st) {
   const int row = t.m * BM + e.q * 32 + static_cast<int>(lane_id());
-  const bool in_range = row < a.N;
+  const bool in_range = t.live && row < a.N;
   const long long xr = in_range ? static_cast<long long>(__ldg(a.x + row)) : -1ll;
   if (t.first) {
     st.run_m = NEG_BIG;
@@ -674,8 +691,8 @@ __device__ __forceinline__ void epi_fwd_stage(const GemmArgs& a, const SmemLayou
   const uint32_t lane = lane_id();
   const int row0 = t.m * BM + e.q * 32;  // first row of this warp's quadrant
   const int row = row0 + static_cast<int>(lane);
-  const bool in_range = row < a.N;
-  const bool store = row0 < a.N;  // uniform: the box starts inside the staging rows
+  const bool in_range = t.live && row < a.N;
+  const bool store = t.live && row0 < a.N;  // uniform: the box starts inside the staging rows
   const long long xr = in_range ? static_cast<long long>(__ldg(a.x + row)) : -1ll;
   if (t.first) {
     st.run_m = NEG_BIG;
@@ -753,7 +770,7 @@ __device__ __forceinline__ bool epi_bwd_g(const GemmArgs& a, const SmemLayout& L
   // their G is 0 without a per-element test.
   long long xr = -1;
   float lse2 = INFINITY, w = 0.0f;
-  if (row < a.N) {
+  if (t.live && row < a.N) {
     const long long xi = static_cast<long long>(__ldg(a.x + row));
     if ((xi != a.ignore_index) && xi >= 0 && xi < a.V) {
       xr = xi;
@@ -846,13 +863,13 @@ __device__ __forceinline__ bool epi_bwd_g(const GemmArgs& a, const SmemLayout& L
       __syncwarp();
       const int gx = t.n * BN + 128 * h;  // column inside the chunk buffer
       const int gy = t.m * BM + e.q * 32;
-      if (lane == 0 && gy < a.N) {  // no store starts outside the buffer
+      if (lane == 0 && t.live && gy < a.N) {  // no store starts outside the buffer
         tma_store_2d(&a.tmOut, e.buf, gx, gy);
         tma_store_2d(&a.tmOut, e.buf + 4096, gx + 64, gy);
         bulk_commit();
       }
     }
-    if (e.q == 0 && lane == 0) {
+    if (e.q == 0 && lane == 0 && t.live) {
       const int vt128 = (vt0 >> 7) + h;
       if (vt128 < a.bm_ld) {
         a.bitmap[static_cast<size_t>(t.m) * a.bm_ld + vt128] = keep ? 1 : 0;
@@ -1039,7 +1056,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& a, const SmemLayou
   FwdState st{NEG_BIG, 0.0f};
   int acc = 0;
   uint32_t acc_phase = 0;
-  const Dims dm = dims_of<MODE>(a);
+  const Dims dm = dims_of<MODE, PAIR>(a);
   for (int k = 0;; ++k) {
     int item = 0;
     if (lane_id() == 0) item = ring_take(L, k, a);

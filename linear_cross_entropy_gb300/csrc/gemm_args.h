@@ -21,6 +21,7 @@ constexpr uint32_t TMEM_COLS = 512;
 // CTA pairs: TMEM columns allocated (together, by both CTAs) and accumulators
 constexpr uint32_t PAIR_TMEM_COLS = 512;
 constexpr int PAIR_ACCS = 2;
+constexpr int PAIR_MIN_BLOCKS = 64;  // recompute as CTA pairs from this many 128-row token blocks
 constexpr int RING = 4;  // depth of the work-item ring between the scheduler and the consumers
 constexpr int BAR_BYTES = 512;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_EPI_WARPS * EPI_WARP_BYTES + BAR_BYTES;

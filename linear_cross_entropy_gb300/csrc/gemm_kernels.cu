@@ -20,6 +20,8 @@ cudaError_t prepare_gemm_kernels() {
   if ((e = set_smem<MODE_FWD_STAGE, true>()) != cudaSuccess) return e;
   if ((e = set_smem<MODE_FWD, false, true>()) != cudaSuccess) return e;
   if ((e = set_smem<MODE_FWD, true, true>()) != cudaSuccess) return e;
+  if ((e = set_smem<MODE_BWD_G, false, true>()) != cudaSuccess) return e;
+  if ((e = set_smem<MODE_BWD_G, true, true>()) != cudaSuccess) return e;
   return set_smem<MODE_GRAD, false>();
 }
 
@@ -49,11 +51,19 @@ int gemm_pair_clusters(int sms) {
   return n;
 }
 
-cudaError_t launch_gemm_fwd_pairs(const GemmArgs& args, int clusters, cudaStream_t stream) {
+cudaError_t launch_gemm_pairs(int mode, const GemmArgs& args, int clusters, cudaStream_t stream) {
   cudaLaunchAttribute attr;
   const cudaLaunchConfig_t cfg = pair_config(clusters, stream, &attr);
-  if (args.softcap > 0.0f) return cudaLaunchKernelEx(&cfg, cce_gemm_kernel<MODE_FWD, true, true>, args);
-  return cudaLaunchKernelEx(&cfg, cce_gemm_kernel<MODE_FWD, false, true>, args);
+  const bool cap = args.softcap > 0.0f;
+  switch (mode) {
+    case MODE_FWD:
+      return cap ? cudaLaunchKernelEx(&cfg, cce_gemm_kernel<MODE_FWD, true, true>, args)
+                 : cudaLaunchKernelEx(&cfg, cce_gemm_kernel<MODE_FWD, false, true>, args);
+    case MODE_BWD_G:
+      return cap ? cudaLaunchKernelEx(&cfg, cce_gemm_kernel<MODE_BWD_G, true, true>, args)
+                 : cudaLaunchKernelEx(&cfg, cce_gemm_kernel<MODE_BWD_G, false, true>, args);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 // One thread waits on an mbarrier that nothing ever arrives on, through the

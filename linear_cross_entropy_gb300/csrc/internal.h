@@ -12,11 +12,12 @@ namespace cce {
 // Launches cce_gemm_kernel<mode> with `grid` persistent CTAs on `stream`.
 cudaError_t launch_gemm(int mode, const GemmArgs& args, int grid, cudaStream_t stream);
 
-// The forward GEMM as clusters of two CTAs sharing each MMA (M = 256): a.items
-// pairs of token blocks x splits, `clusters` persistent pairs.
-cudaError_t launch_gemm_fwd_pairs(const GemmArgs& args, int clusters, cudaStream_t stream);
+// cce_gemm_kernel<mode> (FWD, BWD_G) as `clusters` persistent
+// clusters of two CTAs sharing each MMA (M = 256) over pairs of token blocks;
+// args.tmB2 holds C in 128-row boxes and args.group_n is even.
+cudaError_t launch_gemm_pairs(int mode, const GemmArgs& args, int clusters, cudaStream_t stream);
 
-// How many CTA pairs of the forward GEMM fit on the device at once (0: none).
+// How many CTA pairs of the GEMM kernel fit on the device at once (0: none).
 int gemm_pair_clusters(int sms);
 
 // Launches the bounded-wait self-test kernel (see cce_selftest_wait_timeout).

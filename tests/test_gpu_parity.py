@@ -54,6 +54,19 @@ def test_ragged_shapes_unfiltered(N, D, V, reduction):
     assert_grads_close(got, ref["dE"], ref["dC"], TOL_GRAD, x)
 
 
+@pytest.mark.parametrize("ignore_frac", [0.0, 0.1])
+def test_many_token_blocks_cta_pairs(ignore_frac):
+    """Enough token blocks (65) that the forward and the recompute run as CTA
+    pairs, with an odd block count (the last pair half empty) in the forward
+    and, after compaction of the ignored rows, in the recompute."""
+    N, D, V = 65 * 128, 64, 3000
+    w, (E, C, x) = make(W.small("pairs", N, D, V, ignore_frac=ignore_frac))
+    got = run_cuda(E, C, x, reduction="mean", filter_eps=0.0)
+    ref = oracle_full(E, C, x, reduction="mean")
+    assert_forward_close(got, ref, "mean", x)
+    assert_grads_close(got, ref["dE"], ref["dC"], TOL_GRAD, x)
+
+
 def test_target_in_short_final_panel():
     """'Correctness': a ragged vocabulary with targets inside the short final panel."""
     N, D, V = 200, 64, 1000 + 37
