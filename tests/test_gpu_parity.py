@@ -91,12 +91,15 @@ def test_multi_chunk_backward():
     assert_grads_close(got, ref["dE"], ref["dC"], TOL_GRAD, x)
 
 
-def test_filter_matches_filtered_oracle():
+@pytest.mark.parametrize("D", [128, 256])
+def test_filter_matches_filtered_oracle(D):
     """Frequent-token inputs: softmax mass sits in the lowest 256 ids, so most
     128 x 128 tiles are skipped.  The filtered result matches the filtered
     oracle tightly and the unfiltered oracle within 1e-2; the skip count
-    equals the oracle's tile survival map (no tile lies near eps here)."""
-    N, D, V = 512, 128, 6000
+    equals the oracle's tile survival map (no tile lies near eps here).
+    D = 256: one full-width gradient D tile, whose MN-major B operand comes in
+    one 3-D box of four 64-column groups."""
+    N, V = 512, 6000
     E, C, x = W.frequent_token_inputs(N, D, V, n_freq=256, seed=3)
     got = run_cuda(E, C, x, reduction="mean", filter_eps=O.FILTER_EPS)
     ref = oracle_full(E, C, x, reduction="mean", filter_eps=O.FILTER_EPS)

@@ -88,6 +88,19 @@ def test_single_call_filtered(staging):
     assert got["stats"]["skipped"] > keep.size // 2
 
 
+def test_single_call_filtered_full_width_d_tile():
+    """D = 256 (one full-width gradient D tile, 3-D B boxes) with the filter
+    skipping most tiles."""
+    E_bits, C_bits, x = W.frequent_token_inputs(1024, 256, 9000, n_freq=256)
+    got = _run(E_bits, C_bits, x, reduction="sum", filter_eps=O.FILTER_EPS)
+    Ef, Cf = O.from_bits(E_bits, C_bits)
+    ref = O.loss_and_grad(Ef, Cf, x, reduction="sum", filter_eps=O.FILTER_EPS)
+    _check(got, ref, x, TOL_GRAD_FILTERED)
+    keep = ref["keep"]
+    assert abs(got["stats"]["skipped"] - int((~keep).sum())) <= max(1, keep.size // 200)
+    assert got["stats"]["skipped"] > keep.size // 2
+
+
 def test_single_call_softcap():
     w = W.small("cap", 300, 136, 5000)
     E_bits, C_bits, x = W.make_inputs(w)
