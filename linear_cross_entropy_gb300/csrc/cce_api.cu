@@ -122,38 +122,53 @@ constexpr int COMPACT_THREADS = 1024;
 
 __global__ void compact_kernel(const int64_t* __restrict__ x, int N, int V, long long ignore_index,
                                int* __restrict__ pos, int* __restrict__ ridx, int* count, int32_t* dev_err) {
-  __shared__ int scan[COMPACT_THREADS];
-  const int t = threadIdx.x;
-  const int per = (N + COMPACT_THREADS - 1) / COMPACT_THREADS;
-  const int r0 = min(N, t * per), r1 = min(N, r0 + per);
-  int c = 0;
+  // Tiles of COMPACT_THREADS consecutive rows, one row per thread (coalesced
+  // loads and stores), in order; a tile's ranks come from warp ballots and a
+  // scan of the 32 warp counts, offset by the rows taken in earlier tiles.
+  static_assert(COMPACT_THREADS == 32 * 32, "one scan lane per warp");
+  __shared__ int warp_off[32];
+  __shared__ int tile_total;
+  const int t = static_cast<int>(threadIdx.x), lane = t & 31, w = t >> 5;
+  int base = 0;
   bool bad = false;
-  for (int r = r0; r < r1; ++r) {
-    const long long xi = static_cast<long long>(x[r]);
-    if (xi == ignore_index) continue;
-    if (xi < 0 || xi >= V) {
-      bad = true;
-      continue;
+  for (int r0 = 0; r0 < N; r0 += COMPACT_THREADS) {
+    const int r = r0 + t;
+    bool take = false;
+    if (r < N) {
+      const long long xi = static_cast<long long>(x[r]);
+      if (xi != ignore_index) {
+        if (xi < 0 || xi >= V) {
+          bad = true;
+        } else {
+          take = true;
+        }
+      }
     }
-    ++c;
-  }
-  if (bad && dev_err) atomicOr(reinterpret_cast<int*>(dev_err), CCE_DEVERR_TARGET_RANGE);
-  scan[t] = c;
-  __syncthreads();
-  for (int off = 1; off < COMPACT_THREADS; off <<= 1) {  // inclusive scan (Hillis-Steele)
-    const int v = t >= off ? scan[t - off] : 0;
+    const unsigned m = __ballot_sync(0xffffffffu, take);
+    if (lane == 0) warp_off[w] = __popc(m);
     __syncthreads();
-    scan[t] += v;
+    if (w == 0) {  // exclusive scan of the warp counts
+      const int v = warp_off[lane];
+      int inc = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += n;
+      }
+      warp_off[lane] = inc - v;
+      if (lane == 31) tile_total = inc;
+    }
     __syncthreads();
+    if (r < N) {
+      const int k = base + warp_off[w] + __popc(m & ((1u << lane) - 1u));
+      pos[r] = take ? k : -1;
+      if (take) ridx[k] = r;
+    }
+    base += tile_total;
+    __syncthreads();  // warp_off and tile_total are rewritten by the next tile
   }
-  int k = scan[t] - c;
-  for (int r = r0; r < r1; ++r) {
-    const long long xi = static_cast<long long>(x[r]);
-    const bool take = xi != ignore_index && xi >= 0 && xi < V;
-    pos[r] = take ? k : -1;
-    if (take) ridx[k++] = r;
-  }
-  if (t == COMPACT_THREADS - 1) *count = scan[t];
+  if (__syncthreads_or(bad) && t == 0 && dev_err) atomicOr(reinterpret_cast<int*>(dev_err), CCE_DEVERR_TARGET_RANGE);
+  if (t == 0) *count = base;
 }
 
 // Compact copies of the rows that take part: E_c [k] = E[ridx[k]] and the
