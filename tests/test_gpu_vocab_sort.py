@@ -100,7 +100,7 @@ def test_logit_sums_and_their_order(name, case):
     bound = _sum_bound(Ef, Cf, x)
     err = np.abs(sums - ref)
     assert np.all(err <= bound), f"logit sum off by {err.max():.3e} (bound {bound[np.argmax(err)]:.3e})"
-    # the device's order of its own sums, judged by the oracle's sums
+    # the device's order of its own sums, checked against the oracle's sums
     perm = cce.vocab_order(torch.from_numpy(sums.astype(np.float32)).cuda()).cpu().numpy().astype(np.int64)
     assert np.array_equal(np.sort(perm), np.arange(len(perm)))
     a, b = perm[:-1], perm[1:]
