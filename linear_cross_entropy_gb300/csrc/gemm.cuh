@@ -44,6 +44,13 @@
 // items are handed out dynamically (atomicAdd on a counter) and passed to the
 // MMA and epilogue warps through a small ring in shared memory, so every CTA
 // stays busy until the work runs out; the longest tiles are handed out first.
+//
+// CTA pairs (template flag PAIR; MODE_FWD always, MODE_BWD_G from 64 token
+// blocks): clusters of two CTAs on neighbouring SMs take the items of a pair
+// of token blocks in a fixed order.  Each CTA loads its 128 rows of A and half
+// of the 256-row B tile; the even CTA issues one MMA of M = 256 for both
+// (tcgen05 cta_group::2) and commits to both CTAs' barriers, and each CTA's
+// epilogue reads its own 128 accumulator rows.
 #pragma once
 
 #include <cuda_bf16.h>
