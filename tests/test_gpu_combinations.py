@@ -158,3 +158,23 @@ def test_single_call_filter_options(outputs, fde, fdc, softcap):
     _grads_ok(dE, dC, ref["dE"], ref["dC"], TOL_GRAD_FILTERED)
     keep = ref["keep"]
     assert abs(st["skipped"] - int((~keep).sum())) <= max(1, keep.size // 200)
+
+
+@pytest.mark.parametrize("softcap,sort", [(20.0, False), (0.0, True), (20.0, True)])
+def test_many_blocks_cta_pairs_with_softcap_and_sorting(softcap, sort):
+    """65 token blocks (an odd count): the forward and the recompute run as
+    CTA pairs, here in their softcapped instantiations and over the sorted
+    vocabulary, against the oracle's filtered gradients (sorted order when
+    sorting)."""
+    E_bits, C_bits, x = W.frequent_token_inputs(65 * 128, 64, 4000, n_freq=256, scatter=True, unigram=8.0)
+    dE, dC, st = _two_calls(E_bits, C_bits, x, softcap=softcap, sort=sort)
+    if sort:
+        rdE, rdC, keep = _sorted_oracle(E_bits, C_bits, x, softcap=softcap)
+    else:
+        Ef, Cf = O.from_bits(E_bits, C_bits)
+        f = O.forward(Ef, Cf, x, reduction="mean", softcap=softcap)
+        w = O.row_weights(x, -100, "mean", 1.0, f["count"])
+        rdE, rdC, keep = O.backward_filtered(Ef, Cf, x, f["lse"], w, 128, 128, O.FILTER_EPS, softcap=softcap,
+                                             compact_ignored=True)
+    _grads_ok(dE, dC, rdE, rdC, TOL_GRAD_FILTERED)
+    assert abs(st["skipped"] - int((~keep).sum())) <= max(1, keep.size // 200)
