@@ -301,13 +301,15 @@ def test_mostly_ignored_batch_is_compacted():
             assert got["stats"]["tiles"] == ref["keep"].size
 
 
-@pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
-def test_forward_skipping_ignored_rows(reduction):
+@pytest.mark.parametrize("reduction,ignore_frac", [("mean", 0.3), ("sum", 0.3), ("none", 0.3), ("mean", 0.1)])
+def test_forward_skipping_ignored_rows(reduction, ignore_frac):
     """CCE_FWD_SKIP_IGNORED: the GEMM runs over the compacted rows only; the
     loss is the oracle's, the LSE of rows that take part too, and the other
-    rows read 0; the backward fed with that LSE gives the oracle's gradients."""
+    rows read 0; the backward fed with that LSE gives the oracle's gradients.
+    480 rows take part at ignore_frac 0.3 (4 token blocks), 626 at 0.1 (5: the
+    forward's last CTA pair is half empty)."""
     import linear_cross_entropy_gb300 as cce
-    w = W.small("skip", 700, 136, 5000, ignore_frac=0.3, reduction=reduction)
+    w = W.small("skip", 700, 136, 5000, ignore_frac=ignore_frac, reduction=reduction)
     E_bits, C_bits, x = W.make_inputs(w)
     x = x.copy()
     x[[3, 4, 5]] = O.IGNORE_INDEX
