@@ -98,30 +98,49 @@ class _DeferredErrors:
     raise_pending_errors().  A training step therefore never waits for the
     GPU mid-step; an error surfaces one call or more after the call that set
     it (the kernels treat the offending rows as ignored and complete), and
-    each call's word is reported at most once."""
+    each call's word is reported at most once.  The pinned words and events
+    are a ring per device, allocated once: no pinned allocation per call."""
+
+    SLOTS = 64
 
     def __init__(self):
         self._pending = []  # (pinned word, event, call name), in issue order
+        self._rings = {}  # device index -> [pinned int32 words, events, next slot]
 
     def watch(self, dev_err, what):
-        host = torch.empty(1, dtype=torch.int32, pin_memory=True)
-        host.copy_(dev_err, non_blocking=True)
-        ev = torch.cuda.Event()
-        ev.record()
-        self._pending.append((host, ev, what))
+        ring = self._rings.get(dev_err.device.index)
+        if ring is None:
+            ring = [torch.zeros(self.SLOTS, dtype=torch.int32, pin_memory=True), [None] * self.SLOTS, 0]
+            self._rings[dev_err.device.index] = ring
+        words, events, slot = ring
+        ring[2] = (slot + 1) % self.SLOTS
+        word = words[slot:slot + 1]
+        while any(w.data_ptr() == word.data_ptr() for w, _, _ in self._pending):
+            self._take_oldest(wait=True)  # the slot's previous word is read before the slot is reused
+        with torch.cuda.device(dev_err.device):
+            word.copy_(dev_err, non_blocking=True)
+            if events[slot] is None:
+                events[slot] = torch.cuda.Event()
+            events[slot].record()
+        self._pending.append((word, events[slot], what))
         self.poll(keep_last=True)
+
+    def _take_oldest(self, wait):
+        word, ev, what = self._pending[0]
+        if wait:
+            ev.synchronize()
+        elif not ev.query():
+            return False
+        self._pending.pop(0)
+        _raise_word(int(word[0]), what)
+        return True
 
     def poll(self, wait=False, keep_last=False):
         """Raises for the oldest landed word that is not clean; keep_last
         leaves the newest call's word for later."""
         while len(self._pending) > (1 if keep_last else 0):
-            host, ev, what = self._pending[0]
-            if wait:
-                ev.synchronize()
-            elif not ev.query():
+            if not self._take_oldest(wait):
                 return
-            self._pending.pop(0)
-            _raise_word(int(host[0]), what)
 
 
 _deferred = _DeferredErrors()

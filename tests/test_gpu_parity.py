@@ -204,6 +204,36 @@ def test_autograd_path_reports_errors_without_stalling():
     cce.raise_pending_errors()
 
 
+def test_deferred_error_words_wrap_around_their_ring():
+    """More autograd calls than the ring of pinned error words holds: clean
+    calls report nothing, and a bad target after them is reported once per
+    library call that saw it."""
+    import linear_cross_entropy_gb300 as cce
+    from tests.gpu_util import to_device
+    w, (E, C, x) = make(W.small("o", 64, 64, 500, ignore_frac=0.0))
+    Et, Ct, xt = to_device(E, C, x)
+    for _ in range(cce._DeferredErrors.SLOTS + 5):  # two calls (forward, backward) each
+        Eg = Et.clone().requires_grad_(True)
+        cce.linear_cross_entropy(Eg, Ct, xt).backward()
+    cce.raise_pending_errors()
+    x = x.copy()
+    x[7] = 500
+    Et, Ct, xt = to_device(E, C, x)
+    Eg = Et.clone().requires_grad_(True)
+    reported = []
+    try:
+        cce.linear_cross_entropy(Eg, Ct, xt).backward()
+    except cce.CCEError as e:
+        reported.append(e.status)
+    while True:
+        try:
+            cce.raise_pending_errors()
+            break
+        except cce.CCEError as e:
+            reported.append(e.status)
+    assert reported == [8, 8]
+
+
 def test_autograd_function_matches_oracle():
     import linear_cross_entropy_gb300 as cce
     from tests.gpu_util import to_device
