@@ -94,7 +94,10 @@ size_t cce_backward_workspace_bytes(int64_t N, int64_t D, int64_t V);
  *   reduction     CCE_RED_NONE: loss[i] = loss_i for all N rows (0 on ignored
  *                 rows); CCE_RED_SUM: loss[0] = sum_i loss_i;
  *                 CCE_RED_MEAN: loss[0] = sum_i loss_i / max(count, 1), count =
- *                 number of non-ignored rows (a fully ignored batch gives 0).
+ *                 number of non-ignored rows.  A fully ignored batch gives
+ *                 loss 0 and zero gradients, as the "cut-cross-entropy" card
+ *                 ("Correctness") states; this differs from PyTorch's
+ *                 cross_entropy, whose mean over no rows is NaN.
  *   loss          [N] fp32 for NONE, else [1] fp32 (written).
  *   lse           [N] fp32 (written): LSE_i for every row, ignored rows too.
  *                 Keep it for cce_backward.
@@ -237,6 +240,37 @@ cce_status cce_backward_ex(const void* E, const void* C, const int64_t* x, const
 size_t cce_backward_workspace_bytes_ex(int64_t N, int64_t D, int64_t V, int flags);
 
 /*
+ * Backward with a caller-chosen staging budget.  cce_backward_ex is
+ * cce_backward_ex2 with max_staging_bytes = 0.  The backward walks the
+ * vocabulary in chunks of vc columns ("Cut Your Losses ...", "The Combined
+ * Backward Pass (Algorithm 4)", blocked over the vocabulary): per chunk it
+ * recomputes the logits, stages the filtered, scaled gradient G-hat of the
+ * chunk in the workspace as bf16 [N][vc], and contracts it into dC (the
+ * chunk's rows, written once) and into an fp32 dE accumulator [N][D]
+ * (stored by the first chunk, added by the later ones).
+ * max_staging_bytes bounds that G-hat buffer: vc is the largest multiple of
+ * 256 with N * vc * 2 <= max_staging_bytes, at least 256 and at most 65,536
+ * (and at most ceil(V / 2) rounded up to 256, so the buffer is never an
+ * N x V matrix).  0 selects the default, 512 MiB with vc >= 2048.  A
+ * smaller budget lowers the workspace (the other parts are fixed: the fp32
+ * dE accumulator, N * D * 4 bytes, and a compact copy of the rows that take
+ * part, N * D * 2 bytes) but adds one pass over the dE accumulator (read +
+ * write, N * D * 8 bytes) per extra chunk.  Results are the same at every
+ * budget up to the fp32 summation order of dE across chunks.  Arguments,
+ * checks and status codes otherwise as cce_backward_ex; the workspace must
+ * hold cce_backward_workspace_bytes_ex2(N, D, V, flags, max_staging_bytes).
+ */
+cce_status cce_backward_ex2(const void* E, const void* C, const int64_t* x, const float* lse,
+                            const float* grad_out, int64_t N, int64_t D, int64_t V, int64_t ignore_index,
+                            int reduction, float softcap, float filter_eps, int filter_flags,
+                            size_t max_staging_bytes, void* dE, void* dC, void* workspace, size_t ws_bytes,
+                            int32_t* dev_err, int64_t* dev_stats, void* stream);
+size_t cce_backward_workspace_bytes_ex2(int64_t N, int64_t D, int64_t V, int flags, size_t max_staging_bytes);
+/* The chunk width vc that cce_backward_ex2 uses for N rows, V vocabulary
+ * entries and this budget (0 for invalid sizes). */
+uint64_t cce_backward_chunk_cols(int64_t N, int64_t V, size_t max_staging_bytes);
+
+/*
  * The two steps of vocabulary sorting, exposed on their own (the backward
  * with CCE_SORT_VOCAB runs the same kernels on its compacted rows).
  *
@@ -329,6 +363,20 @@ cce_status cce_memory_accounting(int64_t N, int64_t D, int64_t V, cce_memory_rep
  * wait gives up and ORs CCE_DEVERR_TIMEOUT into *dev_err (device memory).  No
  * fault, no hang: the context stays usable.  Asynchronous on `stream`. */
 cce_status cce_selftest_wait_timeout(int32_t* dev_err, uint32_t timeout_us, void* stream);
+
+/* Self-test of the abort path between the two CTAs of a CTA pair (the
+ * forward and recompute GEMMs run as clusters of two CTAs whose waits depend
+ * on each other).  Launches one cluster of two CTAs running the pair's
+ * handshake: the odd CTA arrives on a barrier of the even CTA, which answers
+ * on a barrier of the odd CTA.  With hold = 1 the odd CTA holds its arrive
+ * back: the even CTA's bounded wait runs out after timeout_us (1 .. 10^7)
+ * microseconds, the odd CTA's wait for the answer runs out as well, the odd
+ * CTA waits the GEMM's bounded 10 ms grace for copies in flight, and both
+ * CTAs meet at the final cluster barrier and exit; CCE_DEVERR_TIMEOUT is
+ * OR-ed into *dev_err.  With hold = 0 the handshake completes and *dev_err is
+ * left alone.  No fault, no hang: the context stays usable.  Other hold
+ * values return CCE_ERR_ARG.  Asynchronous on `stream`. */
+cce_status cce_selftest_pair_timeout(int32_t* dev_err, uint32_t timeout_us, int hold, void* stream);
 
 /* Human-readable name of a status. */
 const char* cce_status_string(cce_status s);

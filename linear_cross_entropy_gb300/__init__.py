@@ -29,7 +29,7 @@ FILTER_EPS = 2.0 ** -12  # finfo(bf16).eps / 32
 
 __all__ = [
     "linear_cross_entropy", "cce_forward", "cce_backward", "CCEError", "FILTER_EPS",
-    "forward_workspace_bytes", "backward_workspace_bytes", "memory_report", "kernel_launch_count",
+    "forward_workspace_bytes", "backward_workspace_bytes", "backward_chunk_cols", "memory_report", "kernel_launch_count",
     "Profiler", "vocab_logit_sums", "vocab_order", "cce_loss_and_grad", "fused_linear_cross_entropy",
     "loss_and_grad_workspace_bytes", "raise_pending_errors",
 ]
@@ -64,9 +64,14 @@ def forward_workspace_bytes(N, D, V, *, skip_ignored=False) -> int:
     return int(_lib.load().cce_forward_workspace_bytes_ex(N, D, V, _lib.FWD_SKIP_IGNORED if skip_ignored else 0))
 
 
-def backward_workspace_bytes(N, D, V, *, filter_outputs="both", vocab_sort=False) -> int:
+def backward_workspace_bytes(N, D, V, *, filter_outputs="both", vocab_sort=False, max_staging_bytes=0) -> int:
     flags = FILTER_OUTPUTS[filter_outputs] | (_lib.SORT_VOCAB if vocab_sort else 0)
-    return int(_lib.load().cce_backward_workspace_bytes_ex(N, D, V, flags))
+    return int(_lib.load().cce_backward_workspace_bytes_ex2(N, D, V, flags, int(max_staging_bytes)))
+
+
+def backward_chunk_cols(N, V, max_staging_bytes=0) -> int:
+    """Vocabulary columns per backward chunk for this G-hat staging budget."""
+    return int(_lib.load().cce_backward_chunk_cols(N, V, int(max_staging_bytes)))
 
 
 def memory_report(N, D, V) -> dict:
@@ -106,23 +111,39 @@ class _DeferredErrors:
     def __init__(self):
         self._pending = []  # (pinned word, event, call name), in issue order
         self._rings = {}  # device index -> [pinned int32 words, events, next slot]
+        self._found = []  # errors read while freeing a slot, raised at the next poll, in order
 
-    def watch(self, dev_err, what):
-        ring = self._rings.get(dev_err.device.index)
-        if ring is None:
-            ring = [torch.zeros(self.SLOTS, dtype=torch.int32, pin_memory=True), [None] * self.SLOTS, 0]
-            self._rings[dev_err.device.index] = ring
-        words, events, slot = ring
-        ring[2] = (slot + 1) % self.SLOTS
-        word = words[slot:slot + 1]
-        while any(w.data_ptr() == word.data_ptr() for w, _, _ in self._pending):
-            self._take_oldest(wait=True)  # the slot's previous word is read before the slot is reused
+    def _make_ring(self, device):
+        return [torch.zeros(self.SLOTS, dtype=torch.int32, pin_memory=True), [None] * self.SLOTS, 0]
+
+    def _record(self, word, events, slot, dev_err):
+        """Copies *dev_err into the pinned word behind the call's kernels and
+        returns the event that marks the copy's completion."""
         with torch.cuda.device(dev_err.device):
             word.copy_(dev_err, non_blocking=True)
             if events[slot] is None:
                 events[slot] = torch.cuda.Event()
             events[slot].record()
-        self._pending.append((word, events[slot], what))
+        return events[slot]
+
+    def watch(self, dev_err, what):
+        key = dev_err.device.index
+        ring = self._rings.get(key)
+        if ring is None:
+            ring = self._make_ring(dev_err.device)
+            self._rings[key] = ring
+        words, events, slot = ring
+        ring[2] = (slot + 1) % self.SLOTS
+        word = words[slot:slot + 1]
+        # The slot's previous word is read before the slot is reused.  An
+        # error found there is kept, not raised yet, so that this call's own
+        # word is recorded (and reported later) whatever the older one holds.
+        while any(w.data_ptr() == word.data_ptr() for w, _, _ in self._pending):
+            try:
+                self._take_oldest(wait=True)
+            except CCEError as e:
+                self._found.append(e)
+        self._pending.append((word, self._record(word, events, slot, dev_err), what))
         self.poll(keep_last=True)
 
     def _take_oldest(self, wait):
@@ -138,6 +159,8 @@ class _DeferredErrors:
     def poll(self, wait=False, keep_last=False):
         """Raises for the oldest landed word that is not clean; keep_last
         leaves the newest call's word for later."""
+        if self._found:
+            raise self._found.pop(0)
         while len(self._pending) > (1 if keep_last else 0):
             if not self._take_oldest(wait):
                 return
@@ -187,14 +210,16 @@ FILTER_OUTPUTS = {"both": 3, "dE": 1, "dC": 2, "none": 0}
 
 
 def cce_backward(E, C, x, lse, grad_out, ignore_index=-100, reduction="mean", filter_eps=FILTER_EPS, *,
-                 filter_outputs="both", softcap=0.0, vocab_sort=False, stream=None, check_errors=True,
-                 workspace=None, dev_err=None, stats=False, dE=None, dC=None):
+                 filter_outputs="both", softcap=0.0, vocab_sort=False, max_staging_bytes=0, stream=None,
+                 check_errors=True, workspace=None, dev_err=None, stats=False, dE=None, dC=None):
     """Returns (dE, dC) or (dE, dC, {tiles, skipped}) with stats=True.
 
     filter_outputs: which gradients skip the filtered tiles -- "both" (plain
     CCE), "dE" (dC from every tile: CCE-Kahan-FullC), "dC" (FullE) or "none".
     vocab_sort: filter over the vocabulary sorted by average logit (the
-    gradients are the same; the tiles, and so what the filter skips, differ)."""
+    gradients are the same; the tiles, and so what the filter skips, differ).
+    max_staging_bytes: bound of the bf16 G-hat chunk buffer in the workspace
+    (0: the default 512 MiB); a smaller budget means more vocabulary chunks."""
     _check_inputs(E, C, x)
     N, D = E.shape
     V = C.shape[0]
@@ -210,17 +235,17 @@ def cce_backward(E, C, x, lse, grad_out, ignore_index=-100, reduction="mean", fi
     if dC is None:
         dC = torch.empty_like(C)
     flags = FILTER_OUTPUTS[filter_outputs] | (_lib.SORT_VOCAB if vocab_sort else 0)
-    need = int(lib.cce_backward_workspace_bytes_ex(N, D, V, flags))
+    need = int(lib.cce_backward_workspace_bytes_ex2(N, D, V, flags, int(max_staging_bytes)))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     if dev_err is None:
         dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
     st_t = torch.zeros(2, dtype=torch.int64, device=dev) if stats else None
     with torch.cuda.device(dev):
-        st = lib.cce_backward_ex(_ptr(E), _ptr(C), _ptr(x), _ptr(lse), _ptr(g), N, D, V, int(ignore_index), red,
-                                 float(softcap), float(filter_eps), flags, _ptr(dE), _ptr(dC),
-                                 _ptr(workspace), workspace.numel(), _ptr(dev_err), _ptr(st_t),
-                                 _stream_handle(stream))
+        st = lib.cce_backward_ex2(_ptr(E), _ptr(C), _ptr(x), _ptr(lse), _ptr(g), N, D, V, int(ignore_index), red,
+                                  float(softcap), float(filter_eps), flags, int(max_staging_bytes), _ptr(dE),
+                                  _ptr(dC), _ptr(workspace), workspace.numel(), _ptr(dev_err), _ptr(st_t),
+                                  _stream_handle(stream))
     _lib.check(st, "cce_backward")
     if check_errors:
         _raise_dev_err(dev_err)
@@ -232,39 +257,41 @@ def cce_backward(E, C, x, lse, grad_out, ignore_index=-100, reduction="mean", fi
 
 class LinearCrossEntropyFunction(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, E, C, x, ignore_index, reduction, filter_eps, filter_outputs, softcap, vocab_sort):
+    def forward(ctx, E, C, x, ignore_index, reduction, filter_eps, filter_outputs, softcap, vocab_sort,
+                max_staging_bytes):
         err = torch.zeros(1, dtype=torch.int32, device=E.device)
         loss, lse = cce_forward(E, C, x, ignore_index, reduction, softcap=softcap, check_errors=False, dev_err=err)
         _deferred.watch(err, "cce_forward")
         ctx.save_for_backward(E, C, x, lse)
-        ctx.cfg = (ignore_index, reduction, filter_eps, filter_outputs, softcap, vocab_sort)
+        ctx.cfg = (ignore_index, reduction, filter_eps, filter_outputs, softcap, vocab_sort, max_staging_bytes)
         return loss
 
     @staticmethod
     def backward(ctx, grad_loss):
         E, C, x, lse = ctx.saved_tensors
-        ignore_index, reduction, filter_eps, filter_outputs, softcap, vocab_sort = ctx.cfg
+        ignore_index, reduction, filter_eps, filter_outputs, softcap, vocab_sort, max_staging_bytes = ctx.cfg
         err = torch.zeros(1, dtype=torch.int32, device=E.device)
         dE, dC = cce_backward(E, C, x, lse, grad_loss, ignore_index, reduction, filter_eps,
                               filter_outputs=filter_outputs, softcap=softcap, vocab_sort=vocab_sort,
-                              check_errors=False, dev_err=err)
+                              max_staging_bytes=max_staging_bytes, check_errors=False, dev_err=err)
         _deferred.watch(err, "cce_backward")
-        return dE, dC, None, None, None, None, None, None, None
+        return dE, dC, None, None, None, None, None, None, None, None
 
 
 def linear_cross_entropy(E, C, x, ignore_index=-100, reduction="mean", filter_eps=FILTER_EPS,
-                         filter_outputs="both", softcap=0.0, vocab_sort=False):
+                         filter_outputs="both", softcap=0.0, vocab_sort=False, max_staging_bytes=0):
     """Cross-entropy of the logits E @ C^T against targets x, never materialised.
 
     E [N, D] bf16 (hidden states), C [V, D] bf16 (classifier weight), x [N]
     int64.  filter_eps is the backward's tile-skip threshold (0 disables);
     filter_outputs picks which gradients it applies to ("both", "dE", "dC",
     "none"); softcap > 0 caps the logits as softcap * tanh(logit / softcap);
-    vocab_sort filters over the vocabulary sorted by average logit.
+    vocab_sort filters over the vocabulary sorted by average logit;
+    max_staging_bytes bounds the backward's G-hat chunk buffer (0: default).
     Device errors (a target outside [0, V)) are raised without stalling the
     step: at a later call or at raise_pending_errors()."""
     return LinearCrossEntropyFunction.apply(E, C, x, ignore_index, reduction, filter_eps, filter_outputs,
-                                            softcap, vocab_sort)
+                                            softcap, vocab_sort, max_staging_bytes)
 
 
 def loss_and_grad_workspace_bytes(N, D, V, max_staging_bytes=0) -> int:

@@ -76,6 +76,13 @@ def load() -> ctypes.CDLL:
     lib.cce_backward_ex.restype = ctypes.c_int
     lib.cce_backward_workspace_bytes_ex.argtypes = [i64, i64, i64, ctypes.c_int]
     lib.cce_backward_workspace_bytes_ex.restype = sz
+    lib.cce_backward_ex2.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_int, ctypes.c_float,
+                                     ctypes.c_float, ctypes.c_int, sz, vp, vp, vp, sz, vp, vp, vp]
+    lib.cce_backward_ex2.restype = ctypes.c_int
+    lib.cce_backward_workspace_bytes_ex2.argtypes = [i64, i64, i64, ctypes.c_int, sz]
+    lib.cce_backward_workspace_bytes_ex2.restype = sz
+    lib.cce_backward_chunk_cols.argtypes = [i64, i64, sz]
+    lib.cce_backward_chunk_cols.restype = ctypes.c_uint64
     lib.cce_vocab_sort_workspace_bytes.argtypes = [i64, i64, i64]
     lib.cce_vocab_sort_workspace_bytes.restype = sz
     lib.cce_vocab_logit_sums.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, vp, sz, vp]
@@ -98,6 +105,8 @@ def load() -> ctypes.CDLL:
     lib.cce_forward_noalloc.restype = ctypes.c_int
     lib.cce_selftest_wait_timeout.argtypes = [vp, ctypes.c_uint32, vp]
     lib.cce_selftest_wait_timeout.restype = ctypes.c_int
+    lib.cce_selftest_pair_timeout.argtypes = [vp, ctypes.c_uint32, ctypes.c_int, vp]
+    lib.cce_selftest_pair_timeout.restype = ctypes.c_int
     lib.cce_memory_accounting.argtypes = [i64, i64, i64, ctypes.POINTER(MemoryReport)]
     lib.cce_memory_accounting.restype = ctypes.c_int
     lib.cce_status_string.argtypes = [ctypes.c_int]

@@ -278,10 +278,14 @@ int fwd_splits(int64_t N, int64_t V) {
   return static_cast<int>(std::min(S, v_tiles));
 }
 
-int64_t bwd_chunk_cols(int64_t N, int64_t V) {
+// Columns of the backward's G-hat chunk [N][vc] bf16 within `budget` bytes
+// (0: the default budget, and at least MIN_CHUNK columns; an explicit budget
+// goes down to one 256-column tile).
+int64_t bwd_chunk_cols(int64_t N, int64_t V, size_t budget = 0) {
   const int64_t vpad = cdiv(V, BN) * BN;
-  int64_t vc = static_cast<int64_t>(G_CHUNK_BUDGET / (2 * static_cast<size_t>(N))) / BN * BN;
-  vc = std::max<int64_t>(MIN_CHUNK, std::min<int64_t>(MAX_CHUNK, vc));
+  const bool dflt = budget == 0;
+  int64_t vc = static_cast<int64_t>((dflt ? G_CHUNK_BUDGET : budget) / (2 * static_cast<size_t>(N))) / BN * BN;
+  vc = std::max<int64_t>(dflt ? MIN_CHUNK : BN, std::min<int64_t>(MAX_CHUNK, vc));
   // At least two chunks whenever V spans more than one tile, so the staging
   // buffer is never an N x V matrix.
   if (V > BN) vc = std::min(vc, cdiv(cdiv(V, 2), BN) * BN);
@@ -360,9 +364,9 @@ struct BwdLayout {
   int64_t vc, bm_ld, n128, nchunks;
 };
 
-BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V, bool sort = false) {
+BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V, bool sort = false, size_t budget = 0) {
   BwdLayout L{};
-  L.vc = bwd_chunk_cols(N, V);
+  L.vc = bwd_chunk_cols(N, V, budget);
   L.bm_ld = cdiv(V, 128);
   L.n128 = cdiv(N, 128);
   L.nchunks = cdiv(V, L.vc);
@@ -656,8 +660,17 @@ size_t cce_backward_workspace_bytes(int64_t N, int64_t D, int64_t V) {
 }
 
 size_t cce_backward_workspace_bytes_ex(int64_t N, int64_t D, int64_t V, int flags) {
+  return cce_backward_workspace_bytes_ex2(N, D, V, flags, 0);
+}
+
+size_t cce_backward_workspace_bytes_ex2(int64_t N, int64_t D, int64_t V, int flags, size_t max_staging_bytes) {
   if (!sizes_ok(N, D, V) || (flags & ~(CCE_FILTER_BOTH | CCE_SORT_VOCAB))) return 0;
-  return bwd_layout(N, D, V, (flags & CCE_SORT_VOCAB) != 0).total;
+  return bwd_layout(N, D, V, (flags & CCE_SORT_VOCAB) != 0, max_staging_bytes).total;
+}
+
+uint64_t cce_backward_chunk_cols(int64_t N, int64_t V, size_t max_staging_bytes) {
+  if (!sizes_ok(N, 8, V)) return 0;
+  return static_cast<uint64_t>(bwd_chunk_cols(N, V, max_staging_bytes));
 }
 
 size_t cce_vocab_sort_workspace_bytes(int64_t N, int64_t D, int64_t V) {
@@ -869,6 +882,14 @@ cce_status cce_backward_ex(const void* E, const void* C, const int64_t* x, const
                            int64_t N, int64_t D, int64_t V, int64_t ignore_index, int reduction, float softcap,
                            float filter_eps, int filter_flags, void* dE, void* dC, void* workspace, size_t ws_bytes,
                            int32_t* dev_err, int64_t* dev_stats, void* stream) {
+  return cce_backward_ex2(E, C, x, lse, grad_out, N, D, V, ignore_index, reduction, softcap, filter_eps, filter_flags,
+                          0, dE, dC, workspace, ws_bytes, dev_err, dev_stats, stream);
+}
+
+cce_status cce_backward_ex2(const void* E, const void* C, const int64_t* x, const float* lse, const float* grad_out,
+                            int64_t N, int64_t D, int64_t V, int64_t ignore_index, int reduction, float softcap,
+                            float filter_eps, int filter_flags, size_t max_staging_bytes, void* dE, void* dC,
+                            void* workspace, size_t ws_bytes, int32_t* dev_err, int64_t* dev_stats, void* stream) {
   if (!E || !C || !x || !lse || !grad_out || !dE || !dC || !workspace) return CCE_ERR_NULL;
   if (!sizes_ok(N, D, V)) return CCE_ERR_SHAPE;
   if (!aligned16(E) || !aligned16(C) || !aligned16(lse) || !aligned16(dE) || !aligned16(dC) ||
@@ -880,7 +901,7 @@ cce_status cce_backward_ex(const void* E, const void* C, const int64_t* x, const
   if (filter_flags & ~(CCE_FILTER_BOTH | CCE_SORT_VOCAB)) return CCE_ERR_ARG;
   if (!(softcap >= 0.0f) || !std::isfinite(softcap)) return CCE_ERR_ARG;
   const bool sort = (filter_flags & CCE_SORT_VOCAB) != 0;
-  const BwdLayout W = bwd_layout(N, D, V, sort);
+  const BwdLayout W = bwd_layout(N, D, V, sort, max_staging_bytes);
   if (ws_bytes < W.total) return CCE_ERR_WORKSPACE;
   int sms = 0, pair_clusters = 0;
   cce_status st = device_check(&sms, &pair_clusters);
@@ -1294,6 +1315,18 @@ cce_status cce_selftest_wait_timeout(int32_t* dev_err, uint32_t timeout_us, void
   cce_status st = device_check(&sms);
   if (st != CCE_OK) return st;
   cudaError_t e = launch_selftest_wait_timeout(dev_err, static_cast<uint64_t>(timeout_us) * 1000u,
+                                               static_cast<cudaStream_t>(stream));
+  g_launches++;
+  return cuda_status(e);
+}
+
+cce_status cce_selftest_pair_timeout(int32_t* dev_err, uint32_t timeout_us, int hold, void* stream) {
+  if (!dev_err) return CCE_ERR_NULL;
+  if (timeout_us == 0 || timeout_us > 10000000u || (hold != 0 && hold != 1)) return CCE_ERR_ARG;
+  int sms = 0;
+  cce_status st = device_check(&sms);
+  if (st != CCE_OK) return st;
+  cudaError_t e = launch_selftest_pair_timeout(dev_err, static_cast<uint64_t>(timeout_us) * 1000u, hold,
                                                static_cast<cudaStream_t>(stream));
   g_launches++;
   return cuda_status(e);

@@ -22,6 +22,8 @@ int gemm_pair_clusters(int sms);
 
 // Launches the bounded-wait self-test kernel (see cce_selftest_wait_timeout).
 cudaError_t launch_selftest_wait_timeout(int32_t* dev_err, uint64_t timeout_ns, cudaStream_t stream);
+// Launches the CTA-pair handshake self-test (see cce_selftest_pair_timeout).
+cudaError_t launch_selftest_pair_timeout(int32_t* dev_err, uint64_t timeout_ns, int hold, cudaStream_t stream);
 
 // Opt the GEMM kernels into their dynamic shared-memory size (once per device).
 cudaError_t prepare_gemm_kernels();

@@ -84,10 +84,41 @@ def assert_forward_close(got, ref, reduction, x, ignore_index=-100):
             assert abs(g - r) <= TOL_LSE * abs(r), f"loss {g!r} vs {r!r}"
 
 
-def assert_grads_close(got, ref_dE, ref_dC, tol, x, ignore_index=-100):
+# Per-row bound beside the Frobenius one: the relative error of every row of
+# dE and dC, with the row's reference norm floored at ROW_FLOOR x the RMS row
+# norm (rows whose reference is nearly zero are judged on that scale).  A
+# single wrong row or ragged tile that the Frobenius figure would dilute
+# fails it; bf16 rounding alone gives about 2e-3 per row.
+TOL_ROW = 5e-2
+ROW_FLOOR = 0.05
+
+
+def row_max_rel(a, b) -> float:
+    """Largest per-row relative error of a against the reference b (2-D)."""
+    a = np.asarray(a, dtype=np.float64).reshape(a.shape[0], -1)
+    b = np.asarray(b, dtype=np.float64).reshape(b.shape[0], -1)
+    den = np.linalg.norm(b, axis=1)
+    rms = float(np.sqrt(np.mean(den * den)))
+    if rms == 0.0:
+        return float(np.abs(a).max()) if a.size else 0.0
+    num = np.linalg.norm(a - b, axis=1)
+    return float(np.max(num / np.maximum(den, ROW_FLOOR * rms)))
+
+
+def assert_grads_close(got, ref_dE, ref_dC, tol, x, ignore_index=-100, row_tol="auto"):
+    """Relative Frobenius error of dE and dC within tol, ignored rows of dE
+    bit-exact +0, and (when the reference takes the same filter decisions
+    as the GPU: row_tol "auto" applies it to unfiltered comparisons, tol <=
+    TOL_GRAD) every row within row_tol."""
     eE, eC = rel_fro(got["dE"], ref_dE), rel_fro(got["dC"], ref_dC)
-    assert eE <= tol, f"dE rel Frobenius err {eE:.3e} > {tol}"
-    assert eC <= tol, f"dC rel Frobenius err {eC:.3e} > {tol}"
+    rE, rC = row_max_rel(got["dE"], ref_dE), row_max_rel(got["dC"], ref_dC)
+    assert eE <= tol, f"dE rel Frobenius err {eE:.3e} > {tol} (worst row {rE:.3e})"
+    assert eC <= tol, f"dC rel Frobenius err {eC:.3e} > {tol} (worst row {rC:.3e})"
+    if row_tol == "auto":
+        row_tol = TOL_ROW if tol <= TOL_GRAD else None
+    if row_tol is not None:
+        assert rE <= row_tol, f"dE worst row rel err {rE:.3e} > {row_tol} (Frobenius {eE:.3e})"
+        assert rC <= row_tol, f"dC worst row rel err {rC:.3e} > {row_tol} (Frobenius {eC:.3e})"
     ign = x == ignore_index
     if np.any(ign):
         raw = got["dE_raw"][torch.from_numpy(np.nonzero(ign)[0]).cuda()]

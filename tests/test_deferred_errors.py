@@ -62,3 +62,43 @@ def test_timeout_word_is_reported_first_and_the_rest_stays_queued():
     with pytest.raises(cce.CCEError) as ei:
         q.poll()
     assert ei.value.status == 8
+
+
+def test_a_full_ring_keeps_the_current_calls_word():
+    """Every slot of the ring is pending and the oldest holds an error: the
+    next call frees that slot, and the older error is reported, but the new
+    call's own word is still recorded and reported after it."""
+    q = cce._DeferredErrors()
+    n = q.SLOTS
+    words = torch.zeros(n, dtype=torch.int32)
+    events = [FakeEvent(False) for _ in range(n)]
+    q._make_ring = lambda device: [words, events, 0]
+
+    def record(word, evs, slot, dev_err):
+        word.copy_(dev_err)
+        evs[slot] = FakeEvent(True)
+        return evs[slot]
+
+    q._record = record
+    dev = torch.zeros(1, dtype=torch.int32)
+    ring = q._make_ring(None)
+    q._rings[dev.device.index] = ring
+    for i in range(n):  # the ring is full; none of the copies has landed yet
+        words[i] = DEVERR_TIMEOUT if i == 0 else 0
+        q._pending.append((words[i:i + 1], events[i], f"call{i}"))
+    bad = torch.tensor([DEVERR_TARGET_RANGE], dtype=torch.int32)
+    reported = []
+    try:
+        q.watch(bad, "new")
+    except cce.CCEError as e:
+        reported.append((e.status, str(e)))
+    assert [e[2] for e in q._pending][-1] == "new"
+    while True:
+        try:
+            q.poll(wait=True)
+            break
+        except cce.CCEError as e:
+            reported.append((e.status, str(e)))
+    assert [r[0] for r in reported] == [9, 8]
+    assert "call0" in reported[0][1] and "new" in reported[1][1]
+    assert q._pending == [] and q._found == []

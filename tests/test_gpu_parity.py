@@ -10,8 +10,9 @@ import torch
 
 import cce_workloads as W
 import oracle as O
-from tests.gpu_util import (TOL_GRAD, TOL_GRAD_FILTERED, TOL_LSE, assert_forward_close, assert_grads_close,
-                            bf16_to_f64, make, oracle_full, rel_fro, run_cuda, to_device)
+from tests.gpu_util import (TOL_GRAD, TOL_GRAD_FILTERED, TOL_LSE, TOL_ROW, assert_forward_close,
+                            assert_grads_close, bf16_to_f64, make, oracle_full, rel_fro, row_max_rel, run_cuda,
+                            to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -107,6 +108,9 @@ def test_filter_matches_filtered_oracle(D):
     assert_grads_close(got, ref["dE"], ref["dC"], TOL_GRAD_FILTERED, x)
     assert rel_fro(got["dE"], ref["dE_f"]) <= TOL_GRAD
     assert rel_fro(got["dC"], ref["dC_f"]) <= TOL_GRAD
+    # the filtered oracle takes the same tile decisions: every row agrees too
+    assert row_max_rel(got["dE"], ref["dE_f"]) <= TOL_ROW
+    assert row_max_rel(got["dC"], ref["dC_f"]) <= TOL_ROW
     keep = ref["keep"]
     st = got["stats"]
     assert st["tiles"] == keep.size
@@ -286,6 +290,8 @@ def test_per_output_filter_flags(outputs, fde, fdc):
                                        filter_dC=fdc, compact_ignored=True)
     assert rel_fro(bf16_to_f64(dE), rE) <= TOL_GRAD
     assert rel_fro(bf16_to_f64(dC), rC) <= TOL_GRAD
+    assert row_max_rel(bf16_to_f64(dE), rE) <= TOL_ROW
+    assert row_max_rel(bf16_to_f64(dC), rC) <= TOL_ROW
     assert st["skipped"] == int((~keep).sum()) > 0
 
 
@@ -328,6 +334,7 @@ def test_mostly_ignored_batch_is_compacted():
         assert_grads_close(got, ref["dE"], ref["dC"], TOL_GRAD if eps == 0 else TOL_GRAD_FILTERED, x)
         if eps:
             assert rel_fro(got["dE"], ref["dE_f"]) <= TOL_GRAD
+            assert row_max_rel(got["dE"], ref["dE_f"]) <= TOL_ROW
             assert got["stats"]["tiles"] == ref["keep"].size
 
 
@@ -361,3 +368,85 @@ def test_forward_skipping_ignored_rows(reduction, ignore_frac):
         assert abs(loss.item() - float(ref["loss"])) <= TOL_LSE * abs(float(ref["loss"]))
     got = {"dE": bf16_to_f64(dE), "dC": bf16_to_f64(dC), "dE_raw": dE}
     assert_grads_close(got, ref["dE"], ref["dC"], TOL_GRAD, x)
+
+
+@pytest.mark.parametrize("targets", ["uniform", "concentrated"])
+def test_filter_threshold_tie(targets):
+    """The filter at its tie: C = 0 and V = 4096 make every logit 0, so every
+    non-target probability is exactly 1/4096 = 2^-12 = eps ("Cut Cross-Entropy:
+    Training Loss Without the Logit Matrix ...", "Gradient filtering: the part
+    that makes it fast": eps = finfo(bf16).eps / 32 and at most 4096 entries
+    per row reach it).  The pages skip a tile when every |G| < eps, so ties
+    survive; a tile whose max |G| lies within 1e-6 relative of eps may flip
+    between the GPU's fp32 and the oracle's fp64, so the GPU's skip count must
+    lie between the oracle's counts at eps (1 - 1e-6) and eps (1 + 1e-6).
+    Every row has the same logits, so the GPU decides every tie the same way:
+    its gradients must match the filtered oracle of that decision, and, when
+    it keeps the ties (the pages' reading), the unfiltered oracle.
+    "uniform": targets spread over the vocabulary (few tiles are decided by
+    the tie alone); "concentrated": targets in the first 256 ids, so 30 of
+    the 32 vocabulary tiles of every token block are decided by the tie."""
+    N, D, V = 512, 64, 4096
+    rng = np.random.default_rng(11)
+    E_bits = W.f32_to_bf16_bits(rng.standard_normal((N, D)).astype(np.float32))
+    C_bits = np.zeros((V, D), dtype=np.uint16)
+    hi = V if targets == "uniform" else 256
+    x = rng.integers(0, hi, size=N).astype(np.int64)
+    got = run_cuda(E_bits, C_bits, x, reduction="mean", filter_eps=O.FILTER_EPS)
+    Ef, Cf = O.from_bits(E_bits, C_bits)
+    f = O.forward(Ef, Cf, x, reduction="mean")
+    assert np.all(f["lse"] == 12.0 * np.log(2.0))  # log V exactly
+    lse_err = np.abs(got["lse"] - f["lse"]) / f["lse"]
+    assert lse_err.max() <= TOL_LSE
+    assert abs(float(got["loss"].reshape(())) - float(f["loss"])) <= TOL_LSE * float(f["loss"])
+    wts = O.row_weights(x, O.IGNORE_INDEX, "mean", 1.0, f["count"])
+    dE_u, dC_u = O.backward(Ef, Cf, x, f["lse"], wts)
+    assert np.all(dE_u == 0.0)  # C = 0
+    refs = {}
+    for side, eps in (("keep_ties", O.FILTER_EPS * (1 - 1e-6)), ("skip_ties", O.FILTER_EPS * (1 + 1e-6))):
+        dEf, dCf, keep = O.backward_filtered(Ef, Cf, x, f["lse"], wts, 128, 128, eps, compact_ignored=True)
+        refs[side] = (dCf, int((~keep).sum()), keep.size)
+    lo, hi_ = refs["keep_ties"][1], refs["skip_ties"][1]
+    assert lo == 0 and hi_ > 0
+    st = got["stats"]
+    assert st["tiles"] == refs["keep_ties"][2]
+    assert lo <= st["skipped"] <= hi_, (st, lo, hi_)
+    assert st["skipped"] in (lo, hi_), "every tie is decided the same way"
+    # dE = G C is exactly zero whatever the filter keeps
+    assert np.all(got["dE"] == 0.0)
+    side = "keep_ties" if st["skipped"] == lo else "skip_ties"
+    dC_ref = refs[side][0]
+    assert rel_fro(got["dC"], dC_ref) <= TOL_GRAD
+    assert row_max_rel(got["dC"], dC_ref) <= TOL_ROW
+    if side == "keep_ties":
+        assert rel_fro(got["dC"], dC_u) <= TOL_GRAD_FILTERED
+    elif targets == "uniform":
+        # few tiles are decided by the tie alone: within the filtered bar either way
+        assert rel_fro(got["dC"], dC_u) <= TOL_GRAD_FILTERED
+
+
+@pytest.mark.parametrize("cols,sort", [(256, False), (512, False), (256, True), (None, False)])
+def test_staging_budget(cols, sort):
+    """cce_backward_ex2: the G-hat chunk buffer bounded by max_staging_bytes.
+    Budgets of one and two 256-column tiles per chunk (36 and 18 chunks at
+    V = 9000, the last one ragged) give the oracle's gradients like the
+    default budget does, with and without vocabulary sorting; the chunk width
+    follows the budget."""
+    import linear_cross_entropy_gb300 as cce
+    N, D, V = 640, 128, 9000
+    budget = 0 if cols is None else N * cols * 2 + 100
+    assert cce.backward_chunk_cols(N, V, budget) == (cols or 4608)
+    w, (E, C, x) = make(W.small("b", N, D, V))
+    Et, Ct, xt = to_device(E, C, x)
+    loss, lse = cce.cce_forward(Et, Ct, xt)
+    need = cce.backward_workspace_bytes(N, D, V, vocab_sort=sort, max_staging_bytes=budget)
+    assert need <= cce.backward_workspace_bytes(N, D, V, vocab_sort=sort)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    for eps in (0.0, O.FILTER_EPS):
+        dE, dC, st = cce.cce_backward(Et, Ct, xt, lse, torch.ones(1, device="cuda"), filter_eps=eps,
+                                      vocab_sort=sort, max_staging_bytes=budget, workspace=ws, stats=True)
+        torch.cuda.synchronize()
+        ref = oracle_full(E, C, x, reduction="mean")
+        got = {"dE": bf16_to_f64(dE), "dC": bf16_to_f64(dC), "dE_raw": dE}
+        assert_grads_close(got, ref["dE"], ref["dC"], TOL_GRAD if eps == 0 else TOL_GRAD_FILTERED, x)
+        assert st["tiles"] == ((x != -100).sum() + 127) // 128 * ((V + 127) // 128)

@@ -15,6 +15,7 @@ import pytest
 import torch
 
 import cce_workloads as W
+import oracle as O
 
 pytestmark = pytest.mark.gpu
 
@@ -62,6 +63,16 @@ def test_noalloc_forward_matches_forward_on_two_calls_in_a_row(lib):
             assert bool(((loss.double() - ref_loss.double()).abs() <= bound).all())
         else:
             assert abs(loss.item() - ref_loss.item()) <= TOL_LSE * abs(ref_loss.item())
+        # and against the fp64 oracle directly
+        E_bits, C_bits, xh = W.make_inputs(w)
+        Ef, Cf = O.from_bits(E_bits, C_bits)
+        f = O.forward(Ef, Cf, xh, reduction=reduction)
+        got_lse = lse.double().cpu().numpy()
+        assert np.max(np.abs(got_lse - f["lse"]) / np.abs(f["lse"])) <= TOL_LSE
+        if reduction == "none":
+            assert np.all(np.abs(loss.double().cpu().numpy() - f["loss_rows"]) <= TOL_LSE * np.abs(f["lse"]))
+        else:
+            assert abs(loss.item() - f["loss"]) <= TOL_LSE * abs(f["loss"])
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(lib):
