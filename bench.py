@@ -458,13 +458,17 @@ def run_e2e(case, steps, stream):
     return out
 
 
-def per_config_cases(headline, headline_filter):
-    """Every (workload, filter mode) of the five workloads except the headline."""
+def per_config_cases(headline, headline_filter, headline_single):
+    """(workload, filter mode, single call) of every workload and filter mode
+    except the headline, in the headline's mode; with a two-call headline, also
+    the single call on the long-context batch."""
     out = []
     for name in W.CONFIG_ORDER:
         for f in W.CONFIGS[name].filter_modes:
             if (name, f) != (headline, headline_filter):
-                out.append((name, f))
+                out.append((name, f, headline_single))
+    if not headline_single:
+        out.append(("long", "on", True))
     return out
 
 
@@ -575,10 +579,12 @@ def run_gpu(args, rank, world, local_rank):
 
     if not args.quick and rank == 0:
         table = []
-        for name, fmode in per_config_cases(args.config, args.filter):
-            c = Case(cce, torch, dev, name, fmode, False, False, single and W.CONFIGS[name].reduction != "none",
+        for name, fmode, sgl in per_config_cases(args.config, args.filter, single):
+            c = Case(cce, torch, dev, name, fmode, False, False, sgl and W.CONFIGS[name].reduction != "none",
                      budget, inputs=keep_inputs if name == args.config else None)
-            table.append(measure_case(c, min(args.steps, 20), 3, stream, peaks, gpu_id))
+            r = measure_case(c, min(args.steps, 20), 3, stream, peaks, gpu_id)
+            r["mode"] = "single call (cce_loss_and_grad)" if c.single else "two calls (cce_forward + cce_backward)"
+            table.append(r)
             del c
             torch.cuda.empty_cache()
         out["per_config"] = table

@@ -260,7 +260,11 @@ class LinearCrossEntropyFunction(torch.autograd.Function):
     def forward(ctx, E, C, x, ignore_index, reduction, filter_eps, filter_outputs, softcap, vocab_sort,
                 max_staging_bytes):
         err = torch.zeros(1, dtype=torch.int32, device=E.device)
-        loss, lse = cce_forward(E, C, x, ignore_index, reduction, softcap=softcap, check_errors=False, dev_err=err)
+        # The LSE is kept only for the backward, which reads it on the rows
+        # that take part; so the forward GEMM skips the other rows
+        # (CCE_FWD_SKIP_IGNORED: same loss, per-row loss 0 where ignored).
+        loss, lse = cce_forward(E, C, x, ignore_index, reduction, softcap=softcap, skip_ignored=True,
+                                check_errors=False, dev_err=err)
         _deferred.watch(err, "cce_forward")
         ctx.save_for_backward(E, C, x, lse)
         ctx.cfg = (ignore_index, reduction, filter_eps, filter_outputs, softcap, vocab_sort, max_staging_bytes)

@@ -131,6 +131,16 @@ def test_fully_ignored_batch():
     assert float(got["loss"].reshape(())) == 0.0
     assert np.all(got["dE"] == 0.0) and np.all(got["dC"] == 0.0)
     assert np.all(np.isfinite(got["lse"]))
+    # the autograd path (its forward skips the rows that take part in nothing: all of them here)
+    import linear_cross_entropy_gb300 as cce
+    Et, Ct, xt = to_device(E, C, x)
+    Et.requires_grad_(True)
+    Ct.requires_grad_(True)
+    loss = cce.linear_cross_entropy(Et, Ct, xt)
+    loss.backward()
+    cce.raise_pending_errors()
+    assert loss.item() == 0.0
+    assert not Et.grad.any() and not Ct.grad.any()
 
 
 def test_custom_ignore_index():
