@@ -460,3 +460,61 @@ def test_staging_budget(cols, sort):
         got = {"dE": bf16_to_f64(dE), "dC": bf16_to_f64(dC), "dE_raw": dE}
         assert_grads_close(got, ref["dE"], ref["dC"], TOL_GRAD if eps == 0 else TOL_GRAD_FILTERED, x)
         assert st["tiles"] == ((x != -100).sum() + 127) // 128 * ((V + 127) // 128)
+
+
+@pytest.mark.parametrize("D", [8, 16, 24, 40, 72])
+def test_small_hidden_sizes(D):
+    """Hidden sizes below one 64-column K-block: the logit GEMMs' K box and
+    the gradient GEMM's D tile (32 columns wide here, 64 at D = 72) reach past
+    D and read zeros there; stores of D tiles stop at D.  Ragged N and V,
+    ignored rows, filter off and on, and the single call."""
+    import linear_cross_entropy_gb300 as cce
+    N, V = 300, 700
+    w, (E, C, x) = make(W.small("sd", N, D, V))
+    for eps in (0.0, O.FILTER_EPS):
+        got = run_cuda(E, C, x, reduction="mean", filter_eps=eps)
+        ref = oracle_full(E, C, x, reduction="mean", filter_eps=eps or None)
+        assert_forward_close(got, ref, "mean", x)
+        assert_grads_close(got, ref["dE"], ref["dC"], TOL_GRAD if eps == 0 else TOL_GRAD_FILTERED, x)
+        if eps:
+            assert rel_fro(got["dE"], ref["dE_f"]) <= TOL_GRAD and rel_fro(got["dC"], ref["dC_f"]) <= TOL_GRAD
+    Et, Ct, xt = to_device(E, C, x)
+    loss, _, dE, dC = cce.cce_loss_and_grad(Et, Ct, xt, filter_eps=0.0)
+    ref = oracle_full(E, C, x, reduction="mean")
+    assert abs(loss.item() - float(ref["loss"])) <= TOL_LSE * abs(float(ref["loss"]))
+    got = {"dE": bf16_to_f64(dE), "dC": bf16_to_f64(dC), "dE_raw": dE}
+    assert_grads_close(got, ref["dE"], ref["dC"], TOL_GRAD, x)
+
+
+@pytest.mark.parametrize("filter_on", [False, True])
+def test_single_entry_vocabulary(filter_on):
+    """V = 1: every row's only logit is its target logit, so LSE_i = a_i,
+    every loss is 0 and G = softmax - onehot = 0 in exact arithmetic.  The
+    GPU's fp32 LSE (a max and a log-sum in base 2) may differ from a_i in the
+    last bits, so the loss and the gradients must be 0 up to 1e-5 of the LSE
+    scale; with the filter on every |G| < eps and the gradients are exact
+    zeros."""
+    N, D, V = 200, 64, 1
+    rng = np.random.default_rng(5)
+    E_bits = W.f32_to_bf16_bits(rng.standard_normal((N, D)).astype(np.float32))
+    C_bits = W.f32_to_bf16_bits(rng.standard_normal((V, D)).astype(np.float32))
+    x = np.zeros(N, dtype=np.int64)
+    x[::7] = O.IGNORE_INDEX
+    eps = O.FILTER_EPS if filter_on else 0.0
+    for reduction in ("mean", "none"):
+        got = run_cuda(E_bits, C_bits, x, reduction=reduction, filter_eps=eps)
+        Ef, Cf = O.from_bits(E_bits, C_bits)
+        f = O.forward(Ef, Cf, x, reduction=reduction)
+        scale = float(np.abs(f["lse"]).max())
+        assert np.max(np.abs(got["lse"] - f["lse"])) <= TOL_LSE * scale
+        assert np.max(np.abs(got["loss"])) <= TOL_LSE * scale
+        if filter_on:
+            assert np.all(got["dE"] == 0.0) and np.all(got["dC"] == 0.0)
+            assert got["stats"]["skipped"] == got["stats"]["tiles"]
+        else:
+            gscale = np.abs(Ef).max() * np.abs(Cf).max()
+            assert np.max(np.abs(got["dE"])) <= TOL_LSE * gscale
+            assert np.max(np.abs(got["dC"])) <= TOL_LSE * gscale * N
+        ign = x == O.IGNORE_INDEX
+        raw = got["dE_raw"][torch.from_numpy(np.nonzero(ign)[0]).cuda()]
+        assert not raw.view(torch.int16).any()
