@@ -7,7 +7,10 @@
 One step = cce_forward + cce_backward (every stage of the path: LSE GEMM with
 target capture, combine + reduction, target count, recompute + G + filter,
 dC GEMM, dE GEMM, dE finalise) over one batch of the seeded synthetic
-workload, inputs resident in HBM.  --mode single times the single call
+workload, inputs resident in HBM.  The forward first compacts away the rows
+whose target is ignore_index (CCE_FWD_SKIP_IGNORED, "Cut Your Losses ...",
+Table A1): the loss and the gradients are unchanged and only those rows' LSE
+reads 0; --all-rows-forward computes every row's LSE.  --mode single times the single call
 instead (cce_loss_and_grad: staged logits, no recompute).  Prints one JSON
 line (rank 0): the headline workload (default: the long-context batch,
 65,536 x 2,048 x 128,256, the largest that the workloads define) with its
@@ -458,17 +461,19 @@ def run_e2e(case, steps, stream):
     return out
 
 
-def per_config_cases(headline, headline_filter, headline_single):
-    """(workload, filter mode, single call) of every workload and filter mode
-    except the headline, in the headline's mode; with a two-call headline, also
-    the single call on the long-context batch."""
+def per_config_cases(headline, headline_filter, headline_single, headline_skip=True):
+    """(workload, filter mode, single call, forward skips ignored rows) of
+    every workload and filter mode except the headline, in the headline's
+    mode; with a two-call headline, also the single call on the long-context
+    batch and that batch with the forward over every row."""
     out = []
     for name in W.CONFIG_ORDER:
         for f in W.CONFIGS[name].filter_modes:
             if (name, f) != (headline, headline_filter):
-                out.append((name, f, headline_single))
+                out.append((name, f, headline_single, headline_skip))
     if not headline_single:
-        out.append(("long", "on", True))
+        out.append(("long", "on", True, True))
+        out.append(("long", "on", False, not headline_skip))
     return out
 
 
@@ -574,16 +579,18 @@ def run_gpu(args, rank, world, local_rank):
     }
     inputs = (case.w, case.E_bits, case.C_bits, case.x)
     keep_inputs = (case.E_bits, case.C_bits, case.x)
+    case_skip = case.skip
     del case
     torch.cuda.empty_cache()
 
     if not args.quick and rank == 0:
         table = []
-        for name, fmode, sgl in per_config_cases(args.config, args.filter, single):
-            c = Case(cce, torch, dev, name, fmode, False, False, sgl and W.CONFIGS[name].reduction != "none",
+        for name, fmode, sgl, skp in per_config_cases(args.config, args.filter, single, case_skip):
+            c = Case(cce, torch, dev, name, fmode, False, skp, sgl and W.CONFIGS[name].reduction != "none",
                      budget, inputs=keep_inputs if name == args.config else None)
             r = measure_case(c, min(args.steps, 20), 3, stream, peaks, gpu_id)
             r["mode"] = "single call (cce_loss_and_grad)" if c.single else "two calls (cce_forward + cce_backward)"
+            r["forward_skips_ignored_rows"] = bool(c.skip or c.single)
             table.append(r)
             del c
             torch.cuda.empty_cache()
@@ -642,8 +649,9 @@ def main(argv=None):
     ap.add_argument("--filter", choices=("on", "off"), default=None)
     ap.add_argument("--vocab-sort", action="store_true",
                     help="filter over the vocabulary sorted by average logit")
-    ap.add_argument("--skip-ignored", action="store_true",
-                    help="two-call mode: the forward skips the rows that take part in no loss")
+    ap.add_argument("--all-rows-forward", action="store_true",
+                    help="two-call mode: the forward computes the LSE of every row, ignored rows too (default: "
+                         "it compacts away the rows that take part in no loss first, CCE_FWD_SKIP_IGNORED)")
     ap.add_argument("--mode", choices=("two-call", "single"), default="two-call",
                     help="two-call: cce_forward + cce_backward; single: cce_loss_and_grad")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -653,6 +661,7 @@ def main(argv=None):
     ap.add_argument("--g-budget-mib", type=int, default=0,
                     help="two-call mode: bound of the backward's G-hat chunk buffer in MiB (0: the default)")
     args = ap.parse_args(argv)
+    args.skip_ignored = not args.all_rows_forward
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.filter is None:

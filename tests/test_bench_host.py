@@ -80,3 +80,16 @@ def test_reference_arm_other_ranks_exit_without_work(monkeypatch):
 def test_warmup_must_be_three_or_more():
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "2"])
+
+
+def test_per_config_covers_every_workload_and_filter_mode():
+    """The default run reports every workload and filter mode besides the
+    headline, plus the single call and the all-rows forward on the
+    long-context batch."""
+    import cce_workloads as W
+    cases = bench.per_config_cases("long", "on", False, True)
+    want = {(n, f) for n in W.CONFIG_ORDER for f in W.CONFIGS[n].filter_modes} - {("long", "on")}
+    assert {(n, f) for n, f, sgl, skp in cases if not sgl and skp} == want
+    assert ("long", "on", True, True) in cases
+    assert ("long", "on", False, False) in cases
+    assert len(cases) == len(want) + 2
