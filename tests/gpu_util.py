@@ -86,7 +86,7 @@ def assert_forward_close(got, ref, reduction, x, ignore_index=-100):
 
 # Per-row bound beside the Frobenius one: the relative error of every row of
 # dE and dC, with the row's reference norm floored at ROW_FLOOR x the RMS row
-# norm (rows whose reference is nearly zero are judged on that scale).  A
+# norm (rows whose reference is nearly zero are measured on that scale).  A
 # single wrong row or ragged tile that the Frobenius figure would dilute
 # fails it; bf16 rounding alone gives about 2e-3 per row.
 TOL_ROW = 5e-2
