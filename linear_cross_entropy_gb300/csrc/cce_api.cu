@@ -114,61 +114,118 @@ __global__ void finish_loss_kernel(const double* __restrict__ blk_sum, const int
   }
 }
 
-// One block: order-preserving compaction of the rows that take part in the
-// backward (non-ignored, in-range target).  pos[r] = compact index or -1;
-// ridx[k] = original row; *count = number of such rows (the mean's divisor).
-// Out-of-range targets are flagged and dropped like ignored rows.
+// Order-preserving compaction of the rows that take part in the backward
+// (non-ignored, in-range target): pos[r] = compact index or -1; ridx[k] =
+// original row; *count = number of such rows (the mean's divisor).
+// Out-of-range targets are flagged and dropped like ignored rows.  Three
+// launches over tiles of COMPACT_THREADS consecutive rows, one row per thread:
+// per-tile counts, one block's exclusive scan of them, then each tile ranks
+// its rows by warp ballots and a scan of the warp counts from its tile offset.
 constexpr int COMPACT_THREADS = 1024;
 
-__global__ void compact_kernel(const int64_t* __restrict__ x, int N, int V, long long ignore_index,
-                               int* __restrict__ pos, int* __restrict__ ridx, int* count, int32_t* dev_err) {
-  // Tiles of COMPACT_THREADS consecutive rows, one row per thread (coalesced
-  // loads and stores), in order; a tile's ranks come from warp ballots and a
-  // scan of the 32 warp counts, offset by the rows taken in earlier tiles.
+__device__ __forceinline__ bool takes_part(const int64_t* __restrict__ x, int r, int N, int V,
+                                           long long ignore_index, bool* bad) {
+  if (r >= N) return false;
+  const long long xi = static_cast<long long>(x[r]);
+  if (xi == ignore_index) return false;
+  if (xi < 0 || xi >= V) {
+    *bad = true;
+    return false;
+  }
+  return true;
+}
+
+__global__ void compact_count_kernel(const int64_t* __restrict__ x, int N, int V, long long ignore_index,
+                                     int* __restrict__ tile_cnt, int32_t* dev_err) {
+  bool bad = false;
+  const int r = blockIdx.x * COMPACT_THREADS + static_cast<int>(threadIdx.x);
+  const int c = __syncthreads_count(takes_part(x, r, N, V, ignore_index, &bad));
+  if (threadIdx.x == 0) tile_cnt[blockIdx.x] = c;
+  if (bad && dev_err) atomicOr(reinterpret_cast<int*>(dev_err), CCE_DEVERR_TARGET_RANGE);
+}
+
+__global__ void compact_scan_kernel(const int* __restrict__ tile_cnt, int ntiles, int* __restrict__ tile_off,
+                                    int* count) {
   static_assert(COMPACT_THREADS == 32 * 32, "one scan lane per warp");
   __shared__ int warp_off[32];
-  __shared__ int tile_total;
+  __shared__ int chunk_total;
   const int t = static_cast<int>(threadIdx.x), lane = t & 31, w = t >> 5;
-  int base = 0;
-  bool bad = false;
-  for (int r0 = 0; r0 < N; r0 += COMPACT_THREADS) {
-    const int r = r0 + t;
-    bool take = false;
-    if (r < N) {
-      const long long xi = static_cast<long long>(x[r]);
-      if (xi != ignore_index) {
-        if (xi < 0 || xi >= V) {
-          bad = true;
-        } else {
-          take = true;
-        }
-      }
+  int carry = 0;
+  for (int b0 = 0; b0 < ntiles; b0 += COMPACT_THREADS) {
+    const int b = b0 + t;
+    const int v = b < ntiles ? tile_cnt[b] : 0;
+    int inc = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, inc, off);
+      if (lane >= off) inc += u;
     }
-    const unsigned m = __ballot_sync(0xffffffffu, take);
-    if (lane == 0) warp_off[w] = __popc(m);
+    if (lane == 31) warp_off[w] = inc;
     __syncthreads();
-    if (w == 0) {  // exclusive scan of the warp counts
-      const int v = warp_off[lane];
-      int inc = v;
+    if (w == 0) {
+      const int ws = warp_off[lane];
+      int winc = ws;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, inc, off);
-        if (lane >= off) inc += n;
+        const int u = __shfl_up_sync(0xffffffffu, winc, off);
+        if (lane >= off) winc += u;
       }
-      warp_off[lane] = inc - v;
-      if (lane == 31) tile_total = inc;
+      warp_off[lane] = winc - ws;
+      if (lane == 31) chunk_total = winc;
     }
     __syncthreads();
-    if (r < N) {
-      const int k = base + warp_off[w] + __popc(m & ((1u << lane) - 1u));
-      pos[r] = take ? k : -1;
-      if (take) ridx[k] = r;
-    }
-    base += tile_total;
-    __syncthreads();  // warp_off and tile_total are rewritten by the next tile
+    if (b < ntiles) tile_off[b] = carry + warp_off[w] + inc - v;
+    carry += chunk_total;
+    __syncthreads();  // warp_off and chunk_total are rewritten by the next chunk
   }
-  if (__syncthreads_or(bad) && t == 0 && dev_err) atomicOr(reinterpret_cast<int*>(dev_err), CCE_DEVERR_TARGET_RANGE);
-  if (t == 0) *count = base;
+  if (t == 0) *count = carry;
+}
+
+__global__ void compact_scatter_kernel(const int64_t* __restrict__ x, int N, int V, long long ignore_index,
+                                       const int* __restrict__ tile_off, int* __restrict__ pos,
+                                       int* __restrict__ ridx) {
+  __shared__ int warp_off[32];
+  const int t = static_cast<int>(threadIdx.x), lane = t & 31, w = t >> 5;
+  const int r = blockIdx.x * COMPACT_THREADS + t;
+  bool bad = false;
+  const bool take = takes_part(x, r, N, V, ignore_index, &bad);
+  const unsigned m = __ballot_sync(0xffffffffu, take);
+  if (lane == 0) warp_off[w] = __popc(m);
+  __syncthreads();
+  if (w == 0) {  // exclusive scan of the warp counts
+    const int v = warp_off[lane];
+    int inc = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, inc, off);
+      if (lane >= off) inc += u;
+    }
+    warp_off[lane] = inc - v;
+  }
+  __syncthreads();
+  if (r < N) {
+    const int k = tile_off[blockIdx.x] + warp_off[w] + __popc(m & ((1u << lane) - 1u));
+    pos[r] = take ? k : -1;
+    if (take) ridx[k] = r;
+  }
+}
+
+int compact_tiles(int64_t N) { return static_cast<int>((N + COMPACT_THREADS - 1) / COMPACT_THREADS); }
+
+// Scratch of the compaction: per-tile counts and offsets.
+size_t compact_scratch_bytes(int64_t N) { return sizeof(int) * 2 * static_cast<size_t>(compact_tiles(N)); }
+
+cudaError_t launch_compact(const int64_t* x, int64_t N, int64_t V, long long ignore_index, int* pos, int* ridx,
+                           int* count, int* scratch, int32_t* dev_err, cudaStream_t s) {
+  const int nt = compact_tiles(N);
+  int* cnt = scratch;
+  int* off = scratch + nt;
+  compact_count_kernel<<<nt, COMPACT_THREADS, 0, s>>>(x, static_cast<int>(N), static_cast<int>(V), ignore_index,
+                                                       cnt, dev_err);
+  compact_scan_kernel<<<1, COMPACT_THREADS, 0, s>>>(cnt, nt, off, count);
+  compact_scatter_kernel<<<nt, COMPACT_THREADS, 0, s>>>(x, static_cast<int>(N), static_cast<int>(V),
+                                                         ignore_index, off, pos, ridx);
+  return cudaGetLastError();
 }
 
 // Compact copies of the rows that take part: E_c [k] = E[ridx[k]] and the
@@ -314,8 +371,8 @@ int grad_tile_width(int64_t D, int step) {
 
 struct FwdLayout {
   size_t counter, part_m, part_s, tgt, blk_sum, blk_cnt, total;
-  // CCE_FWD_SKIP_IGNORED only: compaction map, compact rows and results
-  size_t pos, ridx, count, xc, ec, lsec, lossc;
+  // CCE_FWD_SKIP_IGNORED only: compaction map and scratch, compact rows and results
+  size_t pos, ridx, count, cscr, xc, ec, lsec, lossc;
   int S, nblk;
 };
 
@@ -343,6 +400,8 @@ FwdLayout fwd_layout(int64_t N, int64_t V, int64_t D = 0, bool compact = false) 
     o = align_up(o + sizeof(int) * static_cast<size_t>(N), ALIGN);
     L.count = o;
     o = align_up(o + sizeof(int), ALIGN);
+    L.cscr = o;
+    o = align_up(o + compact_scratch_bytes(N), ALIGN);
     L.xc = o;
     o = align_up(o + sizeof(int64_t) * static_cast<size_t>(N), ALIGN);
     L.ec = o;
@@ -357,7 +416,7 @@ FwdLayout fwd_layout(int64_t N, int64_t V, int64_t D = 0, bool compact = false) 
 }
 
 struct BwdLayout {
-  size_t count, counters, pos, ridx, xc, lsec, gc, ec, bitmap, bitmapT, gbuf, deacc, total;
+  size_t count, counters, cscr, pos, ridx, xc, lsec, gc, ec, bitmap, bitmapT, gbuf, deacc, total;
   // vocabulary sorting only: sort keys, order and its inverse, scratch, and
   // the chunk of C in sorted order
   size_t keys, perm, inv, sortscr, cs;
@@ -375,6 +434,8 @@ BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V, bool sort = false, size_t 
   o = align_up(o + sizeof(int), ALIGN);
   L.counters = o;  // two scheduler counters per chunk
   o = align_up(o + sizeof(int) * 2 * static_cast<size_t>(L.nchunks), ALIGN);
+  L.cscr = o;  // compaction scratch
+  o = align_up(o + compact_scratch_bytes(N), ALIGN);
   L.pos = o;  // compaction map and compact copies of the rows that take part
   o = align_up(o + sizeof(int) * static_cast<size_t>(N), ALIGN);
   L.ridx = o;
@@ -420,7 +481,7 @@ BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V, bool sort = false, size_t 
 constexpr size_t FLCE_STAGING_DEFAULT = size_t(2) << 30;
 
 struct FlceLayout {
-  size_t counters, count, pos, ridx, xc, ec, part_m, part_s, tgt, lse, blk_sum, blk_cnt, stage, mtile, bitmap,
+  size_t counters, count, cscr, pos, ridx, xc, ec, part_m, part_s, tgt, lse, blk_sum, blk_cnt, stage, mtile, bitmap,
       bitmapT, deacc, dcacc, total;
   int64_t Nc, nchunks, Vp, bm_ld, slab, n_tiles, bn, kps;
   int S, Sde, nblk;
@@ -455,6 +516,7 @@ FlceLayout flce_layout(int64_t N, int64_t D, int64_t V, size_t max_staging) {
   };
   L.counters = take(sizeof(int) * 2 * static_cast<size_t>(L.nchunks));
   L.count = take(sizeof(int));
+  L.cscr = take(compact_scratch_bytes(N));
   L.pos = take(sizeof(int) * static_cast<size_t>(N));
   L.ridx = take(sizeof(int) * static_cast<size_t>(N));
   L.xc = take(sizeof(int64_t) * static_cast<size_t>(N));
@@ -768,9 +830,12 @@ static cce_status forward_impl(const void* E, const void* C, const int64_t* x, i
     int* ridx = reinterpret_cast<int*>(ws + W.ridx);
     int64_t* xc = reinterpret_cast<int64_t*>(ws + W.xc);
     void* Ec = ws + W.ec;
-    compact_kernel<<<1, COMPACT_THREADS, 0, s>>>(x, static_cast<int>(N), static_cast<int>(V),
-                                                 static_cast<long long>(ignore_index), pos, ridx, count, dev_err);
-    g_launches++;
+    {
+      cudaError_t ce = launch_compact(x, N, V, static_cast<long long>(ignore_index), pos, ridx, count,
+                                      reinterpret_cast<int*>(ws + W.cscr), dev_err, s);
+      g_launches += 3;
+      if (ce != cudaSuccess) return cuda_status(ce);
+    }
     const int rows_per_block = 8;
     const int blocks = static_cast<int>(std::min<int64_t>(int64_t(sms) * 16, cdiv(N, rows_per_block)));
     gather_rows_kernel<<<std::max(blocks, 1), 32 * rows_per_block, 0, s>>>(
@@ -923,9 +988,12 @@ cce_status cce_backward_ex2(const void* E, const void* C, const int64_t* x, cons
   void* Ec = ws + W.ec;
   {
     PhaseScope ps(2, s);
-    compact_kernel<<<1, COMPACT_THREADS, 0, s>>>(x, static_cast<int>(N), static_cast<int>(V),
-                                                 static_cast<long long>(ignore_index), pos, ridx, count, dev_err);
-    g_launches++;
+    {
+      cudaError_t ce = launch_compact(x, N, V, static_cast<long long>(ignore_index), pos, ridx, count,
+                                      reinterpret_cast<int*>(ws + W.cscr), dev_err, s);
+      g_launches += 3;
+      if (ce != cudaSuccess) return cuda_status(ce);
+    }
     const int rows_per_block = 8;
     const int blocks = static_cast<int>(std::min<int64_t>(int64_t(sms) * 16, cdiv(N, rows_per_block)));
     gather_rows_kernel<<<std::max(blocks, 1), 32 * rows_per_block, 0, s>>>(
@@ -1130,9 +1198,12 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
     cudaError_t e = cudaMemsetAsync(counters, 0, sizeof(int) * 2 * static_cast<size_t>(W.nchunks), s);
     if (e == cudaSuccess && dev_stats) e = cudaMemsetAsync(dev_stats, 0, 2 * sizeof(int64_t), s);
     if (e != cudaSuccess) return cuda_status(e);
-    compact_kernel<<<1, COMPACT_THREADS, 0, s>>>(x, static_cast<int>(N), static_cast<int>(V),
-                                                 static_cast<long long>(ignore_index), pos, ridx, count, dev_err);
-    g_launches++;
+    {
+      cudaError_t ce = launch_compact(x, N, V, static_cast<long long>(ignore_index), pos, ridx, count,
+                                      reinterpret_cast<int*>(ws + W.cscr), dev_err, s);
+      g_launches += 3;
+      if (ce != cudaSuccess) return cuda_status(ce);
+    }
     const int rows_per_block = 8;
     const int blocks = static_cast<int>(std::min<int64_t>(int64_t(sms) * 16, cdiv(N, rows_per_block)));
     gather_rows_kernel<<<std::max(blocks, 1), 32 * rows_per_block, 0, s>>>(
