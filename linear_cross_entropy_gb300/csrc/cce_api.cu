@@ -30,6 +30,7 @@ constexpr size_t ALIGN = 256;         // sub-buffer alignment inside a workspace
 constexpr size_t G_CHUNK_BUDGET = size_t(CCE_G_CHUNK_BUDGET_MIB) << 20;  // bytes of the backward G chunk buffer
 constexpr int64_t MIN_CHUNK = 2048, MAX_CHUNK = 65536;
 constexpr int COMBINE_THREADS = 256;
+constexpr size_t ZERO_BOX_BYTES = size_t(BM) * BK * 2;  // one A operand box
 
 std::atomic<uint64_t> g_launches{0};
 
@@ -416,7 +417,7 @@ FwdLayout fwd_layout(int64_t N, int64_t V, int64_t D = 0, bool compact = false) 
 }
 
 struct BwdLayout {
-  size_t count, counters, cscr, pos, ridx, xc, lsec, gc, ec, bitmap, bitmapT, gbuf, deacc, total;
+  size_t count, counters, zero, cscr, pos, ridx, xc, lsec, gc, ec, bitmap, bitmapT, gbuf, deacc, total;
   // vocabulary sorting only: sort keys, order and its inverse, scratch, and
   // the chunk of C in sorted order
   size_t keys, perm, inv, sortscr, cs;
@@ -434,6 +435,8 @@ BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V, bool sort = false, size_t 
   o = align_up(o + sizeof(int), ALIGN);
   L.counters = o;  // two scheduler counters per chunk
   o = align_up(o + sizeof(int) * 2 * static_cast<size_t>(L.nchunks), ALIGN);
+  L.zero = o;  // 16 KiB of zeros: the A box of a CTA pair's skipped K-block
+  o = align_up(o + ZERO_BOX_BYTES, ALIGN);
   L.cscr = o;  // compaction scratch
   o = align_up(o + compact_scratch_bytes(N), ALIGN);
   L.pos = o;  // compaction map and compact copies of the rows that take part
@@ -1086,6 +1089,18 @@ cce_status cce_backward_ex2(const void* E, const void* C, const int64_t* x, cons
   if (pairs && !pair_operands(&g, Cg, D, c_rows)) return CCE_ERR_CUDA;
   r.bn = grad_tile_width(D, r.b3d ? 64 : 32);
   r.n_tiles = static_cast<int>(cdiv(D, r.bn));
+  // The gradient GEMM as CTA pairs (M = 256, each CTA loading its own 128 A
+  // rows and half of the MN-major B tile) when the D tiles are 256 wide and
+  // B comes in 3-D boxes.
+  const bool grad_pairs = pair_clusters > 0 && r.b3d && r.bn == BN;
+  if (grad_pairs) {
+    ok &= make_tmap_mn3(&r.tmB, Ec, D, N, 2);
+    ok &= make_tmap_mn3(&r.tmB2, Cg, D, c_rows, 2);
+    ok &= make_tmap(&r.tmZ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws + W.zero, BK, BM, BK, BK, BM);
+    if (!ok) return CCE_ERR_CUDA;
+    cudaError_t e = cudaMemsetAsync(ws + W.zero, 0, ZERO_BOX_BYTES, s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
 
   int* counters = reinterpret_cast<int*>(ws + W.counters);
   {
@@ -1127,7 +1142,12 @@ cce_status cce_backward_ex2(const void* E, const void* C, const int64_t* x, cons
     }
     {
       PhaseScope ps(4, s);
-      e = launch_gemm(MODE_GRAD, r, std::min(sms, (r.dc_m_tiles + r.n_blocks) * r.n_tiles), s);
+      if (grad_pairs) {
+        const int items = ((r.dc_m_tiles + 1) / 2 + (r.n_blocks + 1) / 2) * r.n_tiles;
+        e = launch_gemm_pairs(MODE_GRAD, r, std::min(pair_clusters, items), s);
+      } else {
+        e = launch_gemm(MODE_GRAD, r, std::min(sms, (r.dc_m_tiles + r.n_blocks) * r.n_tiles), s);
+      }
       g_launches++;
       if (e != cudaSuccess) return cuda_status(e);
     }

@@ -37,20 +37,24 @@
 //              the whole vocabulary: dE tiles split K into ranges written to
 //              separate fp32 slabs, dC tiles may write fp32 (store or add).
 //
-// Roles (192 threads): warp 0 lane 0 is the scheduler and TMA producer (a
+// Roles (224 threads): warp 0 lane 0 is the scheduler and TMA producer (a
 // 4-stage ring of 48 KiB stages); warp 1 owns TMEM (512 columns = two 128x256
 // fp32 accumulators) and lane 0 issues tcgen05.mma; warps 2..5 are the
-// epilogue (warp w reads TMEM lanes 32*(w%4) .. +31, i.e. tile rows).  Work
-// items are handed out dynamically (atomicAdd on a counter) and passed to the
-// MMA and epilogue warps through a small ring in shared memory, so every CTA
-// stays busy until the work runs out; the longest tiles are handed out first.
+// epilogue (warp w reads TMEM lanes 32*(w%4) .. +31, i.e. tile rows); warp 6
+// is the gradient-GEMM pairs' scheduler and idle otherwise.  Work items are
+// handed out dynamically (atomicAdd on a counter) and passed to the MMA and
+// epilogue warps through a small ring in shared memory, so every CTA stays
+// busy until the work runs out; the longest tiles are handed out first.
 //
 // CTA pairs (template flag PAIR; MODE_FWD always, MODE_BWD_G from 64 token
-// blocks): clusters of two CTAs on neighbouring SMs take the items of a pair
-// of token blocks in a fixed order.  Each CTA loads its 128 rows of A and half
-// of the 256-row B tile; the even CTA issues one MMA of M = 256 for both
-// (tcgen05 cta_group::2) and commits to both CTAs' barriers, and each CTA's
-// epilogue reads its own 128 accumulator rows.
+// blocks, MODE_GRAD of the two-call backward when the D tiles are 256 wide):
+// clusters of two CTAs on neighbouring SMs work on a pair of neighbouring row
+// blocks.  Each CTA loads its 128 rows of A and half of the 256-row B tile;
+// the even CTA issues one MMA of M = 256 for both (tcgen05 cta_group::2) and
+// commits to both CTAs' barriers, and each CTA's epilogue reads its own 128
+// accumulator rows.  FWD and BWD_G pairs take their items in a fixed order;
+// GRAD pairs take them from the even CTA's scheduler warp, which also reads
+// the two tiles' survival maps for the producers (their K-blocks differ).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -88,7 +92,9 @@ __device__ __forceinline__ Dims dims_of(const GemmArgs& a) {
   Dims d;
   d.nb = (n + BM - 1) / BM;
   d.dc_kb = (n + BK - 1) / BK;
-  if constexpr (PAIR) {  // items are pairs of token blocks
+  if constexpr (PAIR && MODE == MODE_GRAD) {  // items are pairs of vocabulary blocks (dC) or token blocks (dE)
+    d.items = (((a.dc_m_tiles + 1) >> 1) + ((d.nb + 1) >> 1) * max(a.de_splits, 1)) * a.n_tiles;
+  } else if constexpr (PAIR) {  // items are pairs of token blocks
     const int nbx = (MODE == MODE_BWD_G || a.n_dev) ? d.nb : a.n_blocks;
     d.items = ((nbx + 1) >> 1) * (MODE == MODE_BWD_G ? a.v_tiles : a.splits);
   } else if constexpr (MODE == MODE_FWD || MODE == MODE_FWD_STAGE) {
@@ -104,13 +110,38 @@ __device__ __forceinline__ Dims dims_of(const GemmArgs& a) {
 // Calls f(tile) for every tile of work item `item`; false if f asked to stop.
 template <int MODE, bool PAIR = false, typename F>
 __device__ __forceinline__ bool for_each_tile_of_item(const GemmArgs& a, const Dims& dm, int item, F&& f) {
-  if constexpr (PAIR) {
+  if constexpr (PAIR && MODE == MODE_GRAD) {
+    // Gradient GEMM as CTA pairs: an item is a pair of neighbouring row
+    // blocks of one kind -- vocabulary blocks 2p, 2p + 1 of the chunk (dC)
+    // or token blocks 2p, 2p + 1 (dE, with its K range) -- and a D tile; the
+    // CTA of rank r owns block 2p + r, which does not exist for the last pair
+    // of an odd count.  Same order as one CTA per tile: the longer kind first,
+    // the D tile fastest.
+    const int r = static_cast<int>(cluster_ctarank());
+    const int nsplit = max(a.de_splits, 1);
+    const int dc_items = ((a.dc_m_tiles + 1) >> 1) * a.n_tiles;
+    const int de_items = ((dm.nb + 1) >> 1) * nsplit * a.n_tiles;
+    int i = item, kind;
+    if (a.dc_first) {
+      kind = i < dc_items ? KIND_DC : KIND_DE;
+      if (kind == KIND_DE) i -= dc_items;
+    } else {
+      kind = i < de_items ? KIND_DE : KIND_DC;
+      if (kind == KIND_DC) i -= de_items;
+    }
+    if (kind == KIND_DC) {
+      const int m = 2 * (i / a.n_tiles) + r;
+      return f(Tile{kind, m, i % a.n_tiles, 0, true, true, m < a.dc_m_tiles});
+    }
+    const int ms = i / a.n_tiles;
+    const int m = 2 * (ms / nsplit) + r;
+    return f(Tile{kind, m, i % a.n_tiles, ms % nsplit, true, true, m < dm.nb});
+  } else if constexpr (PAIR) {
     // CTA pairs (FWD, BWD_G): an item is a pair of neighbouring
     // token blocks with a vocabulary split (FWD) or tile (BWD_G), in the same
     // grouped raster (group_n even, so groups hold whole pairs); the CTA of
     // rank r takes block 2p + r, which does not exist for the last pair of an
     // odd number of blocks.
-    static_assert(MODE != MODE_GRAD, "the gradient GEMM runs one CTA per tile");
     constexpr bool kFwd = MODE != MODE_BWD_G;
     const int nbx = (!kFwd || a.n_dev) ? dm.nb : a.n_blocks;
     const int nbp = (nbx + 1) >> 1, gp = a.group_n >> 1;
@@ -235,6 +266,61 @@ __device__ __forceinline__ int next_kblock(const GemmArgs& a, const Tile& t, int
   }
 }
 
+// Reader of one tile's survival map along its K range (gradient GEMM as CTA
+// pairs): dC tiles (K = tokens) read the vocabulary-major map, dE tiles
+// (K = chunk columns) the token-major one; filter column j covers K-blocks 2j
+// and 2j + 1.  The map is read 64 columns (128 K-blocks) at a time, with 64
+// independent byte loads, into a bit mask.
+struct KeepCursor {
+  const uint8_t* row;  // survival bytes of the tile's filter row (column j at row[j])
+  int jn;              // filter columns up to the end of the tile's K range
+  int w;               // window of columns held in bits (-1: none)
+  uint64_t bits;       // bit i: column 64 w + i is kept
+  bool all;            // the tile's output is not filtered: every K-block is kept
+};
+
+__device__ __forceinline__ KeepCursor keep_cursor(const GemmArgs& a, const Tile& t, int nk) {
+  KeepCursor c;
+  c.jn = (nk + 1) >> 1;
+  c.w = -1;
+  c.bits = 0;
+  if (t.kind == KIND_DC) {
+    c.all = !a.filter_dc;
+    c.row = a.bitmapT + static_cast<size_t>((a.chunk_v0 >> 7) + t.m) * a.n_blocks;
+  } else {
+    c.all = !a.filter_de;
+    c.row = a.bitmap + static_cast<size_t>(t.m) * a.bm_ld + (a.chunk_v0 >> 7);
+  }
+  return c;
+}
+
+__device__ __forceinline__ void keep_window(KeepCursor& c, int w) {
+  const int j0 = 64 * w;
+  uint8_t v[64];
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = (j0 + i < c.jn) ? __ldg(c.row + j0 + i) : uint8_t(0);
+  uint64_t b = 0;
+#pragma unroll
+  for (int i = 0; i < 64; ++i) b |= static_cast<uint64_t>(v[i] != 0) << i;
+  c.bits = b;
+  c.w = w;
+}
+
+// The first K-block >= kb whose filter column the cursor's tile keeps (nk
+// when none); filter column j covers K-blocks 2j and 2j + 1.
+__device__ __forceinline__ int keep_next(KeepCursor& c, int kb, int nk) {
+  if (c.all || kb >= nk) return min(kb, nk);
+  int j = kb >> 1;
+  while (j < c.jn) {
+    const int w = j >> 6;
+    if (w != c.w) keep_window(c, w);
+    const uint64_t m = c.bits >> (j & 63);
+    if (m) return max(kb, 2 * (j + __ffsll(static_cast<long long>(m)) - 1));
+    j = 64 * (w + 1);
+  }
+  return nk;
+}
+
 // Warp-wide: does the output tile have no surviving K-block at all?
 __device__ __forceinline__ bool tile_empty(const GemmArgs& a, const Dims& dm, const Tile& t) {
   if (!(t.kind == KIND_DC ? a.filter_dc : a.filter_de)) return false;  // this output is not filtered
@@ -250,6 +336,43 @@ __device__ __forceinline__ bool tile_empty(const GemmArgs& a, const Dims& dm, co
     for (int j = j0 + lane_id(); j < j1; j += 32) any |= __ldg(row + j);
   }
   return __any_sync(0xffffffffu, any) == 0;
+}
+
+// GRAD as CTA pairs: the pair's MMAs run over the union of the K-blocks its
+// two tiles keep, and a CTA whose own tile skips a K-block of it loads zeros
+// as its A operand there.  PairKeep walks that union on the two tiles' maps
+// (both CTAs the same union); a tile whose block does not exist (the last
+// pair of an odd count) keeps nothing.  The producer walks it only for a K
+// range longer than the scheduler's survival words (see RING_WIDE).
+struct PairKeep {
+  KeepCursor own, peer;
+  bool own_live, peer_live;
+  int nk;
+  int on, pn;  // the next K-block each tile keeps (nk: none left)
+};
+
+__device__ __forceinline__ PairKeep pair_keep(const GemmArgs& a, const Dims& dm, const Tile& t, int nk) {
+  PairKeep p;
+  Tile peer = t;
+  peer.m = t.m ^ 1;
+  p.own_live = t.live;
+  p.peer_live = peer.m < (t.kind == KIND_DC ? a.dc_m_tiles : dm.nb);
+  p.own = keep_cursor(a, t, nk);
+  p.peer = keep_cursor(a, peer, nk);
+  p.nk = nk;
+  const int kb0 = kblock_begin<MODE_GRAD>(a, t);
+  p.on = p.own_live ? keep_next(p.own, kb0, nk) : nk;
+  p.pn = p.peer_live ? keep_next(p.peer, kb0, nk) : nk;
+  return p;
+}
+
+// The pair's current K-block (nk when the union is exhausted).
+__device__ __forceinline__ int pair_kb(const PairKeep& p) { return min(p.on, p.pn); }
+
+// Moves past K-block kb (the current one).
+__device__ __forceinline__ void pair_advance(PairKeep& p, int kb) {
+  if (p.on == kb) p.on = p.own_live ? keep_next(p.own, kb + 1, p.nk) : p.nk;
+  if (p.pn == kb) p.pn = p.peer_live ? keep_next(p.peer, kb + 1, p.nk) : p.nk;
 }
 
 __device__ __forceinline__ float ex2(float v) {
@@ -282,7 +405,12 @@ struct SmemLayout {
   int* abort_flag;
   int* flags;       // [2 parity][2 half][4 warps]
   int* ring_ids;    // [RING]
-  int* stage_meta;  // [STAGES] what the producer put in the stage (META_*)
+  int* stage_meta;  // [MAX_STAGES] what the producer put in the stage (META_*)
+  // gradient-GEMM pairs: per ring slot, this CTA's own survival words, the
+  // union's, and the union's last K-block
+  uint64_t* ring_own;  // [RING][PAIR_MAP_WORDS]
+  uint64_t* ring_uni;  // [RING][PAIR_MAP_WORDS]
+  int* ring_last;      // [RING]
   // CTA pairs: cluster address of the even CTA's tmem_empty[0] (0: no pair)
   uint32_t tmem_empty_lead;
 };
@@ -299,9 +427,9 @@ __device__ __forceinline__ SmemLayout carve_smem(uint8_t* raw) {
   L.stages = base;
   L.epi = base + STAGES * STAGE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(L.epi + NUM_EPI_WARPS * EPI_WARP_BYTES);
-  L.full = bars;                          // STAGES
-  L.empty = L.full + STAGES;              // STAGES
-  L.tmem_full = L.empty + STAGES;         // 2
+  L.full = bars;                          // MAX_STAGES
+  L.empty = L.full + MAX_STAGES;          // MAX_STAGES
+  L.tmem_full = L.empty + MAX_STAGES;     // 2
   L.tmem_empty = L.tmem_full + 2;         // 2
   L.vote = L.tmem_empty + 2;              // 2
   L.drain = L.vote + 2;                   // 1
@@ -312,7 +440,14 @@ __device__ __forceinline__ SmemLayout carve_smem(uint8_t* raw) {
   L.abort_flag = reinterpret_cast<int*>(tail + 4);
   L.flags = reinterpret_cast<int*>(tail + 8);      // 16 ints
   L.ring_ids = reinterpret_cast<int*>(tail + 72);  // RING ints
-  L.stage_meta = reinterpret_cast<int*>(tail + 72 + 4 * RING);  // STAGES ints
+  L.stage_meta = reinterpret_cast<int*>(tail + 72 + 4 * RING);  // MAX_STAGES ints
+  constexpr int kWords = 72 + 4 * RING + 4 * MAX_STAGES;
+  L.ring_own = reinterpret_cast<uint64_t*>(tail + ((kWords + 7) & ~7));
+  L.ring_uni = L.ring_own + RING * PAIR_MAP_WORDS;
+  L.ring_last = reinterpret_cast<int*>(L.ring_uni + RING * PAIR_MAP_WORDS);
+  static_assert(8 * (2 * MAX_STAGES + 7 + 2 * RING) + ((kWords + 7) & ~7) + 16 * RING * PAIR_MAP_WORDS + 4 * RING <=
+                    BAR_BYTES,
+                "barriers and ring data fit their region");
   L.tmem_empty_lead = 0;
   return L;
 }
@@ -327,6 +462,30 @@ __device__ __forceinline__ int ring_take(const SmemLayout& L, int k, const GemmA
   const int item = *reinterpret_cast<volatile int*>(&L.ring_ids[slot]);
   mbar_arrive(&L.ring_empty[slot]);
   return item;
+}
+
+// GRAD as CTA pairs: the even CTA's scheduler warp hands out the items and
+// writes each into both CTAs' rings.  The odd CTA's consumers (its producer
+// and its epilogue warps) take theirs with a cluster-scope wait and free the
+// slot on the even CTA's ring_empty barrier, which counts both CTAs'
+// consumers.
+__device__ __forceinline__ int ring_take_odd(const SmemLayout& L, int k, const GemmArgs& a) {
+  const int slot = k % RING;
+  const uint32_t par = static_cast<uint32_t>((k / RING) & 1);
+  if (!wait_bounded<true>(&L.ring_full[slot], par, L.abort_flag, a.dev_err)) return -1;
+  const int item = *reinterpret_cast<volatile int*>(&L.ring_ids[slot]);
+  mbar_arrive_cluster(mapa_shared(smem_u32(&L.ring_empty[slot]), 0));
+  return item;
+}
+
+// The k-th work item for a consumer of this CTA (pairs of the gradient GEMM:
+// the odd CTA's consumers read what the even CTA's scheduler wrote).
+template <int MODE, bool PAIR>
+__device__ __forceinline__ int ring_take_any(const SmemLayout& L, int k, const GemmArgs& a) {
+  if constexpr (PAIR && MODE == MODE_GRAD) {
+    if (cluster_ctarank() != 0) return ring_take_odd(L, k, a);
+  }
+  return ring_take(L, k, a);
 }
 
 // ------------------------------------------------------------ L2 prefetch
@@ -459,12 +618,243 @@ __device__ __forceinline__ void producer_loop(const GemmArgs& a, const SmemLayou
   }
 }
 
+// The tile that work item `item` gives this CTA (gradient GEMM as CTA pairs).
+__device__ __forceinline__ Tile grad_pair_tile(const GemmArgs& a, const Dims& dm, int item) {
+  Tile t{};
+  for_each_tile_of_item<MODE_GRAD, true>(a, dm, item, [&](const Tile& u) -> bool {
+    t = u;
+    return true;
+  });
+  return t;
+}
+
+// Ring entries of the gradient GEMM as CTA pairs: 4 item + kind, -1 when no
+// work is left.  Kinds: RING_NONE, neither tile keeps a K-block; RING_DENSE,
+// both keep every K-block of the range; RING_BITS, the slot's survival words
+// say which K-blocks the pair runs (their union) and which of them this CTA's
+// own tile keeps; RING_WIDE, a K range of more than PAIR_MAP_WORDS words,
+// which the producer walks on the maps itself.
+constexpr int RING_BITS = 0, RING_NONE = 1, RING_DENSE = 2, RING_WIDE = 3;
+
+// One word of a tile's survival map: bit i for filter column 64 w + i, kept
+// and inside [j0, jn).
+__device__ __forceinline__ uint64_t keep_word(KeepCursor& c, bool live, int w, int j0) {
+  if (!live) return 0;
+  uint64_t b;
+  if (c.all) {
+    b = ~0ull;
+  } else {
+    keep_window(c, w);
+    b = c.bits;
+  }
+  const int lo = j0 - 64 * w, hi = c.jn - 64 * w;  // the range in this word's bits
+  if (lo > 0) b &= ~0ull << lo;
+  if (hi < 64) b &= (1ull << hi) - 1;
+  return b;
+}
+
+// Scheduler of the gradient GEMM as CTA pairs (the even CTA's warp 6): takes
+// the work items from the counter, reads both tiles' survival maps and
+// writes each entry, with its survival words, into both CTAs' rings, up to
+// RING items ahead of the consumers.  The map reads and the counter's atomic
+// latency are thus off the producers' critical path: the producer's work per
+// K-block sets the pace of the pair (the M = 256 MMAs of one K-block take
+// about 500 cycles), and measured, every instruction added to it showed.
+__device__ __forceinline__ void scheduler_loop_grad_pair(const GemmArgs& a, const SmemLayout& L) {
+  volatile int* abort_flag = L.abort_flag;
+  const Dims dm = dims_of<MODE_GRAD, true>(a);
+  for (int k = 0;; ++k) {
+    const int slot = k % RING;
+    // both CTAs' consumers have released the slot's previous item (cluster
+    // scope: the odd CTA's reads of its copy come before the slot is rewritten)
+    if (!wait_bounded<true>(&L.ring_empty[slot], static_cast<uint32_t>(((k / RING) & 1) ^ 1), abort_flag,
+                            a.dev_err))
+      break;
+    const int item = atomicAdd(a.counter, 1);
+    int v = -1;
+    if (item < dm.items) {
+      const Tile t = grad_pair_tile(a, dm, item);  // the even CTA's tile (always live)
+      Tile peer = t;
+      peer.m = t.m + 1;
+      const bool peer_live = peer.m < (t.kind == KIND_DC ? a.dc_m_tiles : dm.nb);
+      const int nk = kblocks_of<MODE_GRAD>(a, dm, t);
+      const int j0 = kblock_begin<MODE_GRAD>(a, t) >> 1;
+      KeepCursor oc = keep_cursor(a, t, nk), pc = keep_cursor(a, peer, nk);
+      const int jn = oc.jn;
+      const int w0 = j0 >> 6, wn = jn > j0 ? ((jn - 1) >> 6) + 1 : w0;
+      int kind = RING_WIDE;
+      if (wn - w0 <= PAIR_MAP_WORDS) {
+        bool any = false, dense = peer_live;
+        int last = -1;
+        uint64_t* own = L.ring_own + slot * PAIR_MAP_WORDS;
+        uint64_t* uni = L.ring_uni + slot * PAIR_MAP_WORDS;
+        const uint32_t own_odd = mapa_shared(smem_u32(own), 1), uni_odd = mapa_shared(smem_u32(uni), 1);
+        for (int w = w0; w < wn; ++w) {
+          const uint64_t ob = keep_word(oc, true, w, j0);
+          const uint64_t pb = keep_word(pc, peer_live, w, j0);
+          const uint64_t ub = ob | pb;
+          uint64_t full = ~0ull;  // the range's bits in this word
+          if (j0 - 64 * w > 0) full &= ~0ull << (j0 - 64 * w);
+          if (jn - 64 * w < 64) full &= (1ull << (jn - 64 * w)) - 1;
+          dense = dense && ob == full && pb == full;
+          if (ub) {
+            any = true;
+            last = min(2 * (64 * w + 63 - __clzll(static_cast<long long>(ub))) + 1, nk - 1);
+          }
+          own[w - w0] = ob;
+          uni[w - w0] = ub;
+          st_shared_cluster_u64(own_odd + 8u * static_cast<uint32_t>(w - w0), pb);  // the odd CTA's own tile
+          st_shared_cluster_u64(uni_odd + 8u * static_cast<uint32_t>(w - w0), ub);
+        }
+        kind = !any ? RING_NONE : (dense ? RING_DENSE : RING_BITS);
+        L.ring_last[slot] = last;
+        st_shared_cluster_u32(mapa_shared(smem_u32(&L.ring_last[slot]), 1), static_cast<uint32_t>(last));
+      }
+      v = 4 * item + kind;
+    }
+    L.ring_ids[slot] = v;
+    st_shared_cluster_u32(mapa_shared(smem_u32(&L.ring_ids[slot]), 1), static_cast<uint32_t>(v));
+    mbar_arrive(&L.ring_full[slot]);
+    mbar_arrive_cluster(mapa_shared(smem_u32(&L.ring_full[slot]), 1));  // release: the slot is visible first
+    if (v < 0) break;
+  }
+}
+
+// Producer of the gradient GEMM as CTA pairs (both CTAs).  Each CTA loads its
+// 128 rows of A (or 16 KiB of zeros where its own tile skips a K-block the
+// other tile keeps) and its half (128 columns) of the MN-major B tile, all
+// completing on the even CTA's full barrier, whose MMA thread issues one
+// M = 256 MMA for both.  The producer holds its ring slot (and reads the
+// slot's survival words) until the tile's loads are issued.
+__device__ __forceinline__ void producer_loop_grad_pair(const GemmArgs& a, const SmemLayout& L) {
+  constexpr int kStages = Pipe<MODE_GRAD, true>::kStages, kStageBytes = Pipe<MODE_GRAD, true>::kStageBytes;
+  volatile int* abort_flag = L.abort_flag;
+  const uint32_t rank = cluster_ctarank();
+  const Dims dm = dims_of<MODE_GRAD, true>(a);
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t issued_mask = 0, issued_par = 0;
+  const int half = static_cast<int>(rank) * (BN / 2);  // this CTA's columns of the B tile
+  const uint32_t full_lead = mapa_shared(smem_u32(&L.full[0]), 0);  // the even CTA's full barriers
+  // Loads K-block kb of tile t into the next stage: this CTA's A rows (zeros
+  // where `mine` is false) and its half of B.
+  auto issue = [&](const Tile& t, int kb, bool mine, bool last) -> bool {
+    if (!wait_bounded(&L.empty[stage], phase ^ 1u, abort_flag, a.dev_err)) return false;
+    uint8_t* sA = L.stages + stage * kStageBytes;
+    uint8_t* sB = sA + A_STAGE_BYTES;
+    const uint32_t fb_lead = full_lead + 8u * static_cast<uint32_t>(stage);
+    if (rank == 0) {
+      L.stage_meta[stage] = last ? META_LAST : 0;
+      mbar_arrive_expect_tx(&L.full[stage], 2 * PAIR_STAGE_BYTES);
+    }
+    const int k0 = kb * BK;
+    const int bz = (t.n * a.bn + half) >> 6;  // first 64-column group of this CTA's B half
+    if (!mine) {
+      tma_load_2d_pair(&a.tmZ, fb_lead, sA, 0, 0);
+    } else if (t.kind == KIND_DC) {
+      tma_load_3d_pair(&a.tmA, fb_lead, sA, 0, k0, (t.m * BM) >> 6);
+    } else {
+      tma_load_2d_pair(&a.tmA2, fb_lead, sA, k0, t.m * BM);
+    }
+    if (t.kind == KIND_DC) {
+      tma_load_3d_pair(&a.tmB, fb_lead, sB, 0, k0, bz);
+    } else {
+      tma_load_3d_pair(&a.tmB2, fb_lead, sB, 0, a.c_row0 + k0, bz);
+    }
+    issued_mask |= 1u << stage;
+    issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+    if (++stage == kStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+    return true;
+  };
+  for (int k = 0;; ++k) {
+    const int slot = k % RING;
+    if (!wait_bounded<true>(&L.ring_full[slot], static_cast<uint32_t>((k / RING) & 1), abort_flag, a.dev_err))
+      break;
+    const int v = *reinterpret_cast<volatile int*>(&L.ring_ids[slot]);
+    auto release = [&] {
+      if (rank == 0) {
+        mbar_arrive(&L.ring_empty[slot]);
+      } else {
+        mbar_arrive_cluster(mapa_shared(smem_u32(&L.ring_empty[slot]), 0));
+      }
+    };
+    const int kind = v & 3;
+    // RING_NONE: no stage at all; the MMA thread reads the same from the ring
+    // entry and signals the epilogues without an MMA.  (A stage without
+    // copies would let the even CTA's MMA thread release this CTA's stage
+    // twice before this CTA waits on it: only the odd CTA's copies, which
+    // complete on the even CTA's full barrier, keep the two CTAs' stage
+    // phases in step.)
+    if (v < 0 || kind == RING_NONE) {
+      release();
+      if (v < 0) break;
+      continue;
+    }
+    const Tile t = grad_pair_tile(a, dm, v >> 2);
+    const int nk = kblocks_of<MODE_GRAD>(a, dm, t);
+    const int kb0 = kblock_begin<MODE_GRAD>(a, t);
+    bool ok = true;
+    if (kind == RING_DENSE) {
+      release();
+      for (int kb = kb0; ok && kb < nk; ++kb) ok = issue(t, kb, true, kb + 1 == nk);
+    } else if (kind == RING_BITS) {
+      // the union's kept filter columns, each two K-blocks
+      const uint64_t* own = L.ring_own + slot * PAIR_MAP_WORDS;
+      const uint64_t* uni = L.ring_uni + slot * PAIR_MAP_WORDS;
+      const int last = L.ring_last[slot];
+      const int w0 = kb0 >> 7, wn = ((nk + 1) >> 1) > (kb0 >> 1) ? ((((nk + 1) >> 1) - 1) >> 6) + 1 : w0;
+      for (int w = w0; ok && w < wn; ++w) {
+        uint64_t u = uni[w - w0];
+        const uint64_t o = own[w - w0];
+        while (ok && u) {
+          const int i = __ffsll(static_cast<long long>(u)) - 1;
+          u &= u - 1;
+          const bool mine = (o >> i) & 1u;
+          const int col = 64 * w + i;
+          const int kb_end = min(2 * col + 2, nk);
+          for (int kb = max(2 * col, kb0); ok && kb < kb_end; ++kb) ok = issue(t, kb, mine, kb == last);
+        }
+      }
+      release();
+    } else {  // RING_WIDE
+      release();
+      PairKeep pk = pair_keep(a, dm, t, nk);
+      for (int kb = pair_kb(pk); ok && kb < nk;) {
+        const bool mine = pk.on == kb;
+        pair_advance(pk, kb);
+        const int next = pair_kb(pk);
+        ok = issue(t, kb, mine, next >= nk);
+        kb = next;
+      }
+    }
+    if (!ok) break;
+  }
+  if (rank != 0 && *abort_flag) {
+    // This CTA's copies complete on the even CTA's barriers; give any still
+    // in flight a bounded 10 ms to land before the CTA exits.
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 10000000ull) {
+    }
+  } else if (*abort_flag) {
+    for (int s = 0; s < kStages; ++s) {
+      if (issued_mask & (1u << s)) {
+        volatile int dummy = 0;
+        wait_bounded(&L.full[s], (issued_par >> s) & 1u, &dummy, nullptr);
+      }
+    }
+  }
+}
+
 // --------------------------------------------------------------------- MMA
 template <int MODE, bool PAIR = false>
 __device__ __forceinline__ void mma_loop(const GemmArgs& a, const SmemLayout& L, uint32_t tmem_base) {
   // CTA pairs: the even CTA issues every MMA (M = 256) for both; the odd
   // CTA's MMA thread has nothing to do.
   if (PAIR && cluster_ctarank() != 0) return;
+  constexpr int kStages = Pipe<MODE, PAIR>::kStages, kStageBytes = Pipe<MODE, PAIR>::kStageBytes;
   volatile int* abort_flag = L.abort_flag;
   int stage = 0;
   uint32_t phase = 0;
@@ -473,8 +863,13 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& a, const SmemLayout& L,
   bool issued_any = false;
   const Dims dm = dims_of<MODE, PAIR>(a);
   for (int k = 0;; ++k) {
-    const int item = ring_take(L, k, a);
+    int item = ring_take(L, k, a);
     if (item < 0) break;
+    bool none_kept = false;  // gradient-GEMM pairs: neither tile keeps a K-block
+    if constexpr (PAIR && MODE == MODE_GRAD) {
+      none_kept = (item & 3) == RING_NONE;
+      item >>= 2;
+    }
     const bool ok = for_each_tile_of_item<MODE, PAIR>(a, dm, item, [&](const Tile& t) -> bool {
       // Operand majorness and tile width of this tile.
       const bool a_mn = (MODE == MODE_GRAD) && t.kind == KIND_DC;
@@ -488,6 +883,18 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& a, const SmemLayout& L,
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
       bool any = false;
+      if constexpr (PAIR && MODE == MODE_GRAD) {
+        // a pair whose two tiles keep no K-block has no stage (see the producer)
+        if (none_kept) {
+          mbar_arrive(&L.tmem_full[acc]);
+          mbar_arrive_cluster(mapa_shared(smem_u32(&L.tmem_full[acc]), 1));
+          if (++acc == PAIR_ACCS) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
+          return true;
+        }
+      }
       // FWD / BWD_G: every K-block; GRAD: the producer's stage tags end the loop
       const int nk = MODE == MODE_GRAD ? 0 : kblocks_of<MODE>(a, dm, t);
       for (int kb = 0;; ++kb) {
@@ -498,15 +905,15 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& a, const SmemLayout& L,
         if constexpr (MODE == MODE_GRAD) {
           meta = *reinterpret_cast<volatile int*>(&L.stage_meta[stage]);
           if (meta & META_EMPTY) {
-            mbar_arrive(&L.empty[stage]);  // hand the stage straight back
-            if (++stage == STAGES) {
+            mbar_arrive(&L.empty[stage]);  // hand the stage straight back (one CTA per tile only)
+            if (++stage == kStages) {
               stage = 0;
               phase ^= 1u;
             }
             break;
           }
         }
-        const uint32_t sA = smem_u32(L.stages + stage * STAGE_BYTES);
+        const uint32_t sA = smem_u32(L.stages + stage * kStageBytes);
         const uint32_t sB = sA + A_STAGE_BYTES;
         const uint64_t adesc = smem_desc_sw128(sA, a_lbo, 1024u);
         const uint64_t bdesc = smem_desc_sw128(sB, b_lbo, 1024u);
@@ -525,14 +932,14 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& a, const SmemLayout& L,
         } else {
           mma_commit(&L.empty[stage]);
         }
-        if (++stage == STAGES) {
+        if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
         }
         if (MODE == MODE_GRAD && (meta & META_LAST)) break;
       }
       if (PAIR) {
-        mma_commit_pair_both(&L.tmem_full[acc]);  // FWD tiles always have MMAs
+        mma_commit_pair_both(&L.tmem_full[acc]);  // both CTAs' epilogues (pairs: every tile here has MMAs)
       } else if (any) {
         mma_commit(&L.tmem_full[acc]);
       } else {
@@ -1066,14 +1473,17 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& a, const SmemLayou
   const Dims dm = dims_of<MODE, PAIR>(a);
   for (int k = 0;; ++k) {
     int item = 0;
-    if (lane_id() == 0) item = ring_take(L, k, a);
+    if (lane_id() == 0) item = ring_take_any<MODE, PAIR>(L, k, a);
     item = __shfl_sync(0xffffffffu, item, 0);
     if (item < 0) break;
+    if (PAIR && MODE == MODE_GRAD) item >>= 2;  // the entry's low bits are for the MMA and producers
     const bool ok = for_each_tile_of_item<MODE, PAIR>(a, dm, item, [&](const Tile& t) -> bool {
       if (!warp_wait_bounded(&L.tmem_full[acc], acc_phase, L.abort_flag, a.dev_err)) return false;
       tc_fence_after();
       bool r = true;
-      if constexpr (MODE == MODE_FWD) {
+      if (MODE == MODE_GRAD && !t.live) {
+        release_tmem(L, acc);  // the missing block of the last pair: nothing to write
+      } else if constexpr (MODE == MODE_FWD) {
         epi_fwd<CAP>(a, L, t, acc, e, st);
       } else if constexpr (MODE == MODE_FWD_STAGE) {
         epi_fwd_stage<CAP>(a, L, t, acc, e, st);
@@ -1110,7 +1520,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cce_gemm_kernel(const __grid_c
   const bool lead = !PAIR || cluster_ctarank() == 0;
   if (PAIR) L.tmem_empty_lead = mapa_shared(smem_u32(&L.tmem_empty[0]), 0);
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < Pipe<MODE, PAIR>::kStages; ++s) {
       mbar_init(&L.full[s], 1);
       mbar_init(&L.empty[s], 1);
     }
@@ -1122,8 +1532,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cce_gemm_kernel(const __grid_c
     }
     for (int i = 0; i < RING; ++i) {
       mbar_init(&L.ring_full[i], 1);
-      // the MMA thread (the odd CTA of a pair has none at work) and every epilogue warp
-      mbar_init(&L.ring_empty[i], (lead ? 1 : 0) + NUM_EPI_WARPS);
+      // the MMA thread (the odd CTA of a pair has none at work) and every
+      // epilogue warp; gradient-GEMM pairs: the even CTA's barrier counts the
+      // consumers of both CTAs (its producer, MMA thread and epilogue warps,
+      // the odd CTA's producer and epilogue warps)
+      mbar_init(&L.ring_empty[i],
+                (PAIR && MODE == MODE_GRAD) ? 2 * (1 + NUM_EPI_WARPS) + 1 : (lead ? 1 : 0) + NUM_EPI_WARPS);
     }
     mbar_init(L.drain, 1);
     *L.abort_flag = 0;
@@ -1137,6 +1551,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cce_gemm_kernel(const __grid_c
       tma_prefetch_desc(&a.tmA2);
       tma_prefetch_desc(&a.tmB2);
       tma_prefetch_desc(&a.tmOut2);
+      if (PAIR) tma_prefetch_desc(&a.tmZ);
     }
   }
   if (warp == 1) {
@@ -1155,11 +1570,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cce_gemm_kernel(const __grid_c
   const uint32_t tmem_base = *L.tmem_base;
 
   if (warp == 0) {
-    if (lane_id() == 0) producer_loop<MODE, PAIR>(a, L);
+    if (lane_id() == 0) {
+      if constexpr (PAIR && MODE == MODE_GRAD) {
+        producer_loop_grad_pair(a, L);
+      } else {
+        producer_loop<MODE, PAIR>(a, L);
+      }
+    }
   } else if (warp == 1) {
     if (lane_id() == 0) mma_loop<MODE, PAIR>(a, L, tmem_base);
-  } else {
+  } else if (warp < 2 + NUM_EPI_WARPS) {
     epilogue_loop<MODE, CAP, PAIR>(a, L, tmem_base, warp);
+  } else if constexpr (PAIR && MODE == MODE_GRAD) {
+    if (lane_id() == 0 && cluster_ctarank() == 0) scheduler_loop_grad_pair(a, L);
   }
 
   tc_fence_before();

@@ -16,14 +16,20 @@ constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;  // 48 KiB
 constexpr int PAIR_STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES / 2;  // one CTA of a pair: A + half of B
 constexpr int NUM_EPI_WARPS = 4;
 constexpr int EPI_WARP_BYTES = 8192;
-constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
+// warps: 0 producer, 1 MMA, 2-5 epilogue, 6 scheduler (gradient-GEMM pairs;
+// idle otherwise)
+constexpr int NUM_THREADS = 96 + 32 * NUM_EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
 // CTA pairs: TMEM columns allocated (together, by both CTAs) and accumulators
 constexpr uint32_t PAIR_TMEM_COLS = 512;
 constexpr int PAIR_ACCS = 2;
 constexpr int PAIR_MIN_BLOCKS = 64;  // recompute as CTA pairs from this many 128-row token blocks
 constexpr int RING = 4;  // depth of the work-item ring between the scheduler and the consumers
-constexpr int BAR_BYTES = 512;
+// gradient-GEMM pairs: survival words per ring slot (64 filter columns, 128
+// K-blocks each): K ranges up to 1024 K-blocks take the scheduler's words
+constexpr int PAIR_MAP_WORDS = 8;
+// barriers, flags, ring ids, stage tags and the pairs' survival words
+constexpr int BAR_BYTES = 1024;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_EPI_WARPS * EPI_WARP_BYTES + BAR_BYTES;
 constexpr int FILTER_TILE = 128;  // filter decisions are per 128 tokens x 128 vocab
 
@@ -35,6 +41,22 @@ constexpr float NEG_BIG = -3.0e38f;  // finite "minus infinity" for the running 
 // is MODE_FWD that also stages its logits for the single call (see mtile).
 enum Mode { MODE_FWD = 0, MODE_BWD_G = 1, MODE_GRAD = 2, MODE_FWD_STAGE = 3 };
 enum Kind { KIND_MAIN = 0, KIND_DC = 1, KIND_DE = 2 };
+
+// Pipeline depth and stage size of one CTA.  A CTA of a gradient-GEMM pair
+// holds 32 KiB of operands per K-block (its A rows and half of B) instead of
+// 48, so the same stage memory holds six stages: the pair's stages complete
+// only when both CTAs' copies (mostly G-hat from DRAM) have landed, and the
+// deeper pipeline covers that latency.  (The logit-GEMM pairs keep four
+// stages: six measured no faster for them.)
+constexpr int PAIR_STAGES = STAGES * STAGE_BYTES / PAIR_STAGE_BYTES;  // 6
+constexpr int MAX_STAGES = PAIR_STAGES > STAGES ? PAIR_STAGES : STAGES;
+static_assert(PAIR_STAGES * PAIR_STAGE_BYTES == STAGES * STAGE_BYTES, "pair stages fill the stage memory");
+template <int MODE, bool PAIR>
+struct Pipe {
+  static constexpr bool kDeep = PAIR && MODE == MODE_GRAD;
+  static constexpr int kStages = kDeep ? PAIR_STAGES : STAGES;
+  static constexpr int kStageBytes = kDeep ? PAIR_STAGE_BYTES : STAGE_BYTES;
+};
 
 struct GemmArgs {
   // FWD / BWD_G: A = E, B = C, Out = G chunk (BWD_G).  GRAD: the dC kind's
@@ -48,6 +70,10 @@ struct GemmArgs {
   CUtensorMap tmA2;
   CUtensorMap tmB2;
   CUtensorMap tmOut2;
+  // GRAD as CTA pairs: one A-sized box (16 KiB) of zeros, loaded in place of
+  // a CTA's A operand for a K-block its own tile skips but the other CTA's
+  // tile keeps (the pair's MMA walks the union of the two tiles' K-blocks)
+  CUtensorMap tmZ;
   int N, D, V;
   int n_blocks;  // ceil(N / 128)
   int k_blocks;  // FWD / BWD_G: ceil(D / 64)

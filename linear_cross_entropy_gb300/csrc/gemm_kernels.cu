@@ -22,6 +22,7 @@ cudaError_t prepare_gemm_kernels() {
   if ((e = set_smem<MODE_FWD, true, true>()) != cudaSuccess) return e;
   if ((e = set_smem<MODE_BWD_G, false, true>()) != cudaSuccess) return e;
   if ((e = set_smem<MODE_BWD_G, true, true>()) != cudaSuccess) return e;
+  if ((e = set_smem<MODE_GRAD, false, true>()) != cudaSuccess) return e;
   return set_smem<MODE_GRAD, false>();
 }
 
@@ -62,6 +63,7 @@ cudaError_t launch_gemm_pairs(int mode, const GemmArgs& args, int clusters, cuda
     case MODE_BWD_G:
       return cap ? cudaLaunchKernelEx(&cfg, cce_gemm_kernel<MODE_BWD_G, true, true>, args)
                  : cudaLaunchKernelEx(&cfg, cce_gemm_kernel<MODE_BWD_G, false, true>, args);
+    case MODE_GRAD: return cudaLaunchKernelEx(&cfg, cce_gemm_kernel<MODE_GRAD, false, true>, args);
     default: return cudaErrorInvalidValue;
   }
 }

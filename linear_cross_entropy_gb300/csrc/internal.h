@@ -12,9 +12,11 @@ namespace cce {
 // Launches cce_gemm_kernel<mode> with `grid` persistent CTAs on `stream`.
 cudaError_t launch_gemm(int mode, const GemmArgs& args, int grid, cudaStream_t stream);
 
-// cce_gemm_kernel<mode> (FWD, BWD_G) as `clusters` persistent
-// clusters of two CTAs sharing each MMA (M = 256) over pairs of token blocks;
-// args.tmB2 holds C in 128-row boxes and args.group_n is even.
+// cce_gemm_kernel<mode> (FWD, BWD_G, GRAD) as `clusters` persistent
+// clusters of two CTAs sharing each MMA (M = 256) over pairs of row blocks.
+// FWD / BWD_G: args.tmB2 holds C in 128-row boxes and args.group_n is even.
+// GRAD: the MN-major B maps come in 128-column (two-group) boxes, args.bn is
+// 256, and args.tmZ is a 16 KiB box of zeros.
 cudaError_t launch_gemm_pairs(int mode, const GemmArgs& args, int clusters, cudaStream_t stream);
 
 // How many CTA pairs of the GEMM kernel fit on the device at once (0: none).

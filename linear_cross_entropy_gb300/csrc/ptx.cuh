@@ -61,16 +61,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same with cluster scope: data the other CTA of a pair wrote into this
+// CTA's shared memory before its release-arrive on *bar is visible after it.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits until the phase with the given parity of *bar has completed.  Returns
 // false (and raises *abort_flag) if the wait ran out after timeout_ns, or if
 // another role of the CTA already aborted.  Call from a single thread.
+// kCluster: acquire at cluster scope (the barrier is arrived on from the
+// other CTA of a pair, which also wrote data the caller reads).
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bounded_ns(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                                 int32_t* dev_err, uint64_t timeout_ns) {
   const uint32_t b = smem_u32(bar);
-  if (mbar_try_wait(b, parity)) return true;
+  auto try_wait = [&]() { return kCluster ? mbar_try_wait_cluster(b, parity) : mbar_try_wait(b, parity); };
+  if (try_wait()) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
-    if (mbar_try_wait(b, parity)) return true;
+    if (try_wait()) return true;
     if (*abort_flag) return false;
     if (globaltimer() - t0 > timeout_ns) {
       *abort_flag = 1;
@@ -80,9 +98,10 @@ __device__ __forceinline__ bool wait_bounded_ns(uint64_t* bar, uint32_t parity, 
   }
 }
 
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                              int32_t* dev_err) {
-  return wait_bounded_ns(bar, parity, abort_flag, dev_err, CCE_WAIT_TIMEOUT_NS);
+  return wait_bounded_ns<kCluster>(bar, parity, abort_flag, dev_err, CCE_WAIT_TIMEOUT_NS);
 }
 
 // Warp-uniform bounded wait: lane 0 waits, the result is broadcast.
@@ -264,6 +283,24 @@ __device__ __forceinline__ void tma_load_2d_pair(const CUtensorMap* m, uint32_t 
       "[%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y)
       : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair(const CUtensorMap* m, uint32_t bar_cluster, void* smem_dst, int32_t x,
+                                                 int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// 32-bit store into the shared memory of a CTA of the cluster (cluster address).
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_shared_cluster_u64(uint32_t cluster_addr, uint64_t v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(cluster_addr), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
