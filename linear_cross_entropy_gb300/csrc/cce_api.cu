@@ -30,7 +30,7 @@ constexpr size_t ALIGN = 256;         // sub-buffer alignment inside a workspace
 constexpr size_t G_CHUNK_BUDGET = size_t(CCE_G_CHUNK_BUDGET_MIB) << 20;  // bytes of the backward G chunk buffer
 constexpr int64_t MIN_CHUNK = 2048, MAX_CHUNK = 65536;
 constexpr int COMBINE_THREADS = 256;
-constexpr size_t ZERO_BOX_BYTES = size_t(BM) * BK * 2;  // one A operand box
+constexpr size_t ZERO_BOX_BYTES = PAIR_GRAD_A_BYTES;  // one A operand box of the pair gradient GEMM
 
 std::atomic<uint64_t> g_launches{0};
 
@@ -617,13 +617,16 @@ bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void*
   return r == CUDA_SUCCESS;
 }
 
-// bf16 [rows][D] viewed as {64 d, rows, D / 64 groups} with box {64, 64,
-// groups}: one TMA instruction brings all 64-column groups of an MN-major
-// operand stage (D % 64 == 0, so the view never reaches past a row).
-bool make_tmap_mn3(CUtensorMap* m, const void* ptr, uint64_t D, uint64_t rows, uint32_t groups = 4) {
+// bf16 [rows][D] viewed as {64 d, rows, D / 64 groups} with box {64,
+// box_rows, groups}: one TMA instruction brings all 64-column groups of an
+// MN-major operand stage (D % 64 == 0, so the view never reaches past a row).
+// The same view of a K-major operand (D = K) brings box_rows rows of `groups`
+// consecutive 64-column K-blocks, one after the other.
+bool make_tmap_mn3(CUtensorMap* m, const void* ptr, uint64_t D, uint64_t rows, uint32_t groups = 4,
+                   uint32_t box_rows = 64) {
   cuuint64_t dims[3] = {64, rows, D / 64};
   cuuint64_t strides[2] = {D * 2, 128};
-  cuuint32_t box[3] = {64, 64, groups};
+  cuuint32_t box[3] = {64, box_rows, groups};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1090,13 +1093,16 @@ cce_status cce_backward_ex2(const void* E, const void* C, const int64_t* x, cons
   r.bn = grad_tile_width(D, r.b3d ? 64 : 32);
   r.n_tiles = static_cast<int>(cdiv(D, r.bn));
   // The gradient GEMM as CTA pairs (M = 256, each CTA loading its own 128 A
-  // rows and half of the MN-major B tile) when the D tiles are 256 wide and
-  // B comes in 3-D boxes.
+  // rows and half of the MN-major B tile, K = 128 per stage) when the D tiles
+  // are 256 wide and B comes in 3-D boxes: every operand is one 3-D box of
+  // two 64-column groups and 128 rows.
   const bool grad_pairs = pair_clusters > 0 && r.b3d && r.bn == BN;
   if (grad_pairs) {
-    ok &= make_tmap_mn3(&r.tmB, Ec, D, N, 2);
-    ok &= make_tmap_mn3(&r.tmB2, Cg, D, c_rows, 2);
-    ok &= make_tmap(&r.tmZ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws + W.zero, BK, BM, BK, BK, BM);
+    ok &= make_tmap_mn3(&r.tmA, gbuf, vc, N, 2, PAIR_BK);  // dC: 128 vocabulary columns x 128 tokens (K)
+    ok &= make_tmap_mn3(&r.tmA2, gbuf, vc, N, 2, BM);      // dE: 128 tokens x two 64-column K-blocks
+    ok &= make_tmap_mn3(&r.tmB, Ec, D, N, 2, PAIR_BK);
+    ok &= make_tmap_mn3(&r.tmB2, Cg, D, c_rows, 2, PAIR_BK);
+    ok &= make_tmap(&r.tmZ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws + W.zero, 64, 2 * BM, 64, 64, 2 * BM);
     if (!ok) return CCE_ERR_CUDA;
     cudaError_t e = cudaMemsetAsync(ws + W.zero, 0, ZERO_BOX_BYTES, s);
     if (e != cudaSuccess) return cuda_status(e);

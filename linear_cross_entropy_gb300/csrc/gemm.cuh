@@ -306,19 +306,17 @@ __device__ __forceinline__ void keep_window(KeepCursor& c, int w) {
   c.w = w;
 }
 
-// The first K-block >= kb whose filter column the cursor's tile keeps (nk
-// when none); filter column j covers K-blocks 2j and 2j + 1.
-__device__ __forceinline__ int keep_next(KeepCursor& c, int kb, int nk) {
-  if (c.all || kb >= nk) return min(kb, nk);
-  int j = kb >> 1;
+// The first filter column >= j that the cursor's tile keeps (jn when none).
+__device__ __forceinline__ int keep_next(KeepCursor& c, int j) {
+  if (c.all) return min(j, c.jn);
   while (j < c.jn) {
     const int w = j >> 6;
     if (w != c.w) keep_window(c, w);
     const uint64_t m = c.bits >> (j & 63);
-    if (m) return max(kb, 2 * (j + __ffsll(static_cast<long long>(m)) - 1));
+    if (m) return j + __ffsll(static_cast<long long>(m)) - 1;
     j = 64 * (w + 1);
   }
-  return nk;
+  return c.jn;
 }
 
 // Warp-wide: does the output tile have no surviving K-block at all?
@@ -340,15 +338,16 @@ __device__ __forceinline__ bool tile_empty(const GemmArgs& a, const Dims& dm, co
 
 // GRAD as CTA pairs: the pair's MMAs run over the union of the K-blocks its
 // two tiles keep, and a CTA whose own tile skips a K-block of it loads zeros
-// as its A operand there.  PairKeep walks that union on the two tiles' maps
-// (both CTAs the same union); a tile whose block does not exist (the last
-// pair of an odd count) keeps nothing.  The producer walks it only for a K
-// range longer than the scheduler's survival words (see RING_WIDE).
+// as its A operand there.  Its K-blocks are 128 deep, one filter column each.
+// PairKeep walks that union on the two tiles' maps (both CTAs the same
+// union); a tile whose block does not exist (the last pair of an odd count)
+// keeps nothing.  The producer walks it only for a K range longer than the
+// scheduler's survival words (see RING_WIDE).
 struct PairKeep {
   KeepCursor own, peer;
   bool own_live, peer_live;
-  int nk;
-  int on, pn;  // the next K-block each tile keeps (nk: none left)
+  int jn;      // end of the K range in columns
+  int on, pn;  // the next column each tile keeps (jn: none left)
 };
 
 __device__ __forceinline__ PairKeep pair_keep(const GemmArgs& a, const Dims& dm, const Tile& t, int nk) {
@@ -359,20 +358,20 @@ __device__ __forceinline__ PairKeep pair_keep(const GemmArgs& a, const Dims& dm,
   p.peer_live = peer.m < (t.kind == KIND_DC ? a.dc_m_tiles : dm.nb);
   p.own = keep_cursor(a, t, nk);
   p.peer = keep_cursor(a, peer, nk);
-  p.nk = nk;
-  const int kb0 = kblock_begin<MODE_GRAD>(a, t);
-  p.on = p.own_live ? keep_next(p.own, kb0, nk) : nk;
-  p.pn = p.peer_live ? keep_next(p.peer, kb0, nk) : nk;
+  p.jn = p.own.jn;
+  const int j0 = kblock_begin<MODE_GRAD>(a, t) >> 1;
+  p.on = p.own_live ? keep_next(p.own, j0) : p.jn;
+  p.pn = p.peer_live ? keep_next(p.peer, j0) : p.jn;
   return p;
 }
 
-// The pair's current K-block (nk when the union is exhausted).
+// The pair's current column (jn when the union is exhausted).
 __device__ __forceinline__ int pair_kb(const PairKeep& p) { return min(p.on, p.pn); }
 
-// Moves past K-block kb (the current one).
-__device__ __forceinline__ void pair_advance(PairKeep& p, int kb) {
-  if (p.on == kb) p.on = p.own_live ? keep_next(p.own, kb + 1, p.nk) : p.nk;
-  if (p.pn == kb) p.pn = p.peer_live ? keep_next(p.peer, kb + 1, p.nk) : p.nk;
+// Moves past column j (the current one).
+__device__ __forceinline__ void pair_advance(PairKeep& p, int j) {
+  if (p.on == j) p.on = p.own_live ? keep_next(p.own, j + 1) : p.jn;
+  if (p.pn == j) p.pn = p.peer_live ? keep_next(p.peer, j + 1) : p.jn;
 }
 
 __device__ __forceinline__ float ex2(float v) {
@@ -407,7 +406,7 @@ struct SmemLayout {
   int* ring_ids;    // [RING]
   int* stage_meta;  // [MAX_STAGES] what the producer put in the stage (META_*)
   // gradient-GEMM pairs: per ring slot, this CTA's own survival words, the
-  // union's, and the union's last K-block
+  // union's, and the union's last (128-deep) K-block
   uint64_t* ring_own;  // [RING][PAIR_MAP_WORDS]
   uint64_t* ring_uni;  // [RING][PAIR_MAP_WORDS]
   int* ring_last;      // [RING]
@@ -631,9 +630,9 @@ __device__ __forceinline__ Tile grad_pair_tile(const GemmArgs& a, const Dims& dm
 // Ring entries of the gradient GEMM as CTA pairs: 4 item + kind, -1 when no
 // work is left.  Kinds: RING_NONE, neither tile keeps a K-block; RING_DENSE,
 // both keep every K-block of the range; RING_BITS, the slot's survival words
-// say which K-blocks the pair runs (their union) and which of them this CTA's
-// own tile keeps; RING_WIDE, a K range of more than PAIR_MAP_WORDS words,
-// which the producer walks on the maps itself.
+// say which K-blocks (one per filter column) the pair runs (their union) and
+// which of them this CTA's own tile keeps; RING_WIDE, a K range of more than
+// PAIR_MAP_WORDS words, which the producer walks on the maps itself.
 constexpr int RING_BITS = 0, RING_NONE = 1, RING_DENSE = 2, RING_WIDE = 3;
 
 // One word of a tile's survival map: bit i for filter column 64 w + i, kept
@@ -699,7 +698,7 @@ __device__ __forceinline__ void scheduler_loop_grad_pair(const GemmArgs& a, cons
           dense = dense && ob == full && pb == full;
           if (ub) {
             any = true;
-            last = min(2 * (64 * w + 63 - __clzll(static_cast<long long>(ub))) + 1, nk - 1);
+            last = 64 * w + 63 - __clzll(static_cast<long long>(ub));
           }
           own[w - w0] = ob;
           uni[w - w0] = ub;
@@ -727,7 +726,7 @@ __device__ __forceinline__ void scheduler_loop_grad_pair(const GemmArgs& a, cons
 // M = 256 MMA for both.  The producer holds its ring slot (and reads the
 // slot's survival words) until the tile's loads are issued.
 __device__ __forceinline__ void producer_loop_grad_pair(const GemmArgs& a, const SmemLayout& L) {
-  constexpr int kStages = Pipe<MODE_GRAD, true>::kStages, kStageBytes = Pipe<MODE_GRAD, true>::kStageBytes;
+  using P = Pipe<MODE_GRAD, true>;
   volatile int* abort_flag = L.abort_flag;
   const uint32_t rank = cluster_ctarank();
   const Dims dm = dims_of<MODE_GRAD, true>(a);
@@ -736,25 +735,25 @@ __device__ __forceinline__ void producer_loop_grad_pair(const GemmArgs& a, const
   uint32_t issued_mask = 0, issued_par = 0;
   const int half = static_cast<int>(rank) * (BN / 2);  // this CTA's columns of the B tile
   const uint32_t full_lead = mapa_shared(smem_u32(&L.full[0]), 0);  // the even CTA's full barriers
-  // Loads K-block kb of tile t into the next stage: this CTA's A rows (zeros
-  // where `mine` is false) and its half of B.
+  // Loads K-block kb (128 deep) of tile t into the next stage: this CTA's A
+  // rows (zeros where `mine` is false) and its half of B, each one 3-D box.
   auto issue = [&](const Tile& t, int kb, bool mine, bool last) -> bool {
     if (!wait_bounded(&L.empty[stage], phase ^ 1u, abort_flag, a.dev_err)) return false;
-    uint8_t* sA = L.stages + stage * kStageBytes;
-    uint8_t* sB = sA + A_STAGE_BYTES;
+    uint8_t* sA = L.stages + stage * P::kStageBytes;
+    uint8_t* sB = sA + P::kABytes;
     const uint32_t fb_lead = full_lead + 8u * static_cast<uint32_t>(stage);
     if (rank == 0) {
       L.stage_meta[stage] = last ? META_LAST : 0;
-      mbar_arrive_expect_tx(&L.full[stage], 2 * PAIR_STAGE_BYTES);
+      mbar_arrive_expect_tx(&L.full[stage], 2 * P::kStageBytes);
     }
-    const int k0 = kb * BK;
+    const int k0 = kb * P::kBK;
     const int bz = (t.n * a.bn + half) >> 6;  // first 64-column group of this CTA's B half
     if (!mine) {
       tma_load_2d_pair(&a.tmZ, fb_lead, sA, 0, 0);
     } else if (t.kind == KIND_DC) {
       tma_load_3d_pair(&a.tmA, fb_lead, sA, 0, k0, (t.m * BM) >> 6);
     } else {
-      tma_load_2d_pair(&a.tmA2, fb_lead, sA, k0, t.m * BM);
+      tma_load_3d_pair(&a.tmA2, fb_lead, sA, 0, t.m * BM, k0 >> 6);  // two 64-column groups of K
     }
     if (t.kind == KIND_DC) {
       tma_load_3d_pair(&a.tmB, fb_lead, sB, 0, k0, bz);
@@ -763,7 +762,7 @@ __device__ __forceinline__ void producer_loop_grad_pair(const GemmArgs& a, const
     }
     issued_mask |= 1u << stage;
     issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-    if (++stage == kStages) {
+    if (++stage == P::kStages) {
       stage = 0;
       phase ^= 1u;
     }
@@ -794,40 +793,37 @@ __device__ __forceinline__ void producer_loop_grad_pair(const GemmArgs& a, const
       continue;
     }
     const Tile t = grad_pair_tile(a, dm, v >> 2);
-    const int nk = kblocks_of<MODE_GRAD>(a, dm, t);
-    const int kb0 = kblock_begin<MODE_GRAD>(a, t);
+    const int nk = kblocks_of<MODE_GRAD>(a, dm, t);  // 64-deep K-blocks
+    const int j0 = kblock_begin<MODE_GRAD>(a, t) >> 1, jn = (nk + 1) >> 1;  // 128-deep ones
     bool ok = true;
     if (kind == RING_DENSE) {
       release();
-      for (int kb = kb0; ok && kb < nk; ++kb) ok = issue(t, kb, true, kb + 1 == nk);
+      for (int j = j0; ok && j < jn; ++j) ok = issue(t, j, true, j + 1 == jn);
     } else if (kind == RING_BITS) {
-      // the union's kept filter columns, each two K-blocks
       const uint64_t* own = L.ring_own + slot * PAIR_MAP_WORDS;
       const uint64_t* uni = L.ring_uni + slot * PAIR_MAP_WORDS;
       const int last = L.ring_last[slot];
-      const int w0 = kb0 >> 7, wn = ((nk + 1) >> 1) > (kb0 >> 1) ? ((((nk + 1) >> 1) - 1) >> 6) + 1 : w0;
+      const int w0 = j0 >> 6, wn = jn > j0 ? ((jn - 1) >> 6) + 1 : w0;
       for (int w = w0; ok && w < wn; ++w) {
         uint64_t u = uni[w - w0];
         const uint64_t o = own[w - w0];
         while (ok && u) {
           const int i = __ffsll(static_cast<long long>(u)) - 1;
           u &= u - 1;
-          const bool mine = (o >> i) & 1u;
-          const int col = 64 * w + i;
-          const int kb_end = min(2 * col + 2, nk);
-          for (int kb = max(2 * col, kb0); ok && kb < kb_end; ++kb) ok = issue(t, kb, mine, kb == last);
+          const int j = 64 * w + i;
+          ok = issue(t, j, (o >> i) & 1u, j == last);
         }
       }
       release();
     } else {  // RING_WIDE
       release();
       PairKeep pk = pair_keep(a, dm, t, nk);
-      for (int kb = pair_kb(pk); ok && kb < nk;) {
-        const bool mine = pk.on == kb;
-        pair_advance(pk, kb);
+      for (int j = pair_kb(pk); ok && j < jn;) {
+        const bool mine = pk.on == j;
+        pair_advance(pk, j);
         const int next = pair_kb(pk);
-        ok = issue(t, kb, mine, next >= nk);
-        kb = next;
+        ok = issue(t, j, mine, next >= jn);
+        j = next;
       }
     }
     if (!ok) break;
@@ -839,7 +835,7 @@ __device__ __forceinline__ void producer_loop_grad_pair(const GemmArgs& a, const
     while (globaltimer() - t0 < 10000000ull) {
     }
   } else if (*abort_flag) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < P::kStages; ++s) {
       if (issued_mask & (1u << s)) {
         volatile int dummy = 0;
         wait_bounded(&L.full[s], (issued_par >> s) & 1u, &dummy, nullptr);
@@ -855,6 +851,7 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& a, const SmemLayout& L,
   // CTA's MMA thread has nothing to do.
   if (PAIR && cluster_ctarank() != 0) return;
   constexpr int kStages = Pipe<MODE, PAIR>::kStages, kStageBytes = Pipe<MODE, PAIR>::kStageBytes;
+  constexpr int kABytes = Pipe<MODE, PAIR>::kABytes, kBK = Pipe<MODE, PAIR>::kBK;
   volatile int* abort_flag = L.abort_flag;
   int stage = 0;
   uint32_t phase = 0;
@@ -876,8 +873,13 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& a, const SmemLayout& L,
       const bool b_mn = (MODE == MODE_GRAD);
       const int n = (MODE == MODE_GRAD) ? a.bn : BN;
       const uint32_t idesc = idesc_bf16(PAIR ? 2 * BM : BM, n, a_mn, b_mn);
-      const uint32_t a_lbo = a_mn ? 8192u : 16u, b_lbo = b_mn ? 8192u : 16u;
-      const uint64_t a_step = a_mn ? (2048u >> 4) : (32u >> 4);  // one K=16 step, encoded
+      // MN-major: 64-element groups kBK rows apart, a K=16 step is 16 rows;
+      // K-major: a K=16 step is 32 bytes of a 128-byte row, and each 64 of K
+      // is a box of its own (BM rows of A further on)
+      const uint32_t a_lbo = a_mn ? kBK * 128u : 16u, b_lbo = b_mn ? kBK * 128u : 16u;
+      auto a_off = [&](int kk) -> uint64_t {
+        return a_mn ? (2048u >> 4) * kk : ((kk >> 2) * (BM * 128u >> 4) + (kk & 3) * (32u >> 4));
+      };
       const uint64_t b_step = b_mn ? (2048u >> 4) : (32u >> 4);
       if (!wait_bounded(&L.tmem_empty[acc], acc_phase ^ 1u, abort_flag, a.dev_err)) return false;
       tc_fence_after();
@@ -914,15 +916,15 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& a, const SmemLayout& L,
           }
         }
         const uint32_t sA = smem_u32(L.stages + stage * kStageBytes);
-        const uint32_t sB = sA + A_STAGE_BYTES;
+        const uint32_t sB = sA + kABytes;
         const uint64_t adesc = smem_desc_sw128(sA, a_lbo, 1024u);
         const uint64_t bdesc = smem_desc_sw128(sB, b_lbo, 1024u);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
+        for (int kk = 0; kk < kBK / 16; ++kk) {
           if constexpr (PAIR) {
-            mma_bf16_pair(d_tmem, adesc + a_step * kk, bdesc + b_step * kk, idesc, (any || kk > 0) ? 1u : 0u);
+            mma_bf16_pair(d_tmem, adesc + a_off(kk), bdesc + b_step * kk, idesc, (any || kk > 0) ? 1u : 0u);
           } else {
-            mma_bf16(d_tmem, adesc + a_step * kk, bdesc + b_step * kk, idesc, (any || kk > 0) ? 1u : 0u);
+            mma_bf16(d_tmem, adesc + a_off(kk), bdesc + b_step * kk, idesc, (any || kk > 0) ? 1u : 0u);
           }
         }
         any = true;

@@ -25,8 +25,8 @@ constexpr uint32_t PAIR_TMEM_COLS = 512;
 constexpr int PAIR_ACCS = 2;
 constexpr int PAIR_MIN_BLOCKS = 64;  // recompute as CTA pairs from this many 128-row token blocks
 constexpr int RING = 4;  // depth of the work-item ring between the scheduler and the consumers
-// gradient-GEMM pairs: survival words per ring slot (64 filter columns, 128
-// K-blocks each): K ranges up to 1024 K-blocks take the scheduler's words
+// gradient-GEMM pairs: survival words per ring slot (64 filter columns, one
+// 128-deep K-block each): K ranges up to 65536 take the scheduler's words
 constexpr int PAIR_MAP_WORDS = 8;
 // barriers, flags, ring ids, stage tags and the pairs' survival words
 constexpr int BAR_BYTES = 1024;
@@ -42,20 +42,24 @@ constexpr float NEG_BIG = -3.0e38f;  // finite "minus infinity" for the running 
 enum Mode { MODE_FWD = 0, MODE_BWD_G = 1, MODE_GRAD = 2, MODE_FWD_STAGE = 3 };
 enum Kind { KIND_MAIN = 0, KIND_DC = 1, KIND_DE = 2 };
 
-// Pipeline depth and stage size of one CTA.  A CTA of a gradient-GEMM pair
-// holds 32 KiB of operands per K-block (its A rows and half of B) instead of
-// 48, so the same stage memory holds six stages: the pair's stages complete
-// only when both CTAs' copies (mostly G-hat from DRAM) have landed, and the
-// deeper pipeline covers that latency.  (The logit-GEMM pairs keep four
-// stages: six measured no faster for them.)
-constexpr int PAIR_STAGES = STAGES * STAGE_BYTES / PAIR_STAGE_BYTES;  // 6
-constexpr int MAX_STAGES = PAIR_STAGES > STAGES ? PAIR_STAGES : STAGES;
-static_assert(PAIR_STAGES * PAIR_STAGE_BYTES == STAGES * STAGE_BYTES, "pair stages fill the stage memory");
+// Pipeline depth and stage size of one CTA.  The gradient GEMM as CTA pairs
+// runs stages two K-blocks deep (K = 128): a CTA's stage is its 128 A rows and
+// half (128 columns) of B, 64 KiB, three of them in the stage memory.  Its
+// producer then issues one stage per 128 of K, half as often as with 64-deep
+// stages, and the producer's work per stage is what paces the pair.  (The
+// logit-GEMM pairs keep four 48 KiB stages: six measured no faster for them.)
+constexpr int PAIR_BK = 128;
+constexpr int PAIR_GRAD_A_BYTES = BM * PAIR_BK * 2;                     // 32 KiB
+constexpr int PAIR_GRAD_STAGE_BYTES = 2 * PAIR_GRAD_A_BYTES;            // + half of B: 64 KiB
+constexpr int PAIR_GRAD_STAGES = STAGES * STAGE_BYTES / PAIR_GRAD_STAGE_BYTES;  // 3
+constexpr int MAX_STAGES = PAIR_GRAD_STAGES > STAGES ? PAIR_GRAD_STAGES : STAGES;
 template <int MODE, bool PAIR>
 struct Pipe {
   static constexpr bool kDeep = PAIR && MODE == MODE_GRAD;
-  static constexpr int kStages = kDeep ? PAIR_STAGES : STAGES;
-  static constexpr int kStageBytes = kDeep ? PAIR_STAGE_BYTES : STAGE_BYTES;
+  static constexpr int kStages = kDeep ? PAIR_GRAD_STAGES : STAGES;
+  static constexpr int kStageBytes = kDeep ? PAIR_GRAD_STAGE_BYTES : STAGE_BYTES;
+  static constexpr int kABytes = kDeep ? PAIR_GRAD_A_BYTES : A_STAGE_BYTES;
+  static constexpr int kBK = kDeep ? PAIR_BK : BK;
 };
 
 struct GemmArgs {
@@ -70,7 +74,7 @@ struct GemmArgs {
   CUtensorMap tmA2;
   CUtensorMap tmB2;
   CUtensorMap tmOut2;
-  // GRAD as CTA pairs: one A-sized box (16 KiB) of zeros, loaded in place of
+  // GRAD as CTA pairs: one A-sized box (32 KiB) of zeros, loaded in place of
   // a CTA's A operand for a K-block its own tile skips but the other CTA's
   // tile keeps (the pair's MMA walks the union of the two tiles' K-blocks)
   CUtensorMap tmZ;

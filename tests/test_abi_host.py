@@ -71,7 +71,7 @@ def test_workspace_queries(lib, N, D, V):
         assert r["bwd_chunk_cols"] < V
     assert N * r["bwd_chunk_cols"] * 2 <= max(512 << 20, N * 256 * 2)
     compaction = N * (4 + 4 + 8 + 4 + 4) + N * D * 2  # row map + compact x, LSE, grad_out and E
-    zero_box = 128 * 64 * 2  # the A operand a CTA pair's gradient GEMM loads where its own tile skips
+    zero_box = 128 * 128 * 2  # the A operand a CTA pair's gradient GEMM loads where its own tile skips
     assert b <= (N * D * 4 + N * r["bwd_chunk_cols"] * 2 + 2 * (N // 128 + 1) * (V // 128 + 1) + compaction
                  + zero_box + 8192)
     assert f < N * V * 4 or V < 1024
