@@ -30,7 +30,7 @@ constexpr size_t ALIGN = 256;         // sub-buffer alignment inside a workspace
 constexpr size_t G_CHUNK_BUDGET = size_t(CCE_G_CHUNK_BUDGET_MIB) << 20;  // bytes of the backward G chunk buffer
 constexpr int64_t MIN_CHUNK = 2048, MAX_CHUNK = 65536;
 constexpr int COMBINE_THREADS = 256;
-constexpr size_t ZERO_BOX_BYTES = PAIR_GRAD_A_BYTES;  // one A operand box of the pair gradient GEMM
+constexpr size_t ZERO_BOX_BYTES = PAIR_A_BYTES;  // one A operand box of the pair gradient GEMM
 
 std::atomic<uint64_t> g_launches{0};
 
@@ -634,12 +634,14 @@ bool make_tmap_mn3(CUtensorMap* m, const void* ptr, uint64_t D, uint64_t rows, u
   return r == CUDA_SUCCESS;
 }
 
-// CTA pairs (FWD, BWD_G): B = C (or a chunk of sorted C rows,
-// `rows` of them) in 128-row boxes, each CTA's half of a 256-row tile; raster
-// groups hold whole pairs.
-bool pair_operands(GemmArgs* a, const void* C, int64_t D, int64_t rows) {
+// CTA pairs (FWD, BWD_G), whose stages are 128 deep in K: A = E (n rows)
+// in boxes of 128 rows and B = C (or a chunk of sorted C rows, `rows` of
+// them) in 128-row boxes, each CTA's half of a 256-row tile, both as two
+// 64-column K groups in one 3-D box (D % 64 == 0); raster groups hold whole
+// pairs.
+bool pair_operands(GemmArgs* a, const void* E, int64_t n, const void* C, int64_t D, int64_t rows) {
   a->group_n = std::max(2, a->group_n & ~1);
-  return make_tmap(&a->tmB2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, D, rows, D, BK, BN / 2);
+  return make_tmap_mn3(&a->tmA, E, D, n, 2, BM) && make_tmap_mn3(&a->tmB2, C, D, rows, 2, BN / 2);
 }
 
 // ---------------------------------------------------------- phase timing
@@ -882,8 +884,8 @@ static cce_status forward_impl(const void* E, const void* C, const int64_t* x, i
   // Clusters of two CTAs share each MMA (M = 256), each CTA loading its 128
   // rows of E and half of the C tile, so a CTA moves two thirds of the
   // operand bytes per MMA.
-  const bool pairs = pair_clusters > 0;
-  if (pairs && !pair_operands(&a, C, D, V)) return CCE_ERR_CUDA;
+  const bool pairs = pair_clusters > 0 && D % 64 == 0;
+  if (pairs && !pair_operands(&a, Eg, N, C, D, V)) return CCE_ERR_CUDA;
   const int units = pairs ? ((a.n_blocks + 1) / 2) * a.splits : a.n_blocks * a.splits;
   a.items = units;
   {
@@ -1088,8 +1090,8 @@ cce_status cce_backward_ex2(const void* E, const void* C, const int64_t* x, cons
   // odd number of compacted blocks the last pair runs half empty; at 32
   // blocks (the Qwen shape) that cost more than the pairs saved (0.737 ->
   // 0.777 ms), at 64 and 128 blocks the pairs won (Llama: 9.85 -> 9.48 ms).
-  const bool pairs = pair_clusters > 0 && cdiv(N, BM) >= PAIR_MIN_BLOCKS;
-  if (pairs && !pair_operands(&g, Cg, D, c_rows)) return CCE_ERR_CUDA;
+  const bool pairs = pair_clusters > 0 && cdiv(N, BM) >= PAIR_MIN_BLOCKS && D % 64 == 0;
+  if (pairs && !pair_operands(&g, Ec, N, Cg, D, c_rows)) return CCE_ERR_CUDA;
   r.bn = grad_tile_width(D, r.b3d ? 64 : 32);
   r.n_tiles = static_cast<int>(cdiv(D, r.bn));
   // The gradient GEMM as CTA pairs (M = 256, each CTA loading its own 128 A

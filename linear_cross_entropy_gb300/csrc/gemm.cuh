@@ -506,6 +506,7 @@ __device__ __forceinline__ void prefetch_next_b(const GemmArgs& a, const Dims& d
 // ---------------------------------------------------------------- producer
 template <int MODE, bool PAIR = false>
 __device__ __forceinline__ void producer_loop(const GemmArgs& a, const SmemLayout& L) {
+  using P = Pipe<MODE, PAIR>;
   volatile int* abort_flag = L.abort_flag;
   int stage = 0;
   uint32_t phase = 0;
@@ -536,7 +537,8 @@ __device__ __forceinline__ void producer_loop(const GemmArgs& a, const SmemLayou
     if (item < 0) break;
     if (kAhead) next = atomicAdd(a.counter, 1);
     const bool ok = for_each_tile_of_item<MODE, PAIR>(a, dm, item, [&](const Tile& t) -> bool {
-      const int nk = kblocks_of<MODE>(a, dm, t);
+      // pairs: K-blocks 128 deep
+      const int nk = PAIR ? (kblocks_of<MODE>(a, dm, t) + 1) >> 1 : kblocks_of<MODE>(a, dm, t);
       if (MODE == MODE_FWD_STAGE) prefetch_next_b(a, dm, t);
       int kb = next_kblock<MODE>(a, t, kblock_begin<MODE>(a, t), nk);
       if (MODE == MODE_GRAD && kb >= nk) {  // nothing survives the filter: an empty tagged stage
@@ -546,7 +548,7 @@ __device__ __forceinline__ void producer_loop(const GemmArgs& a, const SmemLayou
         // tracked like a copy, so the abort drain below waits on this stage's latest phase
         issued_mask |= 1u << stage;
         issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-        if (++stage == STAGES) {
+        if (++stage == P::kStages) {
           stage = 0;
           phase ^= 1u;
         }
@@ -556,16 +558,17 @@ __device__ __forceinline__ void producer_loop(const GemmArgs& a, const SmemLayou
         const int next = next_kblock<MODE>(a, t, kb + 1, nk);
         if (!wait_bounded(&L.empty[stage], phase ^ 1u, abort_flag, a.dev_err)) return false;
         if (MODE == MODE_GRAD) L.stage_meta[stage] = next >= nk ? META_LAST : 0;
-        uint8_t* sA = L.stages + stage * STAGE_BYTES;
-        uint8_t* sB = sA + A_STAGE_BYTES;
+        uint8_t* sA = L.stages + stage * P::kStageBytes;
+        uint8_t* sB = sA + P::kABytes;
         uint64_t* fb = &L.full[stage];
-        const int k0 = kb * BK;
+        const int k0 = kb * P::kBK;
         if constexpr (PAIR) {
-          // this CTA's 128 rows of A and its half (128 rows) of the B tile
+          // this CTA's 128 rows of A and its half (128 rows) of the B tile,
+          // each one 3-D box of two 64-column K groups
           const uint32_t fb_lead = mapa_shared(smem_u32(fb), 0);
-          if (rank == 0) mbar_arrive_expect_tx(fb, 2 * PAIR_STAGE_BYTES);
-          tma_load_2d_pair(&a.tmA, fb_lead, sA, k0, t.m * BM);
-          tma_load_2d_pair(&a.tmB2, fb_lead, sB, k0, a.c_row0 + t.n * BN + static_cast<int>(rank) * (BN / 2));
+          if (rank == 0) mbar_arrive_expect_tx(fb, 2 * P::kStageBytes);
+          tma_load_3d_pair(&a.tmA, fb_lead, sA, 0, t.m * BM, k0 >> 6);
+          tma_load_3d_pair(&a.tmB2, fb_lead, sB, 0, a.c_row0 + t.n * BN + static_cast<int>(rank) * (BN / 2), k0 >> 6);
         } else if (MODE != MODE_GRAD) {
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
           tma_load_2d(&a.tmA, fb, sA, k0, t.m * BM);
@@ -590,7 +593,7 @@ __device__ __forceinline__ void producer_loop(const GemmArgs& a, const SmemLayou
         }
         issued_mask |= 1u << stage;
         issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-        if (++stage == STAGES) {
+        if (++stage == P::kStages) {
           stage = 0;
           phase ^= 1u;
         }
@@ -608,7 +611,7 @@ __device__ __forceinline__ void producer_loop(const GemmArgs& a, const SmemLayou
     }
   } else if (*abort_flag) {
     // Let every copy this thread issued land before the CTA exits.
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < P::kStages; ++s) {
       if (issued_mask & (1u << s)) {
         volatile int dummy = 0;
         wait_bounded(&L.full[s], (issued_par >> s) & 1u, &dummy, nullptr);
@@ -880,7 +883,10 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& a, const SmemLayout& L,
       auto a_off = [&](int kk) -> uint64_t {
         return a_mn ? (2048u >> 4) * kk : ((kk >> 2) * (BM * 128u >> 4) + (kk & 3) * (32u >> 4));
       };
-      const uint64_t b_step = b_mn ? (2048u >> 4) : (32u >> 4);
+      // K-major B: BN rows per 64 of K (a pair's CTA holds 128 of them)
+      auto b_off = [&](int kk) -> uint64_t {
+        return b_mn ? (2048u >> 4) * kk : ((kk >> 2) * ((PAIR ? BN / 2 : BN) * 128u >> 4) + (kk & 3) * (32u >> 4));
+      };
       if (!wait_bounded(&L.tmem_empty[acc], acc_phase ^ 1u, abort_flag, a.dev_err)) return false;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -898,7 +904,7 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& a, const SmemLayout& L,
         }
       }
       // FWD / BWD_G: every K-block; GRAD: the producer's stage tags end the loop
-      const int nk = MODE == MODE_GRAD ? 0 : kblocks_of<MODE>(a, dm, t);
+      const int nk = MODE == MODE_GRAD ? 0 : (PAIR ? (kblocks_of<MODE>(a, dm, t) + 1) >> 1 : kblocks_of<MODE>(a, dm, t));
       for (int kb = 0;; ++kb) {
         if (MODE != MODE_GRAD && kb >= nk) break;
         if (!wait_bounded(&L.full[stage], phase, abort_flag, a.dev_err)) return false;
@@ -922,9 +928,9 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& a, const SmemLayout& L,
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
           if constexpr (PAIR) {
-            mma_bf16_pair(d_tmem, adesc + a_off(kk), bdesc + b_step * kk, idesc, (any || kk > 0) ? 1u : 0u);
+            mma_bf16_pair(d_tmem, adesc + a_off(kk), bdesc + b_off(kk), idesc, (any || kk > 0) ? 1u : 0u);
           } else {
-            mma_bf16(d_tmem, adesc + a_off(kk), bdesc + b_step * kk, idesc, (any || kk > 0) ? 1u : 0u);
+            mma_bf16(d_tmem, adesc + a_off(kk), bdesc + b_off(kk), idesc, (any || kk > 0) ? 1u : 0u);
           }
         }
         any = true;

@@ -13,7 +13,6 @@ constexpr int STAGES = 4;
 constexpr int A_STAGE_BYTES = BM * BK * 2;                  // 16 KiB
 constexpr int B_STAGE_BYTES = BN * BK * 2;                  // 32 KiB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;  // 48 KiB
-constexpr int PAIR_STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES / 2;  // one CTA of a pair: A + half of B
 constexpr int NUM_EPI_WARPS = 4;
 constexpr int EPI_WARP_BYTES = 8192;
 // warps: 0 producer, 1 MMA, 2-5 epilogue, 6 scheduler (gradient-GEMM pairs;
@@ -42,24 +41,23 @@ constexpr float NEG_BIG = -3.0e38f;  // finite "minus infinity" for the running 
 enum Mode { MODE_FWD = 0, MODE_BWD_G = 1, MODE_GRAD = 2, MODE_FWD_STAGE = 3 };
 enum Kind { KIND_MAIN = 0, KIND_DC = 1, KIND_DE = 2 };
 
-// Pipeline depth and stage size of one CTA.  The gradient GEMM as CTA pairs
-// runs stages two K-blocks deep (K = 128): a CTA's stage is its 128 A rows and
-// half (128 columns) of B, 64 KiB, three of them in the stage memory.  Its
+// Pipeline depth and stage size of one CTA.  CTA pairs run stages two
+// K-blocks deep (K = 128): a CTA's stage is its 128 A rows and half (128
+// rows or columns) of B, 64 KiB, three of them in the stage memory.  The
 // producer then issues one stage per 128 of K, half as often as with 64-deep
-// stages, and the producer's work per stage is what paces the pair.  (The
-// logit-GEMM pairs keep four 48 KiB stages: six measured no faster for them.)
+// stages; in the gradient GEMM the producer's work per stage is what paces
+// the pair.
 constexpr int PAIR_BK = 128;
-constexpr int PAIR_GRAD_A_BYTES = BM * PAIR_BK * 2;                     // 32 KiB
-constexpr int PAIR_GRAD_STAGE_BYTES = 2 * PAIR_GRAD_A_BYTES;            // + half of B: 64 KiB
-constexpr int PAIR_GRAD_STAGES = STAGES * STAGE_BYTES / PAIR_GRAD_STAGE_BYTES;  // 3
-constexpr int MAX_STAGES = PAIR_GRAD_STAGES > STAGES ? PAIR_GRAD_STAGES : STAGES;
+constexpr int PAIR_A_BYTES = BM * PAIR_BK * 2;                        // 32 KiB
+constexpr int PAIR_STAGE_BYTES = 2 * PAIR_A_BYTES;                    // + half of B: 64 KiB
+constexpr int PAIR_STAGES = STAGES * STAGE_BYTES / PAIR_STAGE_BYTES;  // 3
+constexpr int MAX_STAGES = PAIR_STAGES > STAGES ? PAIR_STAGES : STAGES;
 template <int MODE, bool PAIR>
 struct Pipe {
-  static constexpr bool kDeep = PAIR && MODE == MODE_GRAD;
-  static constexpr int kStages = kDeep ? PAIR_GRAD_STAGES : STAGES;
-  static constexpr int kStageBytes = kDeep ? PAIR_GRAD_STAGE_BYTES : STAGE_BYTES;
-  static constexpr int kABytes = kDeep ? PAIR_GRAD_A_BYTES : A_STAGE_BYTES;
-  static constexpr int kBK = kDeep ? PAIR_BK : BK;
+  static constexpr int kStages = PAIR ? PAIR_STAGES : STAGES;
+  static constexpr int kStageBytes = PAIR ? PAIR_STAGE_BYTES : STAGE_BYTES;
+  static constexpr int kABytes = PAIR ? PAIR_A_BYTES : A_STAGE_BYTES;
+  static constexpr int kBK = PAIR ? PAIR_BK : BK;
 };
 
 struct GemmArgs {
