@@ -365,8 +365,8 @@ cce_status cce_memory_accounting(int64_t N, int64_t D, int64_t V, cce_memory_rep
 cce_status cce_selftest_wait_timeout(int32_t* dev_err, uint32_t timeout_us, void* stream);
 
 /* Self-test of the abort path between the two CTAs of a CTA pair (the
- * forward and recompute GEMMs run as clusters of two CTAs whose waits depend
- * on each other).  Launches one cluster of two CTAs running the pair's
+ * forward, recompute and gradient GEMMs run as clusters of two CTAs whose
+ * waits depend on each other).  Launches one cluster of two CTAs running the pair's
  * handshake: the odd CTA arrives on a barrier of the even CTA, which answers
  * on a barrier of the odd CTA.  With hold = 1 the odd CTA holds its arrive
  * back: the even CTA's bounded wait runs out after timeout_us (1 .. 10^7)
@@ -377,6 +377,16 @@ cce_status cce_selftest_wait_timeout(int32_t* dev_err, uint32_t timeout_us, void
  * left alone.  No fault, no hang: the context stays usable.  Other hold
  * values return CCE_ERR_ARG.  Asynchronous on `stream`. */
 cce_status cce_selftest_pair_timeout(int32_t* dev_err, uint32_t timeout_us, int hold, void* stream);
+
+/* Test hook of the gradient GEMM as CTA pairs.  A work item carries the
+ * survival map of its K range as 64-bit words (one bit per 128 x 128 filter
+ * tile), at most 40; a longer K range (more than 327,680 rows taking part in
+ * a dC tile) is walked on the maps by the TMA producer instead.  This sets
+ * the most words an item may carry to `words` (1 .. 40; any other value
+ * restores 40) for the calls that start after it, so tests reach the long
+ * path at small sizes, and returns the previous setting.  Process-wide; not
+ * meant for production use.  No device work. */
+int cce_selftest_pair_map_words(int words);
 
 /* Human-readable name of a status. */
 const char* cce_status_string(cce_status s);

@@ -33,6 +33,8 @@ constexpr int COMBINE_THREADS = 256;
 constexpr size_t ZERO_BOX_BYTES = PAIR_A_BYTES;  // one A operand box of the pair gradient GEMM
 
 std::atomic<uint64_t> g_launches{0};
+// survival words a gradient-GEMM pair's work item carries (a test hook lowers it)
+std::atomic<int> g_pair_words{PAIR_MAP_WORDS};
 
 // ------------------------------------------------------------ small kernels
 // Per row: LSE from the per-split partials (fixed split order), loss, and a
@@ -484,8 +486,8 @@ BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V, bool sort = false, size_t 
 constexpr size_t FLCE_STAGING_DEFAULT = size_t(2) << 30;
 
 struct FlceLayout {
-  size_t counters, count, cscr, pos, ridx, xc, ec, part_m, part_s, tgt, lse, blk_sum, blk_cnt, stage, mtile, bitmap,
-      bitmapT, deacc, dcacc, total;
+  size_t counters, count, zero, cscr, pos, ridx, xc, ec, part_m, part_s, tgt, lse, blk_sum, blk_cnt, stage, mtile,
+      bitmap, bitmapT, deacc, dcacc, total;
   int64_t Nc, nchunks, Vp, bm_ld, slab, n_tiles, bn, kps;
   int S, Sde, nblk;
 };
@@ -519,6 +521,7 @@ FlceLayout flce_layout(int64_t N, int64_t D, int64_t V, size_t max_staging) {
   };
   L.counters = take(sizeof(int) * 2 * static_cast<size_t>(L.nchunks));
   L.count = take(sizeof(int));
+  L.zero = take(ZERO_BOX_BYTES);  // the A box of a CTA pair's skipped K-block
   L.cscr = take(compact_scratch_bytes(N));
   L.pos = take(sizeof(int) * static_cast<size_t>(N));
   L.ridx = take(sizeof(int) * static_cast<size_t>(N));
@@ -1106,6 +1109,7 @@ cce_status cce_backward_ex2(const void* E, const void* C, const int64_t* x, cons
     ok &= make_tmap_mn3(&r.tmB2, Cg, D, c_rows, 2, PAIR_BK);
     ok &= make_tmap(&r.tmZ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws + W.zero, 64, 2 * BM, 64, 64, 2 * BM);
     if (!ok) return CCE_ERR_CUDA;
+    r.pair_words = g_pair_words.load();
     cudaError_t e = cudaMemsetAsync(ws + W.zero, 0, ZERO_BOX_BYTES, s);
     if (e != cudaSuccess) return cuda_status(e);
   }
@@ -1199,8 +1203,8 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
   if (!(softcap >= 0.0f) || !std::isfinite(softcap)) return CCE_ERR_ARG;
   const FlceLayout W = flce_layout(N, D, V, max_staging_bytes);
   if (ws_bytes < W.total) return CCE_ERR_WORKSPACE;
-  int sms = 0;
-  cce_status st = device_check(&sms);
+  int sms = 0, pair_clusters = 0;
+  cce_status st = device_check(&sms, &pair_clusters);
   if (st != CCE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -1242,6 +1246,13 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
     if (e != cudaSuccess) return cuda_status(e);
   }
   const bool b3d = D % 64 == 0;
+  // The gradient GEMM as CTA pairs, as in the two-call backward (D tiles 256
+  // wide, 3-D boxes; the dE K ranges start at multiples of 128).
+  const bool grad_pairs = pair_clusters > 0 && b3d && W.bn == BN && W.kps % 2 == 0;
+  if (grad_pairs) {
+    cudaError_t e = cudaMemsetAsync(ws + W.zero, 0, ZERO_BOX_BYTES, s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
   // Chunks cover compact rows r0 .. r0 + Nc - 1; how many compact rows exist
   // is only known on the device, so every launch reads the count and a chunk
   // past it does nothing (its dC contribution is zero).
@@ -1329,6 +1340,12 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
     }
     ok = ok && make_tmap(&r.tmOut2, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, deacc, D,
                          static_cast<uint64_t>(W.Sde) * W.slab, D, 32, 32);
+    if (grad_pairs) {  // every operand one 3-D box of two 64-column groups and 128 rows
+      ok = ok && make_tmap_mn3(&r.tmA, stage, W.Vp, rows, 2, PAIR_BK) && make_tmap_mn3(&r.tmA2, stage, W.Vp, rows, 2, BM) &&
+           make_tmap_mn3(&r.tmB, Ec, D, rows, 2, PAIR_BK) && make_tmap_mn3(&r.tmB2, C, D, V, 2, PAIR_BK) &&
+           make_tmap(&r.tmZ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ws + W.zero, 64, 2 * BM, 64, 64, 2 * BM);
+      r.pair_words = g_pair_words.load();
+    }
     if (!ok) return CCE_ERR_CUDA;
     r.N = static_cast<int>(rows);
     r.D = static_cast<int>(D);
@@ -1364,8 +1381,13 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
     r.counter = counters + 2 * c + 1;
     {
       PhaseScope ps(4, s);
-      const int64_t items = (r.dc_m_tiles + nb * W.Sde) * r.n_tiles;
-      e = launch_gemm(MODE_GRAD, r, static_cast<int>(std::min<int64_t>(sms, items)), s);
+      if (grad_pairs) {
+        const int64_t items = ((r.dc_m_tiles + 1) / 2 + (nb + 1) / 2 * W.Sde) * r.n_tiles;
+        e = launch_gemm_pairs(MODE_GRAD, r, static_cast<int>(std::min<int64_t>(pair_clusters, items)), s);
+      } else {
+        const int64_t items = (r.dc_m_tiles + nb * W.Sde) * r.n_tiles;
+        e = launch_gemm(MODE_GRAD, r, static_cast<int>(std::min<int64_t>(sms, items)), s);
+      }
       g_launches++;
       if (e != cudaSuccess) return cuda_status(e);
     }
@@ -1429,6 +1451,11 @@ cce_status cce_selftest_pair_timeout(int32_t* dev_err, uint32_t timeout_us, int 
                                                static_cast<cudaStream_t>(stream));
   g_launches++;
   return cuda_status(e);
+}
+
+int cce_selftest_pair_map_words(int words) {
+  if (words <= 0 || words > PAIR_MAP_WORDS) words = PAIR_MAP_WORDS;
+  return g_pair_words.exchange(words);
 }
 
 cce_status cce_profile_enable(int enable) {

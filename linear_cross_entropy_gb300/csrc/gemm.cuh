@@ -321,6 +321,9 @@ __device__ __forceinline__ int keep_next(KeepCursor& c, int j) {
 
 // Warp-wide: does the output tile have no surviving K-block at all?
 __device__ __forceinline__ bool tile_empty(const GemmArgs& a, const Dims& dm, const Tile& t) {
+  // no K-block at all (no row of a dC tile's chunk takes part): the MMA thread
+  // never wrote the accumulator
+  if (kblocks_of<MODE_GRAD>(a, dm, t) <= kblock_begin<MODE_GRAD>(a, t)) return true;
   if (!(t.kind == KIND_DC ? a.filter_dc : a.filter_de)) return false;  // this output is not filtered
   int any = 0;
   if (t.kind == KIND_DC) {
@@ -405,11 +408,13 @@ struct SmemLayout {
   int* flags;       // [2 parity][2 half][4 warps]
   int* ring_ids;    // [RING]
   int* stage_meta;  // [MAX_STAGES] what the producer put in the stage (META_*)
-  // gradient-GEMM pairs: per ring slot, this CTA's own survival words, the
-  // union's, and the union's last (128-deep) K-block
-  uint64_t* ring_own;  // [RING][PAIR_MAP_WORDS]
-  uint64_t* ring_uni;  // [RING][PAIR_MAP_WORDS]
-  int* ring_last;      // [RING]
+  // gradient-GEMM pairs: per word slot, this CTA's own survival words, the
+  // union's, and the union's last (128-deep) K-block; the even CTA's
+  // words_free[s] counts both producers' releases of slot s
+  uint64_t* ring_own;  // [WORD_SLOTS][PAIR_MAP_WORDS]
+  uint64_t* ring_uni;  // [WORD_SLOTS][PAIR_MAP_WORDS]
+  int* ring_last;      // [WORD_SLOTS]
+  uint64_t* words_free;  // [WORD_SLOTS]
   // CTA pairs: cluster address of the even CTA's tmem_empty[0] (0: no pair)
   uint32_t tmem_empty_lead;
 };
@@ -434,7 +439,8 @@ __device__ __forceinline__ SmemLayout carve_smem(uint8_t* raw) {
   L.drain = L.vote + 2;                   // 1
   L.ring_full = L.drain + 1;              // RING
   L.ring_empty = L.ring_full + RING;      // RING
-  uint8_t* tail = reinterpret_cast<uint8_t*>(L.ring_empty + RING);
+  L.words_free = L.ring_empty + RING;     // WORD_SLOTS
+  uint8_t* tail = reinterpret_cast<uint8_t*>(L.words_free + WORD_SLOTS);
   L.tmem_base = reinterpret_cast<uint32_t*>(tail);
   L.abort_flag = reinterpret_cast<int*>(tail + 4);
   L.flags = reinterpret_cast<int*>(tail + 8);      // 16 ints
@@ -442,9 +448,10 @@ __device__ __forceinline__ SmemLayout carve_smem(uint8_t* raw) {
   L.stage_meta = reinterpret_cast<int*>(tail + 72 + 4 * RING);  // MAX_STAGES ints
   constexpr int kWords = 72 + 4 * RING + 4 * MAX_STAGES;
   L.ring_own = reinterpret_cast<uint64_t*>(tail + ((kWords + 7) & ~7));
-  L.ring_uni = L.ring_own + RING * PAIR_MAP_WORDS;
-  L.ring_last = reinterpret_cast<int*>(L.ring_uni + RING * PAIR_MAP_WORDS);
-  static_assert(8 * (2 * MAX_STAGES + 7 + 2 * RING) + ((kWords + 7) & ~7) + 16 * RING * PAIR_MAP_WORDS + 4 * RING <=
+  L.ring_uni = L.ring_own + WORD_SLOTS * PAIR_MAP_WORDS;
+  L.ring_last = reinterpret_cast<int*>(L.ring_uni + WORD_SLOTS * PAIR_MAP_WORDS);
+  static_assert(8 * (2 * MAX_STAGES + 7 + 2 * RING + WORD_SLOTS) + ((kWords + 7) & ~7) +
+                        16 * WORD_SLOTS * PAIR_MAP_WORDS + 4 * WORD_SLOTS <=
                     BAR_BYTES,
                 "barriers and ring data fit their region");
   L.tmem_empty_lead = 0;
@@ -635,7 +642,7 @@ __device__ __forceinline__ Tile grad_pair_tile(const GemmArgs& a, const Dims& dm
 // both keep every K-block of the range; RING_BITS, the slot's survival words
 // say which K-blocks (one per filter column) the pair runs (their union) and
 // which of them this CTA's own tile keeps; RING_WIDE, a K range of more than
-// PAIR_MAP_WORDS words, which the producer walks on the maps itself.
+// a.pair_words words, which the producer walks on the maps itself.
 constexpr int RING_BITS = 0, RING_NONE = 1, RING_DENSE = 2, RING_WIDE = 3;
 
 // One word of a tile's survival map: bit i for filter column 64 w + i, kept
@@ -672,6 +679,11 @@ __device__ __forceinline__ void scheduler_loop_grad_pair(const GemmArgs& a, cons
     if (!wait_bounded<true>(&L.ring_empty[slot], static_cast<uint32_t>(((k / RING) & 1) ^ 1), abort_flag,
                             a.dev_err))
       break;
+    // both producers are done with the word slot's previous item
+    const int ws = k % WORD_SLOTS;
+    if (!wait_bounded<true>(&L.words_free[ws], static_cast<uint32_t>(((k / WORD_SLOTS) & 1) ^ 1), abort_flag,
+                            a.dev_err))
+      break;
     const int item = atomicAdd(a.counter, 1);
     int v = -1;
     if (item < dm.items) {
@@ -685,11 +697,11 @@ __device__ __forceinline__ void scheduler_loop_grad_pair(const GemmArgs& a, cons
       const int jn = oc.jn;
       const int w0 = j0 >> 6, wn = jn > j0 ? ((jn - 1) >> 6) + 1 : w0;
       int kind = RING_WIDE;
-      if (wn - w0 <= PAIR_MAP_WORDS) {
+      if (wn - w0 <= a.pair_words) {
         bool any = false, dense = peer_live;
         int last = -1;
-        uint64_t* own = L.ring_own + slot * PAIR_MAP_WORDS;
-        uint64_t* uni = L.ring_uni + slot * PAIR_MAP_WORDS;
+        uint64_t* own = L.ring_own + ws * PAIR_MAP_WORDS;
+        uint64_t* uni = L.ring_uni + ws * PAIR_MAP_WORDS;
         const uint32_t own_odd = mapa_shared(smem_u32(own), 1), uni_odd = mapa_shared(smem_u32(uni), 1);
         for (int w = w0; w < wn; ++w) {
           const uint64_t ob = keep_word(oc, true, w, j0);
@@ -709,8 +721,8 @@ __device__ __forceinline__ void scheduler_loop_grad_pair(const GemmArgs& a, cons
           st_shared_cluster_u64(uni_odd + 8u * static_cast<uint32_t>(w - w0), ub);
         }
         kind = !any ? RING_NONE : (dense ? RING_DENSE : RING_BITS);
-        L.ring_last[slot] = last;
-        st_shared_cluster_u32(mapa_shared(smem_u32(&L.ring_last[slot]), 1), static_cast<uint32_t>(last));
+        L.ring_last[ws] = last;
+        st_shared_cluster_u32(mapa_shared(smem_u32(&L.ring_last[ws]), 1), static_cast<uint32_t>(last));
       }
       v = 4 * item + kind;
     }
@@ -723,11 +735,11 @@ __device__ __forceinline__ void scheduler_loop_grad_pair(const GemmArgs& a, cons
 }
 
 // Producer of the gradient GEMM as CTA pairs (both CTAs).  Each CTA loads its
-// 128 rows of A (or 16 KiB of zeros where its own tile skips a K-block the
+// 128 rows of A (or 32 KiB of zeros where its own tile skips a K-block the
 // other tile keeps) and its half (128 columns) of the MN-major B tile, all
 // completing on the even CTA's full barrier, whose MMA thread issues one
-// M = 256 MMA for both.  The producer holds its ring slot (and reads the
-// slot's survival words) until the tile's loads are issued.
+// M = 256 MMA for both.  The producer holds the item's word slot (and reads
+// its survival words) until the tile's loads are issued.
 __device__ __forceinline__ void producer_loop_grad_pair(const GemmArgs& a, const SmemLayout& L) {
   using P = Pipe<MODE_GRAD, true>;
   volatile int* abort_flag = L.abort_flag;
@@ -776,11 +788,18 @@ __device__ __forceinline__ void producer_loop_grad_pair(const GemmArgs& a, const
     if (!wait_bounded<true>(&L.ring_full[slot], static_cast<uint32_t>((k / RING) & 1), abort_flag, a.dev_err))
       break;
     const int v = *reinterpret_cast<volatile int*>(&L.ring_ids[slot]);
-    auto release = [&] {
+    if (rank == 0) {
+      mbar_arrive(&L.ring_empty[slot]);
+    } else {
+      mbar_arrive_cluster(mapa_shared(smem_u32(&L.ring_empty[slot]), 0));
+    }
+    if (v < 0) break;
+    const int ws = k % WORD_SLOTS;
+    auto free_words = [&] {  // this producer is done with the item's survival words
       if (rank == 0) {
-        mbar_arrive(&L.ring_empty[slot]);
+        mbar_arrive(&L.words_free[ws]);
       } else {
-        mbar_arrive_cluster(mapa_shared(smem_u32(&L.ring_empty[slot]), 0));
+        mbar_arrive_cluster(mapa_shared(smem_u32(&L.words_free[ws]), 0));
       }
     };
     const int kind = v & 3;
@@ -790,9 +809,8 @@ __device__ __forceinline__ void producer_loop_grad_pair(const GemmArgs& a, const
     // twice before this CTA waits on it: only the odd CTA's copies, which
     // complete on the even CTA's full barrier, keep the two CTAs' stage
     // phases in step.)
-    if (v < 0 || kind == RING_NONE) {
-      release();
-      if (v < 0) break;
+    if (kind == RING_NONE) {
+      free_words();
       continue;
     }
     const Tile t = grad_pair_tile(a, dm, v >> 2);
@@ -800,12 +818,12 @@ __device__ __forceinline__ void producer_loop_grad_pair(const GemmArgs& a, const
     const int j0 = kblock_begin<MODE_GRAD>(a, t) >> 1, jn = (nk + 1) >> 1;  // 128-deep ones
     bool ok = true;
     if (kind == RING_DENSE) {
-      release();
+      free_words();
       for (int j = j0; ok && j < jn; ++j) ok = issue(t, j, true, j + 1 == jn);
     } else if (kind == RING_BITS) {
-      const uint64_t* own = L.ring_own + slot * PAIR_MAP_WORDS;
-      const uint64_t* uni = L.ring_uni + slot * PAIR_MAP_WORDS;
-      const int last = L.ring_last[slot];
+      const uint64_t* own = L.ring_own + ws * PAIR_MAP_WORDS;
+      const uint64_t* uni = L.ring_uni + ws * PAIR_MAP_WORDS;
+      const int last = L.ring_last[ws];
       const int w0 = j0 >> 6, wn = jn > j0 ? ((jn - 1) >> 6) + 1 : w0;
       for (int w = w0; ok && w < wn; ++w) {
         uint64_t u = uni[w - w0];
@@ -817,9 +835,9 @@ __device__ __forceinline__ void producer_loop_grad_pair(const GemmArgs& a, const
           ok = issue(t, j, (o >> i) & 1u, j == last);
         }
       }
-      release();
+      free_words();
     } else {  // RING_WIDE
-      release();
+      free_words();
       PairKeep pk = pair_keep(a, dm, t, nk);
       for (int j = pair_kb(pk); ok && j < jn;) {
         const bool mine = pk.on == j;
@@ -1547,6 +1565,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) cce_gemm_kernel(const __grid_c
       mbar_init(&L.ring_empty[i],
                 (PAIR && MODE == MODE_GRAD) ? 2 * (1 + NUM_EPI_WARPS) + 1 : (lead ? 1 : 0) + NUM_EPI_WARPS);
     }
+    for (int i = 0; i < WORD_SLOTS; ++i) mbar_init(&L.words_free[i], 2);  // both producers of a pair
     mbar_init(L.drain, 1);
     *L.abort_flag = 0;
     fence_mbar_init();

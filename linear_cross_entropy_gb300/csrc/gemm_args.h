@@ -24,11 +24,13 @@ constexpr uint32_t PAIR_TMEM_COLS = 512;
 constexpr int PAIR_ACCS = 2;
 constexpr int PAIR_MIN_BLOCKS = 64;  // recompute as CTA pairs from this many 128-row token blocks
 constexpr int RING = 4;  // depth of the work-item ring between the scheduler and the consumers
-// gradient-GEMM pairs: survival words per ring slot (64 filter columns, one
-// 128-deep K-block each): K ranges up to 65536 take the scheduler's words
-constexpr int PAIR_MAP_WORDS = 8;
+// gradient-GEMM pairs: survival words of an item (64 filter columns, one
+// 128-deep K-block each) in WORD_SLOTS slots: K ranges up to 2560 K-blocks
+// (327,680 tokens or vocabulary entries) take the scheduler's words
+constexpr int PAIR_MAP_WORDS = 40;
+constexpr int WORD_SLOTS = 2;
 // barriers, flags, ring ids, stage tags and the pairs' survival words
-constexpr int BAR_BYTES = 1024;
+constexpr int BAR_BYTES = 1792;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_EPI_WARPS * EPI_WARP_BYTES + BAR_BYTES;
 constexpr int FILTER_TILE = 128;  // filter decisions are per 128 tokens x 128 vocab
 
@@ -98,6 +100,7 @@ struct GemmArgs {
   int dc_k_blocks;  // ceil(N / 64)
   int de_k_blocks;  // ceil(chunk_w / 64)
   int dc_first;     // 1: dC tiles are handed out first (they have the longer K)
+  int pair_words;   // GRAD pairs: survival words a work item may carry (1 .. PAIR_MAP_WORDS)
   int first_chunk;  // dE: store (1) or reduce-add (0)
   // dynamic scheduling: work items are handed out by atomicAdd on *counter
   int* counter;     // zeroed before the launch

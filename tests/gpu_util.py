@@ -132,3 +132,23 @@ def make(name_or_w, **kw):
     if kw:
         w = w.with_(**kw)
     return w, W.make_inputs(w)
+
+
+def mixed_survival_inputs(N, D=256, V=1500, seed=5):
+    """Frequent-token inputs (128 frequent ids: vocabulary block 0) whose
+    token blocks differ in what the filter keeps: every third 128-row block
+    has its hidden states scaled by 0.01 (a near-uniform softmax: every tile
+    kept), the others point at their target's classifier row (0.35 C_x: the
+    target takes over 99% of the mass, so only vocabulary block 0 is kept)."""
+    E, C, x = W.frequent_token_inputs(N, D, V, n_freq=128, seed=seed)
+    Ef = W.bf16_bits_to_f32(E).astype(np.float32)
+    Cf = W.bf16_bits_to_f32(C).astype(np.float32)
+    for b in range((N + 127) // 128):
+        r = slice(b * 128, min(N, (b + 1) * 128))
+        if b % 3 == 0:
+            Ef[r] *= np.float32(0.01)
+        else:
+            t = x[r]
+            live = t != O.IGNORE_INDEX
+            Ef[r][live] = np.float32(0.35) * Cf[t[live]]
+    return W.f32_to_bf16_bits(Ef), C, x

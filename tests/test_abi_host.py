@@ -199,3 +199,18 @@ def test_extended_entry_points_reject_bad_options(lib):
     assert lib.cce_backward_ex(*bargs, 0.0, 2.0 ** -12, 8, *tail) == 4      # unknown flag bit
     assert lib.cce_backward_ex(*bargs, 0.0, 2.0 ** -12, 4 | 16, *tail) == 4  # sort plus an unknown bit
     assert lib.cce_backward_ex(*bargs, -3.0, 2.0 ** -12, 3, *tail) == 4     # negative softcap
+
+
+def test_pair_map_words_hook(lib):
+    """The test hook that caps the survival words of a gradient-GEMM pair's
+    work item: returns the previous cap, and out-of-range values restore the
+    default of 40 (host only, no device work)."""
+    prev = lib.cce_selftest_pair_map_words(3)
+    try:
+        assert prev == 40
+        assert lib.cce_selftest_pair_map_words(0) == 3
+        assert lib.cce_selftest_pair_map_words(41) == 40
+        assert lib.cce_selftest_pair_map_words(-5) == 40
+    finally:
+        lib.cce_selftest_pair_map_words(prev)
+    assert lib.cce_selftest_pair_map_words(0) == 40

@@ -11,8 +11,8 @@ import torch
 import cce_workloads as W
 import oracle as O
 from tests.gpu_util import (TOL_GRAD, TOL_GRAD_FILTERED, TOL_LSE, TOL_ROW, assert_forward_close,
-                            assert_grads_close, bf16_to_f64, make, oracle_full, rel_fro, row_max_rel, run_cuda,
-                            to_device)
+                            assert_grads_close, bf16_to_f64, make, mixed_survival_inputs, oracle_full, rel_fro,
+                            row_max_rel, run_cuda, to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -123,42 +123,29 @@ def test_filter_matches_filtered_oracle(D):
         assert np.all(got["dC"][b * 128:(b + 1) * 128] == 0.0)
 
 
-def _mixed_survival_inputs(N, D=256, V=1500, seed=5):
-    """Frequent-token inputs (128 frequent ids: vocabulary block 0) whose
-    token blocks differ in what the filter keeps: every third 128-row block
-    has its hidden states scaled by 0.01 (a near-uniform softmax: every tile
-    kept), the others point at their target's classifier row (0.35 C_x: the
-    target takes over 99% of the mass, so only vocabulary block 0 is kept)."""
-    E, C, x = W.frequent_token_inputs(N, D, V, n_freq=128, seed=seed)
-    Ef = W.bf16_bits_to_f32(E).astype(np.float32)
-    Cf = W.bf16_bits_to_f32(C).astype(np.float32)
-    for b in range((N + 127) // 128):
-        r = slice(b * 128, min(N, (b + 1) * 128))
-        if b % 3 == 0:
-            Ef[r] *= np.float32(0.01)
-        else:
-            t = x[r]
-            live = t != O.IGNORE_INDEX
-            Ef[r][live] = np.float32(0.35) * Cf[t[live]]
-    return W.f32_to_bf16_bits(Ef), C, x
-
-
-@pytest.mark.parametrize("N", [3000, 70000])
-def test_neighbouring_blocks_keep_different_k_blocks(N):
+@pytest.mark.parametrize("N,words", [(3000, 0), (20000, 1)])
+def test_neighbouring_blocks_keep_different_k_blocks(N, words):
     """The gradient GEMM as CTA pairs (D = 256: M = 256 over two neighbouring
     row blocks) where the two blocks of a pair keep different K-blocks: the
     pair runs the union, and a CTA loads zeros for a K-block only its partner
     keeps.  Most token-block pairs differ here (dE), and vocabulary blocks 0
     and 1 do (dC: block 0 keeps every token block, block 1 a third of them).
-    N = 70000: more than 65536 rows take part, so a dC tile's K range (the
-    tokens) is longer than the survival words a work item carries, and the
-    producer walks the maps itself.  No tile lies within 0.1% of eps (checked
-    on the oracle), so the skip count must equal the oracle's exactly.  (The
-    skipped tiles' sum is not small against the kept one in this input, so
-    only the filtered oracle is the reference.)"""
+    words = 1: a work item carries one survival word (64 filter columns), so
+    the dC tiles' K range (149 token blocks) is longer than that and the
+    producer walks the maps itself, as it does beyond 327,680 rows.  No tile
+    lies within 0.1% of eps (checked on the oracle), so the skip count must
+    equal the oracle's exactly.  (The skipped tiles' sum is not small against
+    the kept one in this input, so only the filtered oracle is the
+    reference.)"""
+    from linear_cross_entropy_gb300 import _lib
+    lib = _lib.load()
     D, V = 256, 1500
-    E, C, x = _mixed_survival_inputs(N, D, V)
-    got = run_cuda(E, C, x, reduction="mean", filter_eps=O.FILTER_EPS)
+    E, C, x = mixed_survival_inputs(N, D, V)
+    prev = lib.cce_selftest_pair_map_words(words)
+    try:
+        got = run_cuda(E, C, x, reduction="mean", filter_eps=O.FILTER_EPS)
+    finally:
+        lib.cce_selftest_pair_map_words(prev)
     ref = oracle_full(E, C, x, reduction="mean", filter_eps=O.FILTER_EPS)
     Ef, Cf = O.from_bits(E, C)
     w = O.row_weights(x, O.IGNORE_INDEX, "mean", 1.0, int((x != O.IGNORE_INDEX).sum()))
@@ -169,8 +156,8 @@ def test_neighbouring_blocks_keep_different_k_blocks(N):
     nb, nv = keep.shape
     assert sum(not np.array_equal(keep[p], keep[p + 1]) for p in range(0, nb - 1, 2)) > nb // 8
     assert not np.array_equal(keep[:, 0], keep[:, 1])
-    if N > 65536:
-        assert int((x != O.IGNORE_INDEX).sum()) > 65536
+    if words:
+        assert (nb + 63) // 64 > words
     assert_forward_close(got, ref, "mean", x)
     st = got["stats"]
     assert st["tiles"] == keep.size
@@ -181,14 +168,20 @@ def test_neighbouring_blocks_keep_different_k_blocks(N):
     assert row_max_rel(got["dC"], ref["dC_f"]) <= TOL_ROW
 
 
-def test_fully_ignored_batch():
-    """'Correctness': a fully masked batch gives zero loss and finite zero gradients."""
-    w, (E, C, x) = make(W.small("i", 300, 64, 1000))
+@pytest.mark.parametrize("D,filter_eps", [(64, O.FILTER_EPS), (64, 0.0), (256, 0.0)])
+def test_fully_ignored_batch(D, filter_eps):
+    """'Correctness': a fully masked batch gives zero loss and finite zero
+    gradients, with the filter on or off (off, the dC tiles have no K-block
+    at all and nothing marks them as skipped).  D = 256: the gradient GEMM
+    runs as CTA pairs."""
+    w, (E, C, x) = make(W.small("i", 300, D, 1000))
     x = np.full_like(x, -100)
-    got = run_cuda(E, C, x, reduction="mean")
+    got = run_cuda(E, C, x, reduction="mean", filter_eps=filter_eps)
     assert float(got["loss"].reshape(())) == 0.0
     assert np.all(got["dE"] == 0.0) and np.all(got["dC"] == 0.0)
     assert np.all(np.isfinite(got["lse"]))
+    if filter_eps == 0.0:
+        return
     # the autograd path (its forward skips the rows that take part in nothing: all of them here)
     import linear_cross_entropy_gb300 as cce
     Et, Ct, xt = to_device(E, C, x)

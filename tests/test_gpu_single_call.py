@@ -17,7 +17,7 @@ import torch
 
 import cce_workloads as W
 import oracle as O
-from tests.gpu_util import TOL_GRAD, TOL_GRAD_FILTERED, TOL_LSE, bf16_to_f64, rel_fro, to_device
+from tests.gpu_util import TOL_GRAD, TOL_GRAD_FILTERED, TOL_LSE, bf16_to_f64, mixed_survival_inputs, rel_fro, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -61,6 +61,7 @@ CASES = [
     ("three-chunks", W.small("c", 700, 64, 5000), "mean", 256 * 5120 * 2),
     ("split-dE", W.small("s", 512, 128, 20000), "sum", 256 * 20224 * 2),
     ("wide-D", W.small("w", 300, 600, 3000), "mean", 0),
+    ("pairs-split-dE", W.small("p", 700, 256, 20000), "sum", 256 * 20224 * 2),
 ]
 
 
@@ -101,6 +102,26 @@ def test_single_call_filtered_full_width_d_tile():
     assert got["stats"]["skipped"] > keep.size // 2
 
 
+@pytest.mark.parametrize("staging", [0, 256 * 1536 * 2], ids=["one-chunk", "several-chunks"])
+def test_single_call_pairs_with_different_survival(staging):
+    """D = 256: the single call's gradient GEMM as CTA pairs, on inputs whose
+    neighbouring blocks keep different K-blocks (most token-block pairs, and
+    vocabulary blocks 0 and 1), so the pairs run the union and load zeros
+    where their own tile skips; one token chunk or several.  No tile lies
+    within 0.1% of eps (checked on the oracle): the skip count is exact."""
+    N, D, V = 3000, 256, 1500
+    E_bits, C_bits, x = mixed_survival_inputs(N, D, V)
+    got = _run(E_bits, C_bits, x, reduction="mean", filter_eps=O.FILTER_EPS, max_staging_bytes=staging)
+    Ef, Cf = O.from_bits(E_bits, C_bits)
+    ref = O.loss_and_grad(Ef, Cf, x, reduction="mean", filter_eps=O.FILTER_EPS)
+    for eps in (O.FILTER_EPS * (1 - 1e-3), O.FILTER_EPS * (1 + 1e-3)):
+        assert np.array_equal(O.loss_and_grad(Ef, Cf, x, reduction="mean", filter_eps=eps)["keep"], ref["keep"])
+    keep = ref["keep"]
+    assert got["stats"]["tiles"] == keep.size
+    assert got["stats"]["skipped"] == int((~keep).sum()) > 0
+    _check(got, ref, x, TOL_GRAD_FILTERED)
+
+
 def test_single_call_softcap():
     w = W.small("cap", 300, 136, 5000)
     E_bits, C_bits, x = W.make_inputs(w)
@@ -134,10 +155,14 @@ def test_single_call_is_deterministic():
     assert np.array_equal(a["dC"], b["dC"]) and a["stats"] == b["stats"]
 
 
-def test_single_call_fully_ignored_batch():
-    E_bits, C_bits, x = W.make_inputs(W.small("z", 300, 64, 3000))
+@pytest.mark.parametrize("D,filter_eps", [(64, None), (64, 0.0), (256, 0.0)])
+def test_single_call_fully_ignored_batch(D, filter_eps):
+    """Zero loss and gradients with the filter on or off (off, nothing marks
+    the dC tiles, which have no K-block, as skipped); D = 256: CTA pairs."""
+    E_bits, C_bits, x = W.make_inputs(W.small("z", 300, D, 3000))
     x = np.full_like(x, -100)
-    got = _run(E_bits, C_bits, x, reduction="mean", max_staging_bytes=256 * 3072 * 2)
+    kw = {} if filter_eps is None else {"filter_eps": filter_eps}
+    got = _run(E_bits, C_bits, x, reduction="mean", max_staging_bytes=256 * 3072 * 2, **kw)
     assert got["loss"] == 0.0 and np.all(got["lse"] == 0.0)
     assert np.all(got["dE"] == 0.0) and np.all(got["dC"] == 0.0)
     assert got["stats"]["tiles"] == 0
