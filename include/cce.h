@@ -388,6 +388,17 @@ cce_status cce_selftest_pair_timeout(int32_t* dev_err, uint32_t timeout_us, int 
  * meant for production use.  No device work. */
 int cce_selftest_pair_map_words(int words);
 
+/* Test hook of the gradient GEMM's layout.  With D tiles 256 wide the
+ * gradient GEMM can run as CTA pairs (M = 256 over two row blocks, which
+ * run the union of their surviving K-blocks) or one CTA per tile; with the
+ * filter on both are launched and the chunk's count of kept filter tiles
+ * picks one on the device (pairs from 80% kept).  layout = 1 always runs the
+ * pairs where they apply, 2 always one CTA per tile, 0 (or any other value)
+ * restores the choice, for the calls that start after it; returns the
+ * previous setting.  Process-wide; not meant for production use.  No device
+ * work. */
+int cce_selftest_grad_layout(int layout);
+
 /* Human-readable name of a status. */
 const char* cce_status_string(cce_status s);
 

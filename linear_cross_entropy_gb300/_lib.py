@@ -109,6 +109,8 @@ def load() -> ctypes.CDLL:
     lib.cce_selftest_pair_timeout.restype = ctypes.c_int
     lib.cce_selftest_pair_map_words.argtypes = [ctypes.c_int]
     lib.cce_selftest_pair_map_words.restype = ctypes.c_int
+    lib.cce_selftest_grad_layout.argtypes = [ctypes.c_int]
+    lib.cce_selftest_grad_layout.restype = ctypes.c_int
     lib.cce_memory_accounting.argtypes = [i64, i64, i64, ctypes.POINTER(MemoryReport)]
     lib.cce_memory_accounting.restype = ctypes.c_int
     lib.cce_status_string.argtypes = [ctypes.c_int]

@@ -30,11 +30,17 @@ constexpr size_t ALIGN = 256;         // sub-buffer alignment inside a workspace
 constexpr size_t G_CHUNK_BUDGET = size_t(CCE_G_CHUNK_BUDGET_MIB) << 20;  // bytes of the backward G chunk buffer
 constexpr int64_t MIN_CHUNK = 2048, MAX_CHUNK = 65536;
 constexpr int COMBINE_THREADS = 256;
+// per vocabulary or token chunk: the recompute's and the gradient GEMM's
+// scheduler counters, then KEPT_SLOTS counters of kept filter tiles
+constexpr int CHUNK_COUNTERS = 2 + KEPT_SLOTS;
 constexpr size_t ZERO_BOX_BYTES = PAIR_A_BYTES;  // one A operand box of the pair gradient GEMM
 
 std::atomic<uint64_t> g_launches{0};
 // survival words a gradient-GEMM pair's work item carries (a test hook lowers it)
 std::atomic<int> g_pair_words{PAIR_MAP_WORDS};
+// gradient GEMM with the filter on: 0 picks the layout by the kept tiles, 1
+// always runs CTA pairs where they apply, 2 one CTA per tile (a test hook)
+std::atomic<int> g_grad_layout{0};
 
 // ------------------------------------------------------------ small kernels
 // Per row: LSE from the per-split partials (fixed split order), loss, and a
@@ -435,8 +441,8 @@ BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V, bool sort = false, size_t 
   size_t o = 0;
   L.count = o;
   o = align_up(o + sizeof(int), ALIGN);
-  L.counters = o;  // two scheduler counters per chunk
-  o = align_up(o + sizeof(int) * 2 * static_cast<size_t>(L.nchunks), ALIGN);
+  L.counters = o;  // per chunk: the two launches' scheduler counters and the kept filter tiles
+  o = align_up(o + sizeof(int) * CHUNK_COUNTERS * static_cast<size_t>(L.nchunks), ALIGN);
   L.zero = o;  // 16 KiB of zeros: the A box of a CTA pair's skipped K-block
   o = align_up(o + ZERO_BOX_BYTES, ALIGN);
   L.cscr = o;  // compaction scratch
@@ -519,7 +525,7 @@ FlceLayout flce_layout(int64_t N, int64_t D, int64_t V, size_t max_staging) {
     o = align_up(o + bytes, ALIGN);
     return at;
   };
-  L.counters = take(sizeof(int) * 2 * static_cast<size_t>(L.nchunks));
+  L.counters = take(sizeof(int) * CHUNK_COUNTERS * static_cast<size_t>(L.nchunks));
   L.count = take(sizeof(int));
   L.zero = take(ZERO_BOX_BYTES);  // the A box of a CTA pair's skipped K-block
   L.cscr = take(compact_scratch_bytes(N));
@@ -1101,7 +1107,13 @@ cce_status cce_backward_ex2(const void* E, const void* C, const int64_t* x, cons
   // rows and half of the MN-major B tile, K = 128 per stage) when the D tiles
   // are 256 wide and B comes in 3-D boxes: every operand is one 3-D box of
   // two 64-column groups and 128 rows.
-  const bool grad_pairs = pair_clusters > 0 && r.b3d && r.bn == BN;
+  const int layout = g_grad_layout.load();
+  const bool grad_pairs = pair_clusters > 0 && r.b3d && r.bn == BN && layout != 2;
+  // With the filter on, one CTA per tile is launched beside the pairs and the
+  // chunk's kept-tile count picks the one that runs (pairs run the union of
+  // two tiles' K-blocks, which costs more than it saves when many are skipped)
+  const bool dual = grad_pairs && (r.filter_de || r.filter_dc) && layout == 0;
+  GemmArgs rs = r;  // the one-CTA-per-tile layout
   if (grad_pairs) {
     ok &= make_tmap_mn3(&r.tmA, gbuf, vc, N, 2, PAIR_BK);  // dC: 128 vocabulary columns x 128 tokens (K)
     ok &= make_tmap_mn3(&r.tmA2, gbuf, vc, N, 2, BM);      // dE: 128 tokens x two 64-column K-blocks
@@ -1116,7 +1128,7 @@ cce_status cce_backward_ex2(const void* E, const void* C, const int64_t* x, cons
 
   int* counters = reinterpret_cast<int*>(ws + W.counters);
   {
-    cudaError_t e = cudaMemsetAsync(counters, 0, sizeof(int) * 2 * static_cast<size_t>(W.nchunks), s);
+    cudaError_t e = cudaMemsetAsync(counters, 0, sizeof(int) * CHUNK_COUNTERS * static_cast<size_t>(W.nchunks), s);
     if (e != cudaSuccess) return cuda_status(e);
   }
   for (int64_t ch = 0; ch < W.nchunks; ++ch) {
@@ -1130,12 +1142,16 @@ cce_status cce_backward_ex2(const void* E, const void* C, const int64_t* x, cons
     r.dc_rows = sort ? perm + v0 : nullptr;
     r.dC_out = static_cast<uint16_t*>(dC);
     g.v_tiles = static_cast<int>(cdiv(w, BN));
-    g.counter = counters + 2 * ch;
+    g.counter = counters + CHUNK_COUNTERS * ch;
     r.dc_m_tiles = static_cast<int>(cdiv(w, BM));
     r.de_k_blocks = static_cast<int>(cdiv(w, BK));
     r.dc_first = cdiv(N, BK) >= r.de_k_blocks ? 1 : 0;  // longest tiles first
     r.first_chunk = (ch == 0) ? 1 : 0;
-    r.counter = counters + 2 * ch + 1;
+    r.counter = counters + CHUNK_COUNTERS * ch + 1;
+    // filter on: both gradient-GEMM layouts are launched, the kept-tile count
+    // of the chunk's recompute picks the one that runs
+    g.kept_tiles = dual ? counters + CHUNK_COUNTERS * ch + 2 : nullptr;
+    r.kept_tiles = g.kept_tiles;
     cudaError_t e;
     if (sort) {  // the chunk's C rows in sorted order, zero rows up to the last 256-row tile
       PhaseScope ps(6, s);
@@ -1156,11 +1172,24 @@ cce_status cce_backward_ex2(const void* E, const void* C, const int64_t* x, cons
       PhaseScope ps(4, s);
       if (grad_pairs) {
         const int items = ((r.dc_m_tiles + 1) / 2 + (r.n_blocks + 1) / 2) * r.n_tiles;
+        r.grad_path = dual ? 1 : -1;
         e = launch_gemm_pairs(MODE_GRAD, r, std::min(pair_clusters, items), s);
+        g_launches++;
+        if (e == cudaSuccess && dual) {
+          GemmArgs one = r;  // the same chunk, one CTA per tile
+          one.tmA = rs.tmA;
+          one.tmA2 = rs.tmA2;
+          one.tmB = rs.tmB;
+          one.tmB2 = rs.tmB2;
+          one.grad_path = 0;
+          e = launch_gemm(MODE_GRAD, one, std::min(sms, (one.dc_m_tiles + one.n_blocks) * one.n_tiles), s);
+          g_launches++;
+        }
       } else {
+        r.grad_path = -1;
         e = launch_gemm(MODE_GRAD, r, std::min(sms, (r.dc_m_tiles + r.n_blocks) * r.n_tiles), s);
+        g_launches++;
       }
-      g_launches++;
       if (e != cudaSuccess) return cuda_status(e);
     }
   }
@@ -1227,7 +1256,7 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
   const bool multi = W.nchunks > 1;
   {  // the rows that take part, compacted ("Cut Your Losses ...", Table A1: removing ignored tokens)
     PhaseScope ps(2, s);
-    cudaError_t e = cudaMemsetAsync(counters, 0, sizeof(int) * 2 * static_cast<size_t>(W.nchunks), s);
+    cudaError_t e = cudaMemsetAsync(counters, 0, sizeof(int) * CHUNK_COUNTERS * static_cast<size_t>(W.nchunks), s);
     if (e == cudaSuccess && dev_stats) e = cudaMemsetAsync(dev_stats, 0, 2 * sizeof(int64_t), s);
     if (e != cudaSuccess) return cuda_status(e);
     {
@@ -1248,7 +1277,8 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
   const bool b3d = D % 64 == 0;
   // The gradient GEMM as CTA pairs, as in the two-call backward (D tiles 256
   // wide, 3-D boxes; the dE K ranges start at multiples of 128).
-  const bool grad_pairs = pair_clusters > 0 && b3d && W.bn == BN && W.kps % 2 == 0;
+  const int layout = g_grad_layout.load();
+  const bool grad_pairs = pair_clusters > 0 && b3d && W.bn == BN && W.kps % 2 == 0 && layout != 2;
   if (grad_pairs) {
     cudaError_t e = cudaMemsetAsync(ws + W.zero, 0, ZERO_BOX_BYTES, s);
     if (e != cudaSuccess) return cuda_status(e);
@@ -1290,7 +1320,7 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
     f.softcap = softcap;
     f.inv_softcap = softcap > 0.0f ? 1.0f / softcap : 0.0f;
     f.dev_err = dev_err;
-    f.counter = counters + 2 * c;
+    f.counter = counters + CHUNK_COUNTERS * c;
     cudaError_t e;
     {
       PhaseScope ps(0, s);
@@ -1311,9 +1341,11 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
     {  // (3) staged logits -> G-hat (bf16, in place) and the filter votes
       PhaseScope ps(7, s);
       int launched = 0;
+      // the kept-tile count that picks the gradient GEMM's layout (filter on)
+      int* kept = grad_pairs && (filter_de || filter_dc) && layout == 0 ? counters + CHUNK_COUNTERS * c + 2 : nullptr;
       e = launch_gpass(stage, W.Vp, mtile, rows, V, xc + r0, static_cast<long long>(ignore_index), lsec + r0, count,
                        reduction, softcap, filter_eps, !(filter_de && filter_dc), bitmap, bitmapT, W.bm_ld, count, r0,
-                       s, &launched);
+                       kept, s, &launched);
       g_launches += static_cast<uint64_t>(launched);
       if (e != cudaSuccess) return cuda_status(e);
     }
@@ -1340,6 +1372,7 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
     }
     ok = ok && make_tmap(&r.tmOut2, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, deacc, D,
                          static_cast<uint64_t>(W.Sde) * W.slab, D, 32, 32);
+    GemmArgs one = r;  // the one-CTA-per-tile layout (see the two-call backward)
     if (grad_pairs) {  // every operand one 3-D box of two 64-column groups and 128 rows
       ok = ok && make_tmap_mn3(&r.tmA, stage, W.Vp, rows, 2, PAIR_BK) && make_tmap_mn3(&r.tmA2, stage, W.Vp, rows, 2, BM) &&
            make_tmap_mn3(&r.tmB, Ec, D, rows, 2, PAIR_BK) && make_tmap_mn3(&r.tmB2, C, D, V, 2, PAIR_BK) &&
@@ -1378,13 +1411,29 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
     r.dc_reduce = (!last && c > 0) ? 1 : 0;
     r.dc_acc = (last && multi) ? dcacc : nullptr;
     r.dc_first = 2 * nb >= W.kps ? 1 : 0;  // longest tiles first
-    r.counter = counters + 2 * c + 1;
+    r.counter = counters + CHUNK_COUNTERS * c + 1;
     {
       PhaseScope ps(4, s);
       if (grad_pairs) {
+        const bool dual = (filter_de || filter_dc) && layout == 0;
         const int64_t items = ((r.dc_m_tiles + 1) / 2 + (nb + 1) / 2 * W.Sde) * r.n_tiles;
+        r.kept_tiles = dual ? counters + CHUNK_COUNTERS * c + 2 : nullptr;
+        r.grad_path = dual ? 1 : -1;
         e = launch_gemm_pairs(MODE_GRAD, r, static_cast<int>(std::min<int64_t>(pair_clusters, items)), s);
+        if (e == cudaSuccess && dual) {
+          g_launches++;
+          const GemmArgs pr = r;
+          r.tmA = one.tmA;
+          r.tmA2 = one.tmA2;
+          r.tmB = one.tmB;
+          r.tmB2 = one.tmB2;
+          r.grad_path = 0;
+          const int64_t tiles = (r.dc_m_tiles + nb * W.Sde) * r.n_tiles;
+          e = launch_gemm(MODE_GRAD, r, static_cast<int>(std::min<int64_t>(sms, tiles)), s);
+          r = pr;
+        }
       } else {
+        r.grad_path = -1;
         const int64_t items = (r.dc_m_tiles + nb * W.Sde) * r.n_tiles;
         e = launch_gemm(MODE_GRAD, r, static_cast<int>(std::min<int64_t>(sms, items)), s);
       }
@@ -1456,6 +1505,11 @@ cce_status cce_selftest_pair_timeout(int32_t* dev_err, uint32_t timeout_us, int 
 int cce_selftest_pair_map_words(int words) {
   if (words <= 0 || words > PAIR_MAP_WORDS) words = PAIR_MAP_WORDS;
   return g_pair_words.exchange(words);
+}
+
+int cce_selftest_grad_layout(int layout) {
+  if (layout < 0 || layout > 2) layout = 0;
+  return g_grad_layout.exchange(layout);
 }
 
 cce_status cce_profile_enable(int enable) {

@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(256, CAP ? 3 : 4) gpass_kernel(uint16_t* __res
                                                     int reduction, float softcap, float eps, int store_skipped,
                                                     uint8_t* __restrict__ bitmap, uint8_t* __restrict__ bitmapT,
                                                     int bm_ld, int n_blocks, const int* __restrict__ n_dev,
-                                                    int n_row0) {
+                                                    int n_row0, int* __restrict__ kept) {
   __shared__ float s_c[4][128];  // c_row per 32-column chunk of the tile
   __shared__ float s_m[4][128];  // the chunk maxima (softcap slope)
   __shared__ int s_rel[128];     // target column within the tile, or -1
@@ -147,6 +147,7 @@ __global__ void __launch_bounds__(256, CAP ? 3 : 4) gpass_kernel(uint16_t* __res
   if (t == 0) {
     bitmap[static_cast<size_t>(tb) * bm_ld + vt] = keep ? 1 : 0;
     bitmapT[static_cast<size_t>(vt) * n_blocks + tb] = keep ? 1 : 0;
+    if (keep && kept) atomicAdd(kept + (blockIdx.x + blockIdx.y) % KEPT_SLOTS, 1);
   }
 }
 
@@ -238,19 +239,20 @@ int grid_cap(size_t work, int per_block, int cap) {
 cudaError_t launch_gpass(uint16_t* stage, int64_t pitch, const float* mtile, int64_t rows, int64_t V,
                          const int64_t* x, long long ignore_index, const float* lse, const int* count, int reduction,
                          float softcap, float eps, bool store_skipped, uint8_t* bitmap, uint8_t* bitmapT,
-                         int64_t bm_ld, const int* n_dev, int64_t n_row0, cudaStream_t s, int* launches) {
+                         int64_t bm_ld, const int* n_dev, int64_t n_row0, int* kept, cudaStream_t s,
+                         int* launches) {
   const int nb = static_cast<int>((rows + 127) / 128);
   const dim3 grid(static_cast<unsigned>((V + 127) / 128), static_cast<unsigned>(nb));
   if (softcap > 0.0f) {
     gpass_kernel<true><<<grid, 256, 0, s>>>(stage, static_cast<int>(pitch), mtile, static_cast<int>(rows),
                                             static_cast<int>(V), x, ignore_index, lse, count, reduction, softcap, eps,
                                             store_skipped ? 1 : 0, bitmap, bitmapT, static_cast<int>(bm_ld), nb, n_dev,
-                                            static_cast<int>(n_row0));
+                                            static_cast<int>(n_row0), kept);
   } else {
     gpass_kernel<false><<<grid, 256, 0, s>>>(stage, static_cast<int>(pitch), mtile, static_cast<int>(rows),
                                              static_cast<int>(V), x, ignore_index, lse, count, reduction, softcap,
                                              eps, store_skipped ? 1 : 0, bitmap, bitmapT, static_cast<int>(bm_ld), nb,
-                                             n_dev, static_cast<int>(n_row0));
+                                             n_dev, static_cast<int>(n_row0), kept);
   }
   ++*launches;
   return cudaGetLastError();

@@ -997,6 +997,7 @@ struct EpiCtx {
   uint8_t* buf;    // this warp's 8 KiB staging area (two 4 KiB halves)
   int iter;        // tiles processed so far by this warp
   int last_buf;    // staging half read by the most recent bulk group (-1: none)
+  int kept;        // BWD_G: filter tiles this thread found kept
 };
 
 // Before overwriting staging half b: if the most recent bulk group reads b,
@@ -1314,6 +1315,7 @@ __device__ __forceinline__ bool epi_bwd_g(const GemmArgs& a, const SmemLayout& L
       if (vt128 < a.bm_ld) {
         a.bitmap[static_cast<size_t>(t.m) * a.bm_ld + vt128] = keep ? 1 : 0;
         a.bitmapT[static_cast<size_t>(vt128) * a.n_blocks + t.m] = keep ? 1 : 0;
+        e.kept += keep ? 1 : 0;
       }
     }
   }
@@ -1493,6 +1495,7 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& a, const SmemLayou
   e.buf = L.epi + (warp - 2) * EPI_WARP_BYTES;
   e.iter = 0;
   e.last_buf = -1;
+  e.kept = 0;
   FwdState st{NEG_BIG, 0.0f};
   int acc = 0;
   uint32_t acc_phase = 0;
@@ -1531,8 +1534,31 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& a, const SmemLayou
     });
     if (!ok) break;
   }
+  // BWD_G: one add per thread that wrote survival bytes, in a slot of its own
+  if (MODE == MODE_BWD_G && a.kept_tiles && e.kept) atomicAdd(a.kept_tiles + blockIdx.x % KEPT_SLOTS, e.kept);
   if (lane_id() == 0) bulk_wait_all();
   __syncwarp();
+}
+
+// GRAD with the filter on: CTA pairs run the union of two tiles' K-blocks, so
+// they pay off when nearly every filter tile is kept; when many are skipped,
+// one CTA per tile does less work.  Both are launched; this says whether the
+// launch with this kernel's layout is the one that runs (at least 80% of the
+// chunk's filter tiles kept: pairs).
+template <int MODE, bool PAIR>
+__device__ __forceinline__ bool grad_launch_runs(const GemmArgs& a) {
+  if (MODE != MODE_GRAD || a.grad_path < 0) return true;
+  const Dims dm = dims_of<MODE, PAIR>(a);
+  const long long total = static_cast<long long>(dm.nb) * ((a.chunk_w + FILTER_TILE - 1) / FILTER_TILE);
+  // written by the previous launch: plain loads, all in flight at once
+  int v[KEPT_SLOTS];
+#pragma unroll
+  for (int i = 0; i < KEPT_SLOTS; ++i) v[i] = __ldcg(a.kept_tiles + i);
+  long long kept = 0;
+#pragma unroll
+  for (int i = 0; i < KEPT_SLOTS; ++i) kept += v[i];
+  const bool pairs = 5 * kept >= 4 * total;
+  return pairs == (a.grad_path == 1);
 }
 
 // CAP: logit softcapping in the FWD / BWD_G epilogues (a separate
@@ -1540,6 +1566,12 @@ __device__ __forceinline__ void epilogue_loop(const GemmArgs& a, const SmemLayou
 // PAIR: launched as clusters of two CTAs sharing each MMA (M = 256).
 template <int MODE, bool CAP = false, bool PAIR = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1) cce_gemm_kernel(const __grid_constant__ GemmArgs a) {
+  if (MODE == MODE_GRAD && a.grad_path >= 0) {  // one thread reads the counts; every CTA decides alike
+    __shared__ int runs;
+    if (threadIdx.x == 0) runs = grad_launch_runs<MODE, PAIR>(a) ? 1 : 0;
+    __syncthreads();
+    if (!runs) return;  // the other launch does the work
+  }
   extern __shared__ uint8_t smem_raw[];
   SmemLayout L = carve_smem(smem_raw);
   const int warp = static_cast<int>(threadIdx.x >> 5);

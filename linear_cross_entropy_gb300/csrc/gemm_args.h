@@ -33,6 +33,7 @@ constexpr int WORD_SLOTS = 2;
 constexpr int BAR_BYTES = 1792;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_EPI_WARPS * EPI_WARP_BYTES + BAR_BYTES;
 constexpr int FILTER_TILE = 128;  // filter decisions are per 128 tokens x 128 vocab
+constexpr int KEPT_SLOTS = 32;    // kept-tile counters per chunk (spread to keep the atomics apart)
 
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float NEG_BIG = -3.0e38f;  // finite "minus infinity" for the running max
@@ -101,6 +102,13 @@ struct GemmArgs {
   int de_k_blocks;  // ceil(chunk_w / 64)
   int dc_first;     // 1: dC tiles are handed out first (they have the longer K)
   int pair_words;   // GRAD pairs: survival words a work item may carry (1 .. PAIR_MAP_WORDS)
+  // BWD_G: counts the chunk's kept 128 x 128 filter tiles into
+  // kept_tiles[0 .. KEPT_SLOTS) (any slot; the sum is the count).  GRAD with
+  // the filter on is launched twice, as CTA pairs (grad_path = 1) and one CTA
+  // per tile (grad_path = 0); from the count each launch sees whether it is
+  // the one that runs (grad_path = -1: always runs).
+  int* kept_tiles;
+  int grad_path;
   int first_chunk;  // dE: store (1) or reduce-add (0)
   // dynamic scheduling: work items are handed out by atomicAdd on *counter
   int* counter;     // zeroed before the launch

@@ -59,9 +59,10 @@ cudaError_t launch_gather_vocab_rows(const void* src, const int* rows, int64_t c
 cudaError_t launch_gpass(uint16_t* stage, int64_t pitch, const float* mtile, int64_t rows, int64_t V,
                          const int64_t* x, long long ignore_index, const float* lse, const int* count, int reduction,
                          float softcap, float eps, bool store_skipped, uint8_t* bitmap, uint8_t* bitmapT,
-                         int64_t bm_ld, const int* n_dev, int64_t n_row0, cudaStream_t s, int* launches);
+                         int64_t bm_ld, const int* n_dev, int64_t n_row0, int* kept, cudaStream_t s,
+                         int* launches);
 // the chunk has clamp(*n_dev - n_row0, 0, rows) rows (rows when n_dev is null);
-// rows is also the pitch of mtile.
+// rows is also the pitch of mtile.  kept (may be null): counts the kept tiles.
 cudaError_t launch_finalize_de_slabs(const float* acc, int S, int64_t slab, int64_t N, int64_t D, const int* pos,
                                      void* dE, cudaStream_t s, int sms, int* launches);
 cudaError_t launch_stats_add(const uint8_t* bitmap, const int* n_dev, int64_t n_row0, int64_t max_rows,

@@ -214,3 +214,17 @@ def test_pair_map_words_hook(lib):
     finally:
         lib.cce_selftest_pair_map_words(prev)
     assert lib.cce_selftest_pair_map_words(0) == 40
+
+
+def test_grad_layout_hook(lib):
+    """The test hook that forces the gradient GEMM's layout: returns the
+    previous setting; out-of-range values restore the automatic choice (0)."""
+    prev = lib.cce_selftest_grad_layout(1)
+    try:
+        assert prev == 0
+        assert lib.cce_selftest_grad_layout(2) == 1
+        assert lib.cce_selftest_grad_layout(7) == 2
+        assert lib.cce_selftest_grad_layout(-1) == 0
+    finally:
+        lib.cce_selftest_grad_layout(prev)
+    assert lib.cce_selftest_grad_layout(0) == 0

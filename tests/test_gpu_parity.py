@@ -142,10 +142,12 @@ def test_neighbouring_blocks_keep_different_k_blocks(N, words):
     D, V = 256, 1500
     E, C, x = mixed_survival_inputs(N, D, V)
     prev = lib.cce_selftest_pair_map_words(words)
+    prev_layout = lib.cce_selftest_grad_layout(1)  # pairs (the automatic choice takes one CTA per tile here)
     try:
         got = run_cuda(E, C, x, reduction="mean", filter_eps=O.FILTER_EPS)
     finally:
         lib.cce_selftest_pair_map_words(prev)
+        lib.cce_selftest_grad_layout(prev_layout)
     ref = oracle_full(E, C, x, reduction="mean", filter_eps=O.FILTER_EPS)
     Ef, Cf = O.from_bits(E, C)
     w = O.row_weights(x, O.IGNORE_INDEX, "mean", 1.0, int((x != O.IGNORE_INDEX).sum()))
@@ -166,6 +168,28 @@ def test_neighbouring_blocks_keep_different_k_blocks(N, words):
     assert rel_fro(got["dC"], ref["dC_f"]) <= TOL_GRAD
     assert row_max_rel(got["dE"], ref["dE_f"]) <= TOL_ROW
     assert row_max_rel(got["dC"], ref["dC_f"]) <= TOL_ROW
+
+
+@pytest.mark.parametrize("filter_eps", [O.FILTER_EPS, 0.0])
+def test_gradient_layouts_agree_bitwise(filter_eps):
+    """The gradient GEMM as CTA pairs and one CTA per tile accumulate each
+    tile's kept K-blocks in the same order (the K-blocks a pair runs only for
+    the other tile multiply zeros), so dE and dC are the same bits, on inputs
+    whose neighbouring blocks keep different K-blocks; and the automatic
+    choice between the two (by the chunk's kept tiles) agrees as well."""
+    from linear_cross_entropy_gb300 import _lib
+    lib = _lib.load()
+    E, C, x = mixed_survival_inputs(3000, 256, 1500)
+    runs = []
+    for layout in (1, 2, 0):
+        prev = lib.cce_selftest_grad_layout(layout)
+        try:
+            runs.append(run_cuda(E, C, x, reduction="mean", filter_eps=filter_eps))
+        finally:
+            lib.cce_selftest_grad_layout(prev)
+    for other in runs[1:]:
+        assert np.array_equal(runs[0]["dE"], other["dE"]) and np.array_equal(runs[0]["dC"], other["dC"])
+        assert runs[0]["stats"] == other["stats"]
 
 
 @pytest.mark.parametrize("D,filter_eps", [(64, O.FILTER_EPS), (64, 0.0), (256, 0.0)])

@@ -109,9 +109,21 @@ def test_single_call_pairs_with_different_survival(staging):
     vocabulary blocks 0 and 1), so the pairs run the union and load zeros
     where their own tile skips; one token chunk or several.  No tile lies
     within 0.1% of eps (checked on the oracle): the skip count is exact."""
+    from linear_cross_entropy_gb300 import _lib
+    lib = _lib.load()
     N, D, V = 3000, 256, 1500
     E_bits, C_bits, x = mixed_survival_inputs(N, D, V)
-    got = _run(E_bits, C_bits, x, reduction="mean", filter_eps=O.FILTER_EPS, max_staging_bytes=staging)
+    prev = lib.cce_selftest_grad_layout(1)  # pairs (the automatic choice takes one CTA per tile here)
+    try:
+        got = _run(E_bits, C_bits, x, reduction="mean", filter_eps=O.FILTER_EPS, max_staging_bytes=staging)
+        again = _run(E_bits, C_bits, x, reduction="mean", filter_eps=O.FILTER_EPS, max_staging_bytes=staging)
+        lib.cce_selftest_grad_layout(2)
+        single = _run(E_bits, C_bits, x, reduction="mean", filter_eps=O.FILTER_EPS, max_staging_bytes=staging)
+    finally:
+        lib.cce_selftest_grad_layout(prev)
+    # the same bits as one CTA per tile (and as a second run)
+    assert np.array_equal(got["dE"], single["dE"]) and np.array_equal(got["dC"], single["dC"])
+    assert np.array_equal(got["dE"], again["dE"]) and np.array_equal(got["dC"], again["dC"])
     Ef, Cf = O.from_bits(E_bits, C_bits)
     ref = O.loss_and_grad(Ef, Cf, x, reduction="mean", filter_eps=O.FILTER_EPS)
     for eps in (O.FILTER_EPS * (1 - 1e-3), O.FILTER_EPS * (1 + 1e-3)):
