@@ -54,6 +54,8 @@ WORKLOAD_NAMES = {
     "tiny": "tiny CCE head", "qwen": "Qwen2.5-0.5B-shaped head", "gemma": "Gemma-2-2B-shaped head",
     "llama": "Llama-3-8B-shaped head", "long": "long-context filter stress",
     "freq": "Qwen2.5-0.5B-shaped head, frequent tokens scattered",
+    "freq16k": "Qwen2.5-0.5B-shaped head, frequent tokens scattered, 16384 tokens",
+    "freq64k": "Qwen2.5-0.5B-shaped head, frequent tokens scattered, 65536 tokens",
 }
 
 

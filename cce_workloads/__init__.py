@@ -229,13 +229,18 @@ CONFIGS = {
 }
 CONFIG_ORDER = ("tiny", "qwen", "gemma", "llama", "long")
 
-# A supplementary workload (not one of the five above): the Qwen2.5-0.5B head
+# Supplementary workloads (not among the five above): the Qwen2.5-0.5B head
 # shape with the softmax mass on 256 frequent tokens that a random vocabulary
 # order scatters (frequent_token_inputs with scatter=True, unigram=8) -- the
-# case vocabulary sorting is for.
+# case vocabulary sorting is for -- at 4,096 tokens and at 16,384 and 65,536
+# (the sort's cost is per vocabulary, its saving per token).
 SUPPLEMENTARY = {
     "freq": Workload("freq", 4096, 896, 151936, 0.0, "frequent_scattered", ignore_frac=0.05,
                      reduction="mean", filter_modes=("on",)),
+    "freq16k": Workload("freq16k", 16384, 896, 151936, 0.0, "frequent_scattered", ignore_frac=0.05,
+                        reduction="mean", filter_modes=("on",)),
+    "freq64k": Workload("freq64k", 65536, 896, 151936, 0.0, "frequent_scattered", ignore_frac=0.05,
+                        reduction="mean", filter_modes=("on",)),
 }
 ALL_CONFIGS = {**CONFIGS, **SUPPLEMENTARY}
 

@@ -26,7 +26,9 @@
 //              columns), fp32 tiles stored (first chunk) or reduce-added by
 //              TMA (later chunks): one writer per tile per chunk, chunks in
 //              stream order, so the result is deterministic.  K-blocks of
-//              skipped filter tiles are not loaded and issue no MMA.
+//              skipped filter tiles are not loaded and issue no MMA; CTA pairs
+//              run the union of their two tiles' kept K-blocks, loading zeros
+//              as A where a CTA's own tile skips one.
 //
 //   MODE_FWD_STAGE  MODE_FWD whose epilogue also writes each 32-column logit
 //              chunk, minus its per-row max, as fp16 to a staging buffer (and
