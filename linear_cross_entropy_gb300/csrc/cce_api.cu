@@ -1305,10 +1305,11 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
     f.splits = W.S;
     f.v_tiles = static_cast<int>(cdiv(V, BN));
     f.group_n = raster_group(nb, D);
-    // One CTA per tile: as CTA pairs this kernel measured slower (Qwen shape:
-    // 0.702 -> 0.738 ms; Llama: 10.42 -> 10.47 ms), its epilogue's staging
-    // stores being the same per CTA while the pairs add a half-empty last pair.
     f.items = f.n_blocks * f.splits;  // upper bound; the kernel uses the device count
+    // As CTA pairs with 128-deep stages (with 64-deep ones the pairs had
+    // measured slower here: Qwen 0.702 -> 0.738 ms, Llama 10.42 -> 10.47 ms)
+    const bool fpairs = pair_clusters > 0 && D % 64 == 0;
+    if (fpairs && !pair_operands(&f, Ec, rows, C, D, V)) return CCE_ERR_CUDA;
     f.n_dev = count;
     f.n_row0 = static_cast<int>(r0);
     f.x = xc + r0;
@@ -1324,7 +1325,8 @@ cce_status cce_loss_and_grad(const void* E, const void* C, const int64_t* x, int
     cudaError_t e;
     {
       PhaseScope ps(0, s);
-      e = launch_gemm(MODE_FWD_STAGE, f, std::min(f.items, sms), s);
+      e = fpairs ? launch_gemm_pairs(MODE_FWD_STAGE, f, std::min((f.n_blocks + 1) / 2 * f.splits, pair_clusters), s)
+                 : launch_gemm(MODE_FWD_STAGE, f, std::min(f.items, sms), s);
       g_launches++;
       if (e != cudaSuccess) return cuda_status(e);
     }

@@ -48,8 +48,9 @@
 // epilogue warps through a small ring in shared memory, so every CTA stays
 // busy until the work runs out; the longest tiles are handed out first.
 //
-// CTA pairs (template flag PAIR; MODE_FWD always, MODE_BWD_G from 64 token
-// blocks, MODE_GRAD of the two-call backward when the D tiles are 256 wide):
+// CTA pairs (template flag PAIR; MODE_FWD and MODE_FWD_STAGE when D % 64 ==
+// 0, MODE_BWD_G from 64 token blocks, MODE_GRAD when the D tiles are 256 wide
+// and, with the filter on, at least 80% of the chunk's filter tiles are kept):
 // clusters of two CTAs on neighbouring SMs work on a pair of neighbouring row
 // blocks.  Each CTA loads its 128 rows of A and half of the 256-row B tile;
 // the even CTA issues one MMA of M = 256 for both (tcgen05 cta_group::2) and

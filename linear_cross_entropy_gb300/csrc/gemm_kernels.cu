@@ -23,6 +23,8 @@ cudaError_t prepare_gemm_kernels() {
   if ((e = set_smem<MODE_BWD_G, false, true>()) != cudaSuccess) return e;
   if ((e = set_smem<MODE_BWD_G, true, true>()) != cudaSuccess) return e;
   if ((e = set_smem<MODE_GRAD, false, true>()) != cudaSuccess) return e;
+  if ((e = set_smem<MODE_FWD_STAGE, false, true>()) != cudaSuccess) return e;
+  if ((e = set_smem<MODE_FWD_STAGE, true, true>()) != cudaSuccess) return e;
   return set_smem<MODE_GRAD, false>();
 }
 
@@ -64,6 +66,9 @@ cudaError_t launch_gemm_pairs(int mode, const GemmArgs& args, int clusters, cuda
       return cap ? cudaLaunchKernelEx(&cfg, cce_gemm_kernel<MODE_BWD_G, true, true>, args)
                  : cudaLaunchKernelEx(&cfg, cce_gemm_kernel<MODE_BWD_G, false, true>, args);
     case MODE_GRAD: return cudaLaunchKernelEx(&cfg, cce_gemm_kernel<MODE_GRAD, false, true>, args);
+    case MODE_FWD_STAGE:
+      return cap ? cudaLaunchKernelEx(&cfg, cce_gemm_kernel<MODE_FWD_STAGE, true, true>, args)
+                 : cudaLaunchKernelEx(&cfg, cce_gemm_kernel<MODE_FWD_STAGE, false, true>, args);
     default: return cudaErrorInvalidValue;
   }
 }
