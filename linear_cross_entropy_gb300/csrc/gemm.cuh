@@ -640,6 +640,14 @@ __device__ __forceinline__ Tile grad_pair_tile(const GemmArgs& a, const Dims& dm
   return t;
 }
 
+// Width of a gradient-GEMM pair's tile: BN, or 128 for a last D tile of 128
+// columns (D = 896: 3 x 256 + 128), which then runs MMAs of N = 128 instead
+// of multiplying 128 columns of padding.  Each CTA of a pair holds half of N
+// in whole 64-column groups, so narrower remainders keep N = 256.
+__device__ __forceinline__ int pair_tile_n(const GemmArgs& a, const Tile& t) {
+  return a.D - t.n * a.bn == BN / 2 ? BN / 2 : BN;
+}
+
 // Ring entries of the gradient GEMM as CTA pairs: 4 item + kind, -1 when no
 // work is left.  Kinds: RING_NONE, neither tile keeps a K-block; RING_DENSE,
 // both keep every K-block of the range; RING_BITS, the slot's survival words
@@ -751,7 +759,6 @@ __device__ __forceinline__ void producer_loop_grad_pair(const GemmArgs& a, const
   int stage = 0;
   uint32_t phase = 0;
   uint32_t issued_mask = 0, issued_par = 0;
-  const int half = static_cast<int>(rank) * (BN / 2);  // this CTA's columns of the B tile
   const uint32_t full_lead = mapa_shared(smem_u32(&L.full[0]), 0);  // the even CTA's full barriers
   // Loads K-block kb (128 deep) of tile t into the next stage: this CTA's A
   // rows (zeros where `mine` is false) and its half of B, each one 3-D box.
@@ -765,7 +772,8 @@ __device__ __forceinline__ void producer_loop_grad_pair(const GemmArgs& a, const
       mbar_arrive_expect_tx(&L.full[stage], 2 * P::kStageBytes);
     }
     const int k0 = kb * P::kBK;
-    const int bz = (t.n * a.bn + half) >> 6;  // first 64-column group of this CTA's B half
+    // first 64-column group of this CTA's half of the B tile (of N columns)
+    const int bz = (t.n * a.bn + static_cast<int>(rank) * (pair_tile_n(a, t) / 2)) >> 6;
     if (!mine) {
       tma_load_2d_pair(&a.tmZ, fb_lead, sA, 0, 0);
     } else if (t.kind == KIND_DC) {
@@ -895,7 +903,7 @@ __device__ __forceinline__ void mma_loop(const GemmArgs& a, const SmemLayout& L,
       // Operand majorness and tile width of this tile.
       const bool a_mn = (MODE == MODE_GRAD) && t.kind == KIND_DC;
       const bool b_mn = (MODE == MODE_GRAD);
-      const int n = (MODE == MODE_GRAD) ? a.bn : BN;
+      const int n = (MODE == MODE_GRAD) ? (PAIR ? pair_tile_n(a, t) : a.bn) : BN;
       const uint32_t idesc = idesc_bf16(PAIR ? 2 * BM : BM, n, a_mn, b_mn);
       // MN-major: 64-element groups kBK rows apart, a K=16 step is 16 rows;
       // K-major: a K=16 step is 32 bytes of a 128-byte row, and each 64 of K

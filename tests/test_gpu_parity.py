@@ -44,6 +44,7 @@ def test_tiny_config(filter_on):
     (640, 128, 9000),   # several backward chunks
     (300, 448, 3000),   # two gradient D tiles, the second one ragged (192 of 256 columns)
     (260, 600, 2000),   # three gradient D tiles, the last one ragged (88 of 256 columns)
+    (700, 384, 3000),   # D tiles of 256 and 128: CTA pairs run the second with N = 128
 ])
 @pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
 def test_ragged_shapes_unfiltered(N, D, V, reduction):
@@ -170,16 +171,18 @@ def test_neighbouring_blocks_keep_different_k_blocks(N, words):
     assert row_max_rel(got["dC"], ref["dC_f"]) <= TOL_ROW
 
 
+@pytest.mark.parametrize("D", [256, 384])
 @pytest.mark.parametrize("filter_eps", [O.FILTER_EPS, 0.0])
-def test_gradient_layouts_agree_bitwise(filter_eps):
+def test_gradient_layouts_agree_bitwise(filter_eps, D):
     """The gradient GEMM as CTA pairs and one CTA per tile accumulate each
     tile's kept K-blocks in the same order (the K-blocks a pair runs only for
     the other tile multiply zeros), so dE and dC are the same bits, on inputs
     whose neighbouring blocks keep different K-blocks; and the automatic
-    choice between the two (by the chunk's kept tiles) agrees as well."""
+    choice between the two (by the chunk's kept tiles) agrees as well.
+    D = 384: the pairs run the 128-column second D tile with N = 128."""
     from linear_cross_entropy_gb300 import _lib
     lib = _lib.load()
-    E, C, x = mixed_survival_inputs(3000, 256, 1500)
+    E, C, x = mixed_survival_inputs(3000, D, 1500)
     runs = []
     for layout in (1, 2, 0):
         prev = lib.cce_selftest_grad_layout(layout)
