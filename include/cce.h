@@ -402,7 +402,10 @@ int cce_selftest_grad_layout(int layout);
 /* Human-readable name of a status. */
 const char* cce_status_string(cce_status s);
 
-/* ABI version (major * 100 + minor). */
+/* ABI version (major * 100 + minor): 101.  Minor 1 added cce_backward_ex2,
+ * cce_backward_workspace_bytes_ex2, cce_backward_chunk_cols and the
+ * selftest entry points cce_selftest_pair_timeout, cce_selftest_pair_map_words
+ * and cce_selftest_grad_layout; nothing of 1.0 changed. */
 int cce_abi_version(void);
 
 /* Number of kernels this library has launched in this process. */

@@ -708,7 +708,7 @@ using namespace cce;
 
 extern "C" {
 
-int cce_abi_version(void) { return 100; }
+int cce_abi_version(void) { return 101; }
 
 uint64_t cce_kernel_launch_count(void) { return g_launches.load(); }
 

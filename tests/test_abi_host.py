@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.cce_abi_version() == 100
+    assert lib.cce_abi_version() == 101
     for s in range(10):
         assert lib.cce_status_string(s)
 
