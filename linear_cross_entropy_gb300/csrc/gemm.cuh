@@ -1333,12 +1333,42 @@ __device__ __forceinline__ bool epi_bwd_g(const GemmArgs& a, const SmemLayout& L
   return ok;
 }
 
+// An empty output tile's boxes: staging half 0 is zeroed once (`bytes` of
+// it: one 32-row box) and lane 0 stores all nbox boxes of 32 columns from
+// it, x0 + 32 j, one bulk group, instead of staging and waiting box by box.
+// Sparse survival leaves most tiles of a chunk empty, and their zeros are
+// most of what such a launch writes.
+__device__ __forceinline__ void zero_boxes(const CUtensorMap* tm, EpiCtx& e, int x0, int gy, int nbox, int bytes,
+                                           bool reduce) {
+  const uint32_t lane = lane_id();
+  staging_acquire(e, 0);
+  const uint32_t sb = smem_u32(e.buf);
+  for (int o = static_cast<int>(lane) * 16; o < bytes; o += 32 * 16) st_shared_v4(sb + o, 0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    for (int j = 0; j < nbox; ++j) {
+      if (reduce) {
+        tma_reduce_add_2d(tm, e.buf, x0 + 32 * j, gy);
+      } else {
+        tma_store_2d(tm, e.buf, x0 + 32 * j, gy);
+      }
+    }
+    bulk_commit();
+  }
+  e.last_buf = 0;
+}
+
 // fp32 output rows gy .. gy + 31 of tensor map tm, columns x0 .. x0 + 32 * nbox - 1:
 // 32-column boxes (128-byte swizzle) from TMEM, or zeros when the tile is
 // empty; stored, or reduce-added by TMA.
 __device__ __forceinline__ void store_f32_boxes(const CUtensorMap* tm, EpiCtx& e, uint32_t tbase, int x0, int gy,
                                                 int nbox, bool empty, bool reduce) {
   const uint32_t lane = lane_id();
+  if (empty) {  // every box from one zeroed staging half, in one bulk group
+    if (nbox > 0) zero_boxes(tm, e, x0, gy, nbox, 4096, reduce);
+    return;
+  }
 #pragma unroll 1
   for (int j = 0; j < nbox; ++j) {
     const int b = j & 1;
@@ -1395,6 +1425,19 @@ __device__ __forceinline__ void epi_dc(const GemmArgs& a, const Dims& dm, const 
     const int lr = ly + static_cast<int>(lane);
     const bool row_ok = lr < a.chunk_w;
     const size_t grow = row_ok ? static_cast<size_t>(__ldg(a.dc_rows + lr)) : 0;
+    if (empty) {
+      // zeros need no TMEM lane of their own: the warp writes one row at a
+      // time, 16 bytes a lane, each store a contiguous run of the row
+      release_tmem(L, acc);
+      const int rows = min(32, a.chunk_w - ly);
+      const bool col_ok = x0 + 8 * static_cast<int>(lane) < min(a.D, x0 + a.bn);
+#pragma unroll 4
+      for (int i = 0; i < rows; ++i) {
+        const size_t gi = __shfl_sync(0xffffffffu, grow, i);
+        if (col_ok) reinterpret_cast<uint4*>(a.dC_out + gi * a.D + x0)[lane] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      return;
+    }
     uint4* dst = reinterpret_cast<uint4*>(a.dC_out + grow * a.D + x0);
     const int nb = (ly < a.chunk_w) ? min(a.bn / 32, (a.D - x0 + 31) / 32) : 0;
 #pragma unroll 1
@@ -1427,6 +1470,11 @@ __device__ __forceinline__ void epi_dc(const GemmArgs& a, const Dims& dm, const 
   // chunks, read by each lane for its own row, before rounding to bf16
   const int arow = ly + static_cast<int>(lane);
   const float* accrow = (a.dc_acc && arow < a.chunk_w) ? a.dc_acc + static_cast<size_t>(a.c_row0 + arow) * a.D : nullptr;
+  if (empty && !a.dc_acc) {
+    if (nbox > 0) zero_boxes(&a.tmOut, e, x0, gy, nbox, 2048, false);
+    release_tmem(L, acc);
+    return;
+  }
 #pragma unroll 1
   for (int j = 0; j < nbox; ++j) {
     const int b = j & 1;
