@@ -786,7 +786,7 @@ cce_status cce_vocab_order(const float* keys, int64_t V, int32_t* perm, void* wo
   cce_status st = device_check(&sms);
   if (st != CCE_OK) return st;
   int launched = 0;
-  cudaError_t e = launch_vocab_order(keys, V, perm, workspace, static_cast<cudaStream_t>(stream), sms, &launched);
+  cudaError_t e = launch_vocab_order(keys, V, perm, workspace, static_cast<cudaStream_t>(stream), &launched, nullptr);
   g_launches += static_cast<uint64_t>(launched);
   return cuda_status(e);
 }
@@ -1033,9 +1033,9 @@ cce_status cce_backward_ex2(const void* E, const void* C, const int64_t* x, cons
     float* keys = reinterpret_cast<float*>(ws + W.keys);
     void* scr = ws + W.sortscr;
     cudaError_t e = launch_vocab_keys(Ec, N, count, nullptr, 0, D, C, V, keys, scr, s, sms, &launched);
-    if (e == cudaSuccess) e = launch_vocab_order(keys, V, perm, scr, s, sms, &launched);
-    if (e == cudaSuccess)
-      e = launch_remap_targets(perm, V, reinterpret_cast<int*>(ws + W.inv), xc, count, N, s, sms, &launched);
+    int* inv = reinterpret_cast<int*>(ws + W.inv);
+    if (e == cudaSuccess) e = launch_vocab_order(keys, V, perm, scr, s, &launched, inv);
+    if (e == cudaSuccess) e = launch_remap_targets(inv, xc, count, N, s, sms, &launched);
     g_launches += static_cast<uint64_t>(launched);
     if (e != cudaSuccess) return cuda_status(e);
   }

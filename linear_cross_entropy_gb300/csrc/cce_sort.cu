@@ -135,29 +135,39 @@ __device__ __forceinline__ uint32_t ascending_bits(float k) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__global__ void order_init_kernel(const float* __restrict__ keys, int V, uint32_t* __restrict__ bits,
-                                  int* __restrict__ vals) {
-  for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < V; v += gridDim.x * blockDim.x) {
-    bits[v] = ascending_bits(keys[v]);
-    vals[v] = v;
-  }
-}
+// Per-block digit counts: a block holds at most SORT_TILE = 1024 keys, so a
+// count fits 16 bits; a row of 256 counts is 128 words, word w holding digit
+// 2w in its low half and 2w + 1 in its high half (block-major: row b of a
+// pass at hist + 128 b).  One 16-byte load brings a lane eight counts.
+constexpr int HIST_WORDS = 128;
 
-// Radix pass, step 1: per-block digit counts, stored digit-major
-// (hist[digit * nblocks + block]) so that scanning a row gives every block's
-// offset within that digit.
-__global__ void radix_hist_kernel(const uint32_t* __restrict__ keys, int n, int shift, int nblocks,
-                                  int* __restrict__ hist) {
+// Radix sort, launch 1: each block takes SORT_TILE keys, writes their
+// ascending bits and the identity order, and counts the keys' lowest digits
+// into its row of the first pass's counts.  It also zeroes its rows of the
+// later passes' counts, which the passes before them fill with atomics.
+__global__ void radix_init_kernel(const float* __restrict__ keys, int n, uint32_t* __restrict__ hist, int nblocks,
+                                  uint32_t* __restrict__ bits, int* __restrict__ vals) {
   __shared__ int h[256];
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0;
+  const int t = threadIdx.x;
+  h[t] = 0;  // SORT_THREADS == 256 digits
   __syncthreads();
   const int base = blockIdx.x * SORT_TILE;
-  for (int i = threadIdx.x; i < SORT_TILE; i += blockDim.x) {
+  for (int i = t; i < SORT_TILE; i += SORT_THREADS) {
     const int k = base + i;
-    if (k < n) atomicAdd(&h[(keys[k] >> shift) & 0xFF], 1);  // a count: order does not matter
+    if (k < n) {
+      const uint32_t u = ascending_bits(keys[k]);
+      bits[k] = u;
+      vals[k] = k;
+      atomicAdd(&h[u & 0xFF], 1);  // a count: order does not matter
+    }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i * nblocks + blockIdx.x] = h[i];
+  if (t < HIST_WORDS) {
+    const size_t w = static_cast<size_t>(blockIdx.x) * HIST_WORDS + t;
+    const size_t pass_stride = static_cast<size_t>(nblocks) * HIST_WORDS;
+    hist[w] = static_cast<uint32_t>(h[2 * t]) | (static_cast<uint32_t>(h[2 * t + 1]) << 16);
+    for (int p = 1; p < 4; ++p) hist[p * pass_stride + w] = 0u;
+  }
 }
 
 // Exclusive scan of one value per thread over a block of SORT_THREADS
@@ -185,73 +195,115 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* 
   return before + inc - v;
 }
 
-// Radix pass, step 2: block d turns row d of the counts (one count per
-// sort block) into exclusive offsets within digit d, and writes the row's
-// total to totals[d].
-__global__ void radix_scan_kernel(int* __restrict__ hist, int nblocks, int* __restrict__ totals) {
-  __shared__ int warp_sums[SORT_WARPS];
-  int* row = hist + static_cast<size_t>(blockIdx.x) * nblocks;
-  int carry = 0;
-  for (int base = 0; base < nblocks; base += SORT_THREADS) {
-    const int i = base + static_cast<int>(threadIdx.x);
-    const int v = i < nblocks ? row[i] : 0;
-    int tot;
-    const int ex = block_exclusive_scan(v, warp_sums, &tot);
-    if (i < nblocks) row[i] = carry + ex;
-    carry += tot;
-  }
-  if (threadIdx.x == 0) totals[blockIdx.x] = carry;
-}
-
-// Radix pass, step 3: stable scatter.  A block walks its keys in order, 256
-// per round; a key's output position is the first position of its digit
-// (keys of smaller digits) + its block's offset within the digit + keys with
-// that digit in earlier rounds + in earlier warps of this round + in earlier
-// lanes of its warp.
-__global__ void radix_scatter_kernel(const uint32_t* __restrict__ keys, const int* __restrict__ vals, int n,
-                                     int shift, int nblocks, const int* __restrict__ offsets,
-                                     const int* __restrict__ totals, uint32_t* __restrict__ keys_out,
-                                     int* __restrict__ vals_out) {
+// One stable radix pass on digit (key >> shift) & 0xFF, in one launch.
+//  1. Offsets: from the pass's per-block digit counts, every block sums each
+//     digit over all blocks (its total) and over the blocks before it; digit
+//     d starts at the totals of the smaller digits.  Warp w reads the count
+//     rows w, w + 8, ..., each row 512 coalesced bytes, eight digits a lane.
+//     The block's keys and values are loaded first, so their latency
+//     overlaps these reads.
+//  2. Scatter: the block walks its keys in order, 256 per round; a key's
+//     output position is its digit's start + the keys with that digit in
+//     earlier blocks, earlier rounds, earlier warps of this round and earlier
+//     lanes of its warp.
+//  3. The next pass's counts (hist_next, unless this is the last pass): each
+//     key adds one to the count of its next digit in the block that its
+//     output position falls in; lanes with the same target add once,
+//     together.  The counts are integers, so the order of the atomics does
+//     not matter.
+// The last pass may also write inv[value] = position (the inverse order).
+__global__ void radix_pass_kernel(const uint32_t* __restrict__ keys, const int* __restrict__ vals, int n, int shift,
+                                  int nblocks, const uint32_t* __restrict__ hist, uint32_t* __restrict__ hist_next,
+                                  uint32_t* __restrict__ keys_out, int* __restrict__ vals_out, int* __restrict__ inv) {
+  __shared__ int part_tot[SORT_WARPS][256];
+  __shared__ int part_bef[SORT_WARPS][256];
   __shared__ int running[256];
   __shared__ int wcount[SORT_WARPS][256];
   __shared__ int warp_sums[SORT_WARPS];
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  {
-    int tot;
-    const int digit_base = block_exclusive_scan(totals[t], warp_sums, &tot);  // SORT_THREADS == 256 digits
-    running[t] = digit_base + offsets[static_cast<size_t>(t) * nblocks + blockIdx.x];
+  const int blk = static_cast<int>(blockIdx.x);
+  const int base = blk * SORT_TILE;
+  uint32_t kr[SORT_ROUNDS];
+  int vr[SORT_ROUNDS];
+#pragma unroll
+  for (int r = 0; r < SORT_ROUNDS; ++r) {
+    const int k = base + r * SORT_THREADS + t;
+    kr[r] = k < n ? keys[k] : 0u;
+    vr[r] = k < n ? vals[k] : 0;
   }
-  const int base = blockIdx.x * SORT_TILE;
+  {
+    int tot[8], bef[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) tot[j] = bef[j] = 0;
+#pragma unroll 8
+    for (int b = warp; b < nblocks; b += SORT_WARPS) {
+      // written by atomics in the previous launch: read from L2
+      const uint4 q = __ldcg(reinterpret_cast<const uint4*>(hist + static_cast<size_t>(b) * HIST_WORDS) + lane);
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+      const bool earlier = b < blk;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int lo = static_cast<int>(w[i] & 0xFFFFu), hi = static_cast<int>(w[i] >> 16);
+        tot[2 * i] += lo;
+        tot[2 * i + 1] += hi;
+        bef[2 * i] += earlier ? lo : 0;
+        bef[2 * i + 1] += earlier ? hi : 0;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {  // lane's digits: 8 lane .. 8 lane + 7
+      part_tot[warp][8 * lane + j] = tot[j];
+      part_bef[warp][8 * lane + j] = bef[j];
+    }
+  }
+  __syncthreads();
+  {
+    int total = 0, before = 0;
+#pragma unroll
+    for (int w = 0; w < SORT_WARPS; ++w) {
+      total += part_tot[w][t];
+      before += part_bef[w][t];
+    }
+    int all;
+    const int digit_base = block_exclusive_scan(total, warp_sums, &all);  // SORT_THREADS == 256 digits
+    running[t] = digit_base + before;
+  }
+  const int shift_next = shift + 8;
+#pragma unroll
   for (int round = 0; round < SORT_ROUNDS; ++round) {
-    for (int i = t; i < SORT_WARPS * 256; i += blockDim.x) (&wcount[0][0])[i] = 0;
+    for (int i = t; i < SORT_WARPS * 256; i += SORT_THREADS) (&wcount[0][0])[i] = 0;
     __syncthreads();
     const int k = base + round * SORT_THREADS + t;
     const bool live = k < n;
-    const uint32_t key = live ? keys[k] : 0u;
+    const uint32_t key = kr[round];
     const int digit = live ? static_cast<int>((key >> shift) & 0xFF) : 256 + lane;  // dead lanes match nothing
     const unsigned peers = __match_any_sync(0xffffffffu, digit);
     const int rank_in_warp = __popc(peers & ((1u << lane) - 1u));
     if (live && rank_in_warp == 0) wcount[warp][digit] = __popc(peers);
     __syncthreads();
+    int pos = 0;
     if (live) {
-      int pos = running[digit] + rank_in_warp;
+      pos = running[digit] + rank_in_warp;
       for (int w = 0; w < warp; ++w) pos += wcount[w][digit];
+      const int v = vr[round];
       keys_out[pos] = key;
-      vals_out[pos] = vals[k];
+      vals_out[pos] = v;
+      if (inv) inv[v] = pos;
+    }
+    if (hist_next) {
+      const int slot = live ? (pos / SORT_TILE) * 256 + static_cast<int>((key >> shift_next) & 0xFF) : -1 - lane;
+      const unsigned same = __match_any_sync(0xffffffffu, slot);
+      if (live && (same & ((1u << lane) - 1u)) == 0u)  // digit 2w + h: half h of word w
+        atomicAdd(hist_next + (slot >> 1), static_cast<uint32_t>(__popc(same)) << (16 * (slot & 1)));
     }
     __syncthreads();
-    for (int d = t; d < 256; d += blockDim.x) {
+    for (int d = t; d < 256; d += SORT_THREADS) {
       int c = 0;
       for (int w = 0; w < SORT_WARPS; ++w) c += wcount[w][d];
       running[d] += c;
     }
     __syncthreads();
   }
-}
-
-// inv[perm[j]] = j
-__global__ void invert_kernel(const int* __restrict__ perm, int V, int* __restrict__ inv) {
-  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < V; j += gridDim.x * blockDim.x) inv[perm[j]] = j;
 }
 
 // Compact targets -> sorted positions for the n rows that take part; the
@@ -295,8 +347,7 @@ size_t vocab_keys_scratch_bytes(int64_t N, int64_t D) {
 
 size_t vocab_order_scratch_bytes(int64_t V) {
   const int64_t nblocks = cdiv64(V, SORT_TILE);
-  return 3 * align256(static_cast<size_t>(V) * 4) + align256(static_cast<size_t>(256) * nblocks * 4) +
-         align256(256 * 4);
+  return 3 * align256(static_cast<size_t>(V) * 4) + align256(static_cast<size_t>(4) * HIST_WORDS * nblocks * 4);
 }
 
 cudaError_t launch_vocab_keys(const void* E, int64_t N, const int* n_dev, const int64_t* x, long long ignore_index,
@@ -320,8 +371,8 @@ cudaError_t launch_vocab_keys(const void* E, int64_t N, const int* n_dev, const 
   return cudaGetLastError();
 }
 
-cudaError_t launch_vocab_order(const float* keys, int64_t V, int* perm, void* scratch, cudaStream_t s, int sms,
-                               int* launches) {
+cudaError_t launch_vocab_order(const float* keys, int64_t V, int* perm, void* scratch, cudaStream_t s,
+                               int* launches, int* inv) {
   const int n = static_cast<int>(V);
   const int nblocks = static_cast<int>(cdiv64(V, SORT_TILE));
   uint8_t* p = static_cast<uint8_t*>(scratch);
@@ -329,9 +380,9 @@ cudaError_t launch_vocab_order(const float* keys, int64_t V, int* perm, void* sc
   uint32_t* keys_a = reinterpret_cast<uint32_t*>(p);
   uint32_t* keys_b = reinterpret_cast<uint32_t*>(p + vb);
   int* vals_b = reinterpret_cast<int*>(p + 2 * vb);
-  int* hist = reinterpret_cast<int*>(p + 3 * vb);
-  int* totals = reinterpret_cast<int*>(p + 3 * vb + align256(static_cast<size_t>(256) * nblocks * 4));
-  order_init_kernel<<<grid_for(V, 256, sms * 4), 256, 0, s>>>(keys, n, keys_a, perm);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(p + 3 * vb);  // [4 passes][nblocks][HIST_WORDS]
+  const size_t pass_stride = static_cast<size_t>(nblocks) * HIST_WORDS;
+  radix_init_kernel<<<nblocks, SORT_THREADS, 0, s>>>(keys, n, hist, nblocks, keys_a, perm);
   ++*launches;
   // four stable 8-bit passes, ping-ponging between (keys_a, perm) and
   // (keys_b, vals_b); after the fourth the result is back in (keys_a, perm)
@@ -340,22 +391,20 @@ cudaError_t launch_vocab_order(const float* keys, int64_t V, int* perm, void* sc
   uint32_t* kout = keys_b;
   int* vout = vals_b;
   for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 8 * pass;
-    radix_hist_kernel<<<nblocks, SORT_THREADS, 0, s>>>(kin, n, shift, nblocks, hist);
-    radix_scan_kernel<<<256, SORT_THREADS, 0, s>>>(hist, nblocks, totals);
-    radix_scatter_kernel<<<nblocks, SORT_THREADS, 0, s>>>(kin, vin, n, shift, nblocks, hist, totals, kout, vout);
-    *launches += 3;
+    uint32_t* next = pass < 3 ? hist + (pass + 1) * pass_stride : nullptr;
+    radix_pass_kernel<<<nblocks, SORT_THREADS, 0, s>>>(kin, vin, n, 8 * pass, nblocks, hist + pass * pass_stride, next,
+                                                        kout, vout, pass == 3 ? inv : nullptr);
+    ++*launches;
     std::swap(kin, kout);
     std::swap(vin, vout);
   }
   return cudaGetLastError();
 }
 
-cudaError_t launch_remap_targets(const int* perm, int64_t V, int* inv, int64_t* xc, const int* n_dev, int64_t N,
-                                 cudaStream_t s, int sms, int* launches) {
-  invert_kernel<<<grid_for(V, 256, sms * 4), 256, 0, s>>>(perm, static_cast<int>(V), inv);
+cudaError_t launch_remap_targets(const int* inv, int64_t* xc, const int* n_dev, int64_t N, cudaStream_t s, int sms,
+                                 int* launches) {
   remap_targets_kernel<<<grid_for(N, 256, sms * 4), 256, 0, s>>>(xc, n_dev, static_cast<int>(N), inv);
-  *launches += 2;
+  *launches += 1;
   return cudaGetLastError();
 }
 

@@ -40,13 +40,14 @@ size_t vocab_order_scratch_bytes(int64_t V);
 cudaError_t launch_vocab_keys(const void* E, int64_t N, const int* n_dev, const int64_t* x, long long ignore_index,
                               int64_t D, const void* C, int64_t V, float* keys, void* scratch, cudaStream_t s,
                               int sms, int* launches);
-// perm = the stable ascending order of keys (perm[j] = token at position j).
-cudaError_t launch_vocab_order(const float* keys, int64_t V, int* perm, void* scratch, cudaStream_t s, int sms,
-                               int* launches);
-// inv = perm^-1; compact targets xc[k < *n_dev] become sorted positions, the
+// perm = the stable ascending order of keys (perm[j] = token at position j);
+// inv (optional) = perm^-1.  Five launches.
+cudaError_t launch_vocab_order(const float* keys, int64_t V, int* perm, void* scratch, cudaStream_t s,
+                               int* launches, int* inv);
+// Compact targets xc[k < *n_dev] become sorted positions inv[xc[k]], the
 // zero rows padding the last 128-row block get -1.
-cudaError_t launch_remap_targets(const int* perm, int64_t V, int* inv, int64_t* xc, const int* n_dev, int64_t N,
-                                 cudaStream_t s, int sms, int* launches);
+cudaError_t launch_remap_targets(const int* inv, int64_t* xc, const int* n_dev, int64_t N, cudaStream_t s, int sms,
+                                 int* launches);
 // dst[j] = src[rows[j]] (bf16 rows of D) for j < count, zero rows up to total.
 cudaError_t launch_gather_vocab_rows(const void* src, const int* rows, int64_t count, int64_t total, int64_t D,
                                      void* dst, cudaStream_t s, int sms, int* launches);

@@ -91,7 +91,8 @@ def test_sorted_workspace_adds_keys_order_and_two_chunks(lib, N, D, V):
     extra = bs - b
     assert extra >= 12 * V + vc * D * 2
     scratch = lib.cce_vocab_sort_workspace_bytes(N, D, V)
-    assert 12 * V <= scratch <= 12 * V + 4 * (256 * (V // 1024 + 1) + D * (N // 32 + 2)) + 4096
+    # ping-pong keys and values (12 bytes a token), four passes of per-block digit counts
+    assert 12 * V <= scratch <= 12 * V + 4 * (4 * 256 * (V // 1024 + 1) + D * (N // 32 + 2)) + 4096
     assert extra <= 12 * V + scratch + vc * D * 2 + 8 * 256
     assert lib.cce_backward_workspace_bytes_ex(N, D, V, 8) == 0
 
