@@ -54,7 +54,7 @@ def _keys(rng, V):
     return k
 
 
-@pytest.mark.parametrize("V", [1, 7, 1023, 1024, 1025, 5000, 151936])
+@pytest.mark.parametrize("V", [1, 7, 1023, 1024, 1025, 5000, 151936, 256000, 300001])
 def test_order_is_the_stable_ascending_order(V):
     import linear_cross_entropy_gb300 as cce
     rng = np.random.default_rng(V)
